@@ -1,0 +1,15 @@
+"""CPU oracle for the group-head low-rank latent KV cache.
+
+TEST INFRASTRUCTURE ONLY.  This package is a plain, slow, obviously correct
+restatement of what the method computes, written from the method's
+description (PALU — True Low-Rank Latent Storage for Keys and Values; the
+SVDq cache module page; the KIVI quantizer and bit-packing passages of the
+VeloxQuant-MLX blog).  It is used by the tests, by the package's smoke check
+and by the benchmark's CPU-baseline leg.  The product path never imports it,
+and it shares no code with the CUDA path.
+
+Every function pinned by a test against something other than itself (closed
+forms, constructed spectra, library routines, hand-worked cases).  See
+tests/test_oracle_pins.py.
+"""
+from .palu_oracle import *  # noqa: F401,F403
