@@ -1,0 +1,217 @@
+/*
+ * libpalu — group-head low-rank latent KV cache (PALU style) for GB300 (sm_103a).
+ *
+ * The method (page "PALU — True Low-Rank Latent Storage for Keys and Values",
+ * section "How it works"): the KV heads of a layer are split into contiguous
+ * head groups; per group, keys (and separately values) of the prefill are
+ * centred by their mean mu_g and projected on a shared basis V_g (D x r) from
+ * a truncated SVD; the cache stores only the latent codes [S, r], mixed-bit
+ * quantized per (channel, 32-token group) -- the top quarter of channels by
+ * singular value at 4 bits, the rest at 2 bits -- with the asymmetric min/max
+ * quantizer of the blog post "VeloxQuant-MLX 0.8.0 adds KIVI" ("What KIVI
+ * is").  Single-token decode attention runs on the codes directly.
+ *
+ * Conventions for every call:
+ *  - Pointers named as device pointers must point to memory of the current
+ *    CUDA device; the caller allocates and owns all memory.  Host pointers are
+ *    named as such.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous on it unless stated otherwise.
+ *  - A call returns PALU_OK or an error code; palu_last_error() then gives a
+ *    message for the calling thread.  Argument errors are detected on the host
+ *    before anything is launched.  Conditions only the device can see (append
+ *    past capacity while replaying a captured graph, a bounded wait that ran
+ *    out, K/V length mismatch, eigen-solver not converged) set bits of the
+ *    cache's device error word, reported by palu_cache_sync().
+ *  - Supported: head_dim 128, group_size 32, hi_bit 4, lo_bit 2, rank 1..128,
+ *    query heads per KV head 1..8, fp16 inputs.
+ */
+#ifndef PALU_H
+#define PALU_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PALU_OK = 0,
+  PALU_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or configuration */
+  PALU_ERR_UNSUPPORTED = 2,   /* valid by the method but not built here (e.g. head_dim != 128) */
+  PALU_ERR_CAPACITY = 3,      /* append beyond the cache capacity */
+  PALU_ERR_NOT_INITIALIZED = 4,
+  PALU_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+  PALU_ERR_DEVICE = 6         /* a kernel reported an error through the device error word */
+} palu_status;
+
+/* Energy reading for the rank threshold ("retain 90% of singular value
+ * energy", section "Usage"): cumulative sum of singular values (default) or
+ * of squared singular values. */
+enum { PALU_ENERGY_SIGMA = 0, PALU_ENERGY_SIGMA2 = 1 };
+
+/* Which tensor a cache holds; keys and values use different record layouts. */
+enum { PALU_ROLE_KEY = 0, PALU_ROLE_VALUE = 1 };
+
+/* Bits of the device error word. */
+enum {
+  PALU_DEVERR_CAPACITY = 1u,        /* append beyond capacity (nothing written) */
+  PALU_DEVERR_TIMEOUT = 2u,         /* a bounded wait on a copy ran out */
+  PALU_DEVERR_LENGTH_MISMATCH = 4u, /* key and value caches differ in length */
+  PALU_DEVERR_NOT_CONVERGED = 8u    /* eigen-solver hit its sweep limit */
+};
+
+/* Configuration, mirroring the page's KVCacheConfig fields (section "Usage"):
+ * palu_rank, palu_energy_threshold, palu_n_head_groups, palu_hi_bit,
+ * palu_lo_bit, palu_hi_fraction, palu_group_size, palu_quantize_values. */
+typedef struct {
+  int32_t head_dim;          /* D; must be 128 */
+  int32_t n_head_groups;     /* KV heads are split into this many contiguous groups */
+  int32_t rank;              /* > 0: explicit rank; 0: rank from energy_threshold */
+  int32_t energy_mode;       /* PALU_ENERGY_SIGMA or PALU_ENERGY_SIGMA2 */
+  double energy_threshold;   /* fraction of energy retained, (0, 1] */
+  double hi_fraction;        /* fraction of channels (by singular value) at hi_bit: n_hi = ceil(f*r) */
+  int32_t hi_bit;            /* 4 */
+  int32_t lo_bit;            /* 2 */
+  int32_t group_size;        /* tokens per quantization group: 32 */
+  int32_t quantize;          /* 1: mixed-bit codes; 0: fp16 latents (value caches only) */
+} palu_config;
+
+/* A cache for one tensor (K or V) of one layer.  Plain data: copying it
+ * copies the description, not the device buffers.  Fill it with
+ * palu_cache_init(); do not edit fields afterwards. */
+typedef struct {
+  int32_t magic;
+  int32_t role;
+  int32_t head_dim, rank, n_hi, n_groups, heads_per_group, quantize;
+  int32_t batch, kv_heads;
+  int32_t n_hi_oct, n_lo_oct, n_oct, record_bytes;
+  int64_t capacity;          /* tokens */
+  int64_t n_blk_cap;         /* 32-token block records per stream */
+  void* blocks;              /* device [batch, kv_heads, n_blk_cap, record_bytes] */
+  float* tail;               /* device [batch, kv_heads, 32, rank] fp32 (quantized caches) */
+  void* state;               /* device state: length, error word, basis, mean */
+  int64_t length;            /* tokens appended through this descriptor (host count) */
+} palu_cache;
+
+typedef struct {
+  int64_t length;            /* tokens per stream */
+  int32_t rank, n_hi;
+  double code_bytes;         /* packed code bits of the real channels of full blocks / 8 */
+  double meta_bytes;         /* fp16 scale+zero of the real channels of full blocks */
+  double tail_bytes;         /* fp32 latents of the partial block (fp16 latents if unquantized) */
+  double record_bytes;       /* bytes of block records in use, including channel padding */
+  double basis_bytes;        /* V_g and mu_g of all groups, fp32 */
+  double fp16_bytes;         /* what the [S, D] fp16 tensor would take */
+  double effective_bits;     /* code bits per element: (n_hi*hi_bit + (r-n_hi)*lo_bit)/D, 16r/D unquantized */
+  double bits_with_meta;     /* including scale/zero metadata */
+} palu_stats;
+
+/* Message for the last error on the calling thread ("" if none). */
+const char* palu_last_error(void);
+
+/* Library version string. */
+const char* palu_version(void);
+
+/* Fill cfg with the page's defaults: head_dim 128, 4 groups, energy
+ * threshold 0.90 (sigma reading), 4/2 bits, hi_fraction 0.25, group 32,
+ * quantized values. */
+palu_status palu_config_default(palu_config* cfg);
+
+/* Device workspace needed by palu_fit for x of [batch, kv_heads, seq, D]. */
+palu_status palu_fit_workspace_size(const palu_config* cfg, int64_t batch, int32_t kv_heads,
+                                    int64_t seq, size_t* bytes);
+
+/* Fit the group bases of one tensor of one layer from its prefill
+ * (section "How it works", prefill steps 1-3).
+ *   x        device fp16 [batch, kv_heads, seq, D], contiguous, 16-byte aligned.
+ *   basis    device fp32 [n_groups, D, D]: basis[g, d, j] is entry d of
+ *            direction j; directions sorted by descending singular value,
+ *            each with its largest-magnitude entry positive.
+ *   mu       device fp32 [n_groups, D]: per-group mean of the stacked rows.
+ *   eigvals  device fp64 [n_groups, D]: squared singular values, descending.
+ *   rank_out host int32: r = minimum over groups of the selected rank.
+ *   group_ranks host int32 [n_groups] (may be NULL): rank selected per group.
+ * Rows of group g are all (batch, head in group, token) triples.  The centred
+ * Gram matrix is built on tensor cores and reduced in fp64; a one-block
+ * cyclic Jacobi solver diagonalises it.  This call synchronises `stream` once
+ * (the rank is needed on the host to size the cache). */
+palu_status palu_fit(const palu_config* cfg, const void* x, int64_t batch, int32_t kv_heads,
+                     int64_t seq, void* workspace, size_t workspace_bytes, float* basis,
+                     float* mu, double* eigvals, int32_t* rank_out, int32_t* group_ranks,
+                     void* stream);
+
+/* Byte sizes of the three device buffers of a cache (all 256-byte aligned
+ * sizes): block records, fp32 tail (0 for unquantized values) and state. */
+palu_status palu_cache_size(const palu_config* cfg, int32_t role, int32_t rank, int64_t batch,
+                            int32_t kv_heads, int64_t capacity, size_t* block_bytes,
+                            size_t* tail_bytes, size_t* state_bytes);
+
+/* Initialise an empty cache (length 0) on caller-owned buffers.
+ *   basis    device fp32 [n_groups, D, basis_ld]; columns 0..rank-1 of each
+ *            group are used (e.g. palu_fit's output with basis_ld = D).
+ *   mu       device fp32 [n_groups, D].
+ *   blocks, tail, state: device buffers of at least the sizes given by
+ *            palu_cache_size, 256-byte aligned; tail may be NULL when the
+ *            cache is unquantized.
+ * The basis and mean are copied into `state`; the caller may free them after
+ * the call has completed on `stream`. */
+palu_status palu_cache_init(palu_cache* cache, const palu_config* cfg, int32_t role, int32_t rank,
+                            int64_t batch, int32_t kv_heads, int64_t capacity, const float* basis,
+                            int32_t basis_ld, const float* mu, void* blocks, void* tail,
+                            void* state, void* stream);
+
+/* Project `tokens` new tokens into the stored bases, quantize and append
+ * (prefill steps 4-5 when the cache is empty; decode steps 1-2 afterwards).
+ *   x  device fp16 [batch, kv_heads, tokens, D], contiguous, 16-byte aligned.
+ * Latents are computed to fp32 accuracy, (x - mu_g) V_g.  A 32-token block is
+ * quantized when its last token arrives; until then its latents wait
+ * unquantized in the tail, so appending one token at a time stores exactly the
+ * codes of one long append.  Reads and advances the device-side length, so a
+ * captured graph of appends stays correct when replayed. */
+palu_status palu_encode_append(palu_cache* cache, const void* x, int64_t tokens, void* stream);
+
+/* Device workspace needed by palu_decode_attn. */
+palu_status palu_decode_workspace_size(const palu_cache* k, const palu_cache* v, int32_t q_heads,
+                                       size_t* bytes);
+
+/* Single-token decode attention over the latent cache (decode step 3),
+ * computed from the packed codes without reconstructing K or V:
+ *   scores_t = softmax_scale * (q~ . L^K_t + q . mu^K),  q~ = q V^K
+ *   out      = (sum_t p_t L^V_t / sum_t p_t) (V^V)^T + mu^V
+ * over every cached token, including the one appended this step.
+ *   q    device fp16 [batch, q_heads, D]; query head h reads KV head
+ *        h / (q_heads / kv_heads).
+ *   out  device [batch, q_heads, D], fp32 if out_fp32 else fp16.
+ *   softmax_scale 0 selects 1/sqrt(D).
+ * k and v must have the same batch, kv_heads and length. */
+palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v, const void* q,
+                             int32_t q_heads, float softmax_scale, void* out, int32_t out_fp32,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Byte accounting of a cache (section "Evidence": compressed bytes against
+ * fp16 bytes; section "Effective bit-width").  Host only. */
+palu_status palu_cache_stats(const palu_cache* cache, palu_stats* stats);
+
+/* Synchronise `stream`, read the device length and error word, update
+ * cache->length and clear the error word.  Returns PALU_ERR_DEVICE (with the
+ * bits in the message and in *device_error if not NULL) when it was set. */
+palu_status palu_cache_sync(palu_cache* cache, uint32_t* device_error, void* stream);
+
+/* Comparator: plain split-K decode attention on uncompressed fp16 K and V
+ * (the dense baseline the latent cache is measured against).
+ *   k, v  device fp16 [batch, kv_heads, seq_cap, D]; tokens 0..seq-1 are used.
+ *   q     device fp16 [batch, q_heads, D];  out as in palu_decode_attn. */
+palu_status palu_fp16_decode_workspace_size(int64_t batch, int32_t kv_heads, int64_t seq_cap,
+                                            int32_t q_heads, size_t* bytes);
+palu_status palu_fp16_decode_attn(const void* k, const void* v, int64_t batch, int32_t kv_heads,
+                                  int64_t seq, int64_t seq_cap, const void* q, int32_t q_heads,
+                                  float softmax_scale, void* out, int32_t out_fp32,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PALU_H */

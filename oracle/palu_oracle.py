@@ -505,8 +505,9 @@ class OracleCache:
         D = self.V.shape[1]
         n_tok = self.B * self.Hkv * self.length
         if self.quantize:
+            # codes exist for full blocks only; the partial block is held unquantized
             code_bits = self.n_hi * self.hi_bit + (self.r - self.n_hi) * self.lo_bit
-            code_bytes = n_tok * code_bits / 8.0
+            code_bytes = self.B * self.Hkv * (self.length // BLOCK) * BLOCK * code_bits / 8.0
             meta_bytes = (self.length // BLOCK) * self.B * self.Hkv * self.r * 4
             tail_bytes = (self.length % BLOCK) * self.B * self.Hkv * self.r * 4
         else:

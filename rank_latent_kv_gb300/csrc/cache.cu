@@ -1,0 +1,525 @@
+// Cache set-up and the encode/append kernel.
+//
+// Method (page "PALU — True Low-Rank Latent Storage for Keys and Values",
+// "How it works"): prefill steps 4-5 and decode steps 1-2 -- project new
+// tokens into the stored group basis, L = (x - mu_g) V_g, then mixed-bit
+// quantize per (channel, 32-token group) with the asymmetric min/max
+// quantizer (blog post "VeloxQuant-MLX 0.8.0 adds KIVI", "What KIVI is") and
+// pack the codes LSB-first (blog post "How I built VeloxQuant-MLX", "The
+// Bit-Packing Problem").
+#include <math.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "palu_internal.cuh"
+
+namespace palu {
+
+// ------------------------------------------------------------------ init
+// One CTA per (group, direction j): copies column j of the caller's basis to
+// row j of basisT, and forms mu_g . V_g[:, j] in fp64, stored as a float pair.
+__global__ void cache_init_kernel(const float* __restrict__ basis, int ld, const float* __restrict__ mu,
+                                  float* basisT, float* mu_out, float2* mv, StateHeader* hdr, int r) {
+  const int g = blockIdx.y, j = blockIdx.x, d = threadIdx.x;
+  __shared__ double red[kHeadDim];
+  const float vj = basis[((size_t)g * kHeadDim + d) * ld + j];
+  basisT[((size_t)g * r + j) * kHeadDim + d] = vj;
+  const float m = mu[(size_t)g * kHeadDim + d];
+  if (j == 0) mu_out[(size_t)g * kHeadDim + d] = m;
+  red[d] = (double)m * (double)vj;
+  __syncthreads();
+  for (int s = kHeadDim / 2; s > 0; s >>= 1) {
+    if (d < s) red[d] += red[d + s];
+    __syncthreads();
+  }
+  if (d == 0) {
+    const double t = red[0];
+    const float hi = (float)t;
+    mv[(size_t)g * r + j] = make_float2(hi, (float)(t - (double)hi));
+  }
+  if (g == 0 && j == 0 && d == 0) {
+    hdr->length = 0;
+    hdr->err = 0;
+    hdr->ticket = 0;
+  }
+}
+
+// ------------------------------------------------------------------ encode
+// Shared-memory plan of one encode CTA (one 32-token block of one stream).
+struct EncodeSmem {
+  int xs_off, basis_off, lat_off, codes_off, sz_off, rec_off, total;
+};
+
+__host__ __device__ inline int align16(int x) { return (x + 15) / 16 * 16; }
+
+__host__ __device__ inline EncodeSmem encode_smem(int r, int rec_bytes) {
+  EncodeSmem s;
+  s.xs_off = 0;                                                        // half [32][128]
+  s.basis_off = s.xs_off + kBlock * kHeadDim * 2;                      // float [r][129]
+  s.lat_off = s.basis_off + align16(4 * r * (kHeadDim + 1));           // float [32][r+1]
+  s.codes_off = s.lat_off + align16(4 * kBlock * (r + 1));             // u8 [32][r]
+  s.sz_off = s.codes_off + align16(kBlock * r);                        // half2 [r] (scale, zero)
+  s.rec_off = s.sz_off + align16(4 * r);                               // record
+  s.total = s.rec_off + align16(rec_bytes);
+  return s;
+}
+
+// Position of code (t, j) inside a quantized record: byte offset and shift.
+// Mirrors the layout definition: channel j -> (octet, slot); (token, slot)
+// -> (lane, field k, half); 4-bit octets are u32 words per lane, 2-bit octets
+// u16 halfwords per lane (paired), LSB-first fields.
+__device__ __forceinline__ void code_pos(int role, int n_hi, int n_hi_oct, int n_lo_oct, int t, int j, int& byte,
+                                         int& shift) {
+  int octet, slot;
+  if (j < n_hi) {
+    octet = j >> 3;
+    slot = j & 7;
+  } else {
+    const int jj = j - n_hi;
+    octet = n_hi_oct + (jj >> 3);
+    slot = jj & 7;
+  }
+  const int k = 2 * (t >> 4) + ((t & 15) >> 3);
+  int g, c, half;
+  if (role == PALU_ROLE_KEY) {
+    g = t & 7;
+    c = slot >> 1;
+    half = slot & 1;
+  } else {
+    g = slot;
+    c = (t & 7) >> 1;
+    half = t & 1;
+  }
+  const int lane = 4 * g + c;
+  int unit, bit;
+  if (octet < n_hi_oct) {
+    unit = 128 * octet + 4 * lane;
+    bit = 4 * k + 16 * half;
+  } else {
+    const int lo = octet - n_hi_oct;
+    const int npair = n_lo_oct >> 1;
+    unit = 128 * n_hi_oct + (lo < 2 * npair ? 128 * (lo >> 1) + 4 * lane + 2 * (lo & 1) : 128 * npair + 2 * lane);
+    bit = 2 * k + 8 * half;
+  }
+  byte = unit + (bit >> 3);
+  shift = bit & 7;
+}
+
+__device__ __forceinline__ int latent_off(int t, int j) {
+  const int octet = j >> 3, slot = j & 7;
+  const int k = 2 * (t >> 4) + ((t & 15) >> 3);
+  const int lane = 4 * slot + ((t & 7) >> 1);
+  return 512 * octet + 16 * lane + 4 * k + 2 * (t & 1);
+}
+
+// grid (blocks touched, kv_heads, batch), 128 threads.
+__global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const __half* __restrict__ x,
+                                                            long long T, int Hkv) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int r = cv.r;
+  const EncodeSmem L = encode_smem(r, cv.rec_bytes);
+  __half* xs = reinterpret_cast<__half*>(smem + L.xs_off);
+  float* bas = reinterpret_cast<float*>(smem + L.basis_off);
+  float* lat = reinterpret_cast<float*>(smem + L.lat_off);
+  uint8_t* codes = smem + L.codes_off;
+  __half2* sz = reinterpret_cast<__half2*>(smem + L.sz_off);
+  uint8_t* rec = smem + L.rec_off;
+
+  const int tid = threadIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const long long p0 = __ldcg(&cv.hdr->length);
+  const long long p1 = p0 + T;
+  const unsigned int n_cta = gridDim.x * gridDim.y * gridDim.z;
+
+  if (p1 > cv.capacity) {
+    if (blockIdx.x == 0 && h == 0 && b == 0 && tid == 0) set_dev_error(cv.hdr, PALU_DEVERR_CAPACITY);
+    return;  // nothing written, length unchanged (no CTA takes a ticket)
+  }
+
+  const long long blk = p0 / kBlock + blockIdx.x;
+  const long long lo = blk * kBlock;
+  if (lo < p1) {
+    const long long new_lo = lo > p0 ? lo : p0;
+    const long long hi = (lo + kBlock < p1) ? lo + kBlock : p1;
+    const int off_new = (int)(new_lo - lo);
+    const int n_new = (int)(hi - new_lo);
+    const bool complete = (hi - lo) == kBlock;
+    const int grp = h / cv.heads_per_group;
+
+    // stage the new tokens' rows and the group basis
+    const __half* xsrc = x + (((long long)b * Hkv + h) * T + (new_lo - p0)) * kHeadDim;
+    for (int i = tid; i < n_new * (kHeadDim / 8); i += blockDim.x) {
+      const int t = i / (kHeadDim / 8), q = i % (kHeadDim / 8);
+      reinterpret_cast<uint4*>(xs + (off_new + t) * kHeadDim)[q] =
+          reinterpret_cast<const uint4*>(xsrc + (long long)t * kHeadDim)[q];
+    }
+    const float* bsrc = cv.basisT + (size_t)grp * r * kHeadDim;
+    for (int i = tid; i < r * (kHeadDim / 4); i += blockDim.x) {
+      const int j = i / (kHeadDim / 4), q = i % (kHeadDim / 4);
+      const float4 v = reinterpret_cast<const float4*>(bsrc + (size_t)j * kHeadDim)[q];
+      float* dst = bas + j * (kHeadDim + 1) + 4 * q;
+      dst[0] = v.x;
+      dst[1] = v.y;
+      dst[2] = v.z;
+      dst[3] = v.w;
+    }
+    __syncthreads();
+
+    // projection: warp w takes tokens off_new + w + 4i, lane takes channels lane + 32k.
+    // Each (token, channel) latent is sum_d x_d V_dj accumulated as an
+    // unevaluated float pair (error-free products and sums), minus mu_g.V_g[:, j],
+    // then rounded once to fp32.
+    {
+      const int warp = tid >> 5, lane = tid & 31;
+      float S[8][4], E[8][4];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) S[i][k] = E[i][k] = 0.f;
+      const int nt = (n_new - warp + 3) / 4;  // tokens of this warp (may be <= 0)
+      for (int d = 0; d < kHeadDim; ++d) {
+        float v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int j = lane + 32 * k;
+          v[k] = j < r ? bas[j * (kHeadDim + 1) + d] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (i < nt) {
+            const float xv = __half2float(xs[(off_new + warp + 4 * i) * kHeadDim + d]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float pp, pe, s2, se;
+              two_prod(xv, v[k], pp, pe);
+              two_sum(S[i][k], pp, s2, se);
+              S[i][k] = s2;
+              E[i][k] = __fadd_rn(E[i][k], __fadd_rn(se, pe));
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = lane + 32 * k;
+        if (j < r) {
+          const float2 m = cv.mv[(size_t)grp * r + j];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (i < nt) {
+              float a, ae;
+              two_sum(S[i][k], -m.x, a, ae);
+              const float low = __fadd_rn(__fsub_rn(E[i][k], m.y), ae);
+              lat[(off_new + warp + 4 * i) * (r + 1) + j] = __fadd_rn(a, low);
+            }
+          }
+        }
+      }
+    }
+
+    const long long rec_index = ((long long)b * Hkv + h) * cv.n_blk_cap + blk;
+    uint8_t* gdst = cv.blocks + rec_index * cv.rec_bytes;
+    float* tail = cv.quantize ? cv.tail + ((long long)b * Hkv + h) * kBlock * r : nullptr;
+
+    if (cv.quantize) {
+      if (complete) {
+        // earlier tokens of this block come from the tail
+        for (int i = tid; i < off_new * r; i += blockDim.x) {
+          const int t = i / r, j = i % r;
+          lat[t * (r + 1) + j] = tail[t * r + j];
+        }
+        for (int i = tid; i < cv.rec_bytes / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(rec)[i] = 0u;
+        __syncthreads();
+        // quantize: one thread per channel
+        for (int j = tid; j < r; j += blockDim.x) {
+          float mn = lat[j], mx = lat[j];
+          for (int t = 1; t < kBlock; ++t) {
+            const float v = lat[t * (r + 1) + j];
+            mn = fminf(mn, v);
+            mx = fmaxf(mx, v);
+          }
+          const int bits = j < cv.n_hi ? 4 : 2;
+          const float qmax = (float)((1 << bits) - 1);
+          const float scale = __fdiv_rn(__fsub_rn(mx, mn), qmax);
+          const __half sh = __float2half_rn(scale);
+          const __half zh = __float2half_rn(mn);
+          const float s32 = __half2float(sh), z32 = __half2float(zh);
+          sz[j] = __halves2half2(sh, zh);
+          for (int t = 0; t < kBlock; ++t) {
+            float q = 0.f;
+            if (s32 != 0.f) {
+              q = rintf(__fdiv_rn(__fsub_rn(lat[t * (r + 1) + j], z32), s32));
+              q = fminf(fmaxf(q, 0.f), qmax);
+            }
+            codes[t * r + j] = (uint8_t)q;
+          }
+        }
+        __syncthreads();
+        // pack codes (each byte assembled by the thread owning it: fields are disjoint)
+        for (int i = tid; i < kBlock * r; i += blockDim.x) {
+          const int t = i / r, j = i % r;
+          int byte, shift;
+          code_pos(cv.role, cv.n_hi, cv.n_hi_oct, cv.n_lo_oct, t, j, byte, shift);
+          atomicOr(reinterpret_cast<unsigned int*>(rec + (byte & ~3)), (unsigned int)codes[i] << (8 * (byte & 3) + shift));
+        }
+        // scale / zero per padded channel
+        const int n_pad = 8 * cv.n_oct;
+        const int szb = 128 * cv.n_hi_oct + 64 * cv.n_lo_oct;
+        __half* r16 = reinterpret_cast<__half*>(rec + szb);
+        for (int pch = tid; pch < n_pad; pch += blockDim.x) {
+          const int j = padded_to_channel(pch, r, cv.n_hi, cv.n_hi_oct, 1);
+          const __half2 v = j >= 0 ? sz[j] : __halves2half2(__float2half(0.f), __float2half(0.f));
+          if (cv.role == PALU_ROLE_KEY) {
+            r16[pch] = __low2half(v);
+            r16[n_pad + pch] = __high2half(v);
+          } else {
+            r16[2 * pch] = __low2half(v);
+            r16[2 * pch + 1] = __high2half(v);
+          }
+        }
+        __syncthreads();
+        for (int i = tid; i < cv.rec_bytes / 16; i += blockDim.x)
+          reinterpret_cast<uint4*>(gdst)[i] = reinterpret_cast<const uint4*>(rec)[i];
+      } else {
+        __syncthreads();
+        for (int i = tid; i < n_new * r; i += blockDim.x) {
+          const int t = off_new + i / r, j = i % r;
+          tail[t * r + j] = lat[t * (r + 1) + j];
+        }
+      }
+    } else {
+      // fp16 latents: read-modify-write the block record
+      if (off_new > 0) {
+        for (int i = tid; i < cv.rec_bytes / 16; i += blockDim.x)
+          reinterpret_cast<uint4*>(rec)[i] = reinterpret_cast<const uint4*>(gdst)[i];
+      } else {
+        for (int i = tid; i < cv.rec_bytes / 16; i += blockDim.x)
+          reinterpret_cast<uint4*>(rec)[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncthreads();
+      for (int i = tid; i < n_new * r; i += blockDim.x) {
+        const int t = off_new + i / r, j = i % r;
+        *reinterpret_cast<__half*>(rec + latent_off(t, j)) = __float2half_rn(lat[t * (r + 1) + j]);
+      }
+      __syncthreads();
+      for (int i = tid; i < cv.rec_bytes / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(gdst)[i] = reinterpret_cast<const uint4*>(rec)[i];
+    }
+  }
+
+  // the last CTA to finish publishes the new length
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned int t = atomicAdd(&cv.hdr->ticket, 1u);
+    if (t == n_cta - 1) {
+      cv.hdr->length = p1;
+      cv.hdr->ticket = 0u;
+      __threadfence();
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host
+static int64_t n_hi_of(const palu_config* cfg, int r) {
+  const double v = ceil(cfg->hi_fraction * (double)r - 1e-9);
+  return std::max<int64_t>(0, std::min<int64_t>(r, (int64_t)v));
+}
+
+static palu_status check_config(const palu_config* cfg) {
+  if (!cfg) return fail(PALU_ERR_INVALID_ARG, "config is NULL");
+  if (cfg->head_dim != kHeadDim) return fail(PALU_ERR_UNSUPPORTED, "head_dim must be 128");
+  if (cfg->group_size != kBlock) return fail(PALU_ERR_UNSUPPORTED, "group_size must be 32");
+  if (cfg->hi_bit != 4 || cfg->lo_bit != 2) return fail(PALU_ERR_UNSUPPORTED, "hi_bit must be 4 and lo_bit 2");
+  if (!(cfg->hi_fraction >= 0.0 && cfg->hi_fraction <= 1.0))
+    return fail(PALU_ERR_INVALID_ARG, "hi_fraction must be in [0, 1]");
+  if (cfg->n_head_groups < 1) return fail(PALU_ERR_INVALID_ARG, "n_head_groups must be >= 1");
+  return PALU_OK;
+}
+
+struct Geometry {
+  int n_hi, n_hi_oct, n_lo_oct, n_oct, rec_bytes;
+};
+
+static Geometry geometry(const palu_config* cfg, int role, int r) {
+  Geometry g;
+  const bool quant = cfg->quantize || role == PALU_ROLE_KEY;
+  if (quant) {
+    g.n_hi = (int)n_hi_of(cfg, r);
+    g.n_hi_oct = (g.n_hi + 7) / 8;
+    g.n_lo_oct = (r - g.n_hi + 7) / 8;
+    g.n_oct = g.n_hi_oct + g.n_lo_oct;
+    g.rec_bytes = 128 * g.n_hi_oct + 64 * g.n_lo_oct + 4 * 8 * g.n_oct;
+  } else {
+    g.n_hi = 0;
+    g.n_hi_oct = g.n_lo_oct = 0;
+    g.n_oct = (r + 7) / 8;
+    g.rec_bytes = 512 * g.n_oct;
+  }
+  return g;
+}
+
+static palu_status check_cache_args(const palu_config* cfg, int32_t role, int32_t rank, int64_t batch,
+                                    int32_t kv_heads, int64_t capacity) {
+  palu_status st = check_config(cfg);
+  if (st != PALU_OK) return st;
+  if (role != PALU_ROLE_KEY && role != PALU_ROLE_VALUE) return fail(PALU_ERR_INVALID_ARG, "role must be KEY or VALUE");
+  if (role == PALU_ROLE_KEY && !cfg->quantize)
+    return fail(PALU_ERR_INVALID_ARG, "quantize=0 (fp16 latents) applies to value caches only");
+  if (rank < 1 || rank > kMaxRank) return fail(PALU_ERR_INVALID_ARG, "rank must be in [1, 128]");
+  if (batch < 1 || kv_heads < 1 || capacity < 1) return fail(PALU_ERR_INVALID_ARG, "batch, kv_heads, capacity must be >= 1");
+  if (kv_heads % cfg->n_head_groups != 0)
+    return fail(PALU_ERR_INVALID_ARG, "kv_heads must be a multiple of n_head_groups (contiguous head groups)");
+  if (batch * (int64_t)kv_heads > 65535 * 64LL) return fail(PALU_ERR_UNSUPPORTED, "batch*kv_heads too large");
+  return PALU_OK;
+}
+
+}  // namespace palu
+
+using namespace palu;
+
+extern "C" palu_status palu_cache_size(const palu_config* cfg, int32_t role, int32_t rank, int64_t batch,
+                                       int32_t kv_heads, int64_t capacity, size_t* block_bytes, size_t* tail_bytes,
+                                       size_t* state_bytes) {
+  palu_status st = check_cache_args(cfg, role, rank, batch, kv_heads, capacity);
+  if (st != PALU_OK) return st;
+  const Geometry g = geometry(cfg, role, rank);
+  const int64_t n_blk = (capacity + kBlock - 1) / kBlock;
+  const bool quant = cfg->quantize || role == PALU_ROLE_KEY;
+  if (block_bytes) *block_bytes = align_up((size_t)batch * kv_heads * n_blk * g.rec_bytes, 256);
+  if (tail_bytes) *tail_bytes = quant ? align_up(sizeof(float) * (size_t)batch * kv_heads * kBlock * rank, 256) : 0;
+  if (state_bytes) *state_bytes = state_layout(cfg->n_head_groups, rank).total;
+  return PALU_OK;
+}
+
+extern "C" palu_status palu_cache_init(palu_cache* cache, const palu_config* cfg, int32_t role, int32_t rank,
+                                       int64_t batch, int32_t kv_heads, int64_t capacity, const float* basis,
+                                       int32_t basis_ld, const float* mu, void* blocks, void* tail, void* state,
+                                       void* stream) {
+  if (!cache) return fail(PALU_ERR_INVALID_ARG, "cache is NULL");
+  palu_status st = check_cache_args(cfg, role, rank, batch, kv_heads, capacity);
+  if (st != PALU_OK) return st;
+  const bool quant = cfg->quantize || role == PALU_ROLE_KEY;
+  if (!basis || !mu || !blocks || !state || (quant && !tail))
+    return fail(PALU_ERR_INVALID_ARG, "basis, mu, blocks, state (and tail for quantized caches) must be non-NULL");
+  if (basis_ld < rank) return fail(PALU_ERR_INVALID_ARG, "basis_ld must be >= rank");
+  if (((uintptr_t)blocks | (uintptr_t)state | (uintptr_t)(tail ? tail : state)) & 255)
+    return fail(PALU_ERR_INVALID_ARG, "blocks, tail and state must be 256-byte aligned");
+  const Geometry g = geometry(cfg, role, rank);
+  palu_cache c;
+  std::memset(&c, 0, sizeof(c));
+  c.magic = kCacheMagic;
+  c.role = role;
+  c.head_dim = kHeadDim;
+  c.rank = rank;
+  c.n_hi = g.n_hi;
+  c.n_groups = cfg->n_head_groups;
+  c.heads_per_group = kv_heads / cfg->n_head_groups;
+  c.quantize = quant ? 1 : 0;
+  c.batch = (int32_t)batch;
+  c.kv_heads = kv_heads;
+  c.n_hi_oct = g.n_hi_oct;
+  c.n_lo_oct = g.n_lo_oct;
+  c.n_oct = g.n_oct;
+  c.record_bytes = g.rec_bytes;
+  c.capacity = capacity;
+  c.n_blk_cap = (capacity + kBlock - 1) / kBlock;
+  c.blocks = blocks;
+  c.tail = quant ? static_cast<float*>(tail) : nullptr;
+  c.state = state;
+  c.length = 0;
+  const StateLayout sl = state_layout(c.n_groups, rank);
+  uint8_t* s = static_cast<uint8_t*>(state);
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  cache_init_kernel<<<dim3(rank, c.n_groups), kHeadDim, 0, strm>>>(
+      basis, basis_ld, mu, reinterpret_cast<float*>(s + sl.basis_off), reinterpret_cast<float*>(s + sl.mu_off),
+      reinterpret_cast<float2*>(s + sl.mv_off), reinterpret_cast<StateHeader*>(s), rank);
+  st = cuda_check(cudaGetLastError(), "cache_init_kernel launch");
+  if (st != PALU_OK) return st;
+  *cache = c;
+  return PALU_OK;
+}
+
+static palu_status check_cache(const palu_cache* c, const char* name) {
+  if (!c) return fail(PALU_ERR_INVALID_ARG, std::string(name) + " is NULL");
+  if (c->magic != kCacheMagic) return fail(PALU_ERR_NOT_INITIALIZED, std::string(name) + " is not initialised");
+  return PALU_OK;
+}
+
+extern "C" palu_status palu_encode_append(palu_cache* cache, const void* x, int64_t tokens, void* stream) {
+  palu_status st = check_cache(cache, "cache");
+  if (st != PALU_OK) return st;
+  if (tokens < 0) return fail(PALU_ERR_INVALID_ARG, "tokens must be >= 0");
+  if (tokens == 0) return PALU_OK;
+  if (!x || ((uintptr_t)x & 15)) return fail(PALU_ERR_INVALID_ARG, "x must be a non-NULL, 16-byte aligned device pointer");
+  if (cache->length + tokens > cache->capacity)
+    return fail(PALU_ERR_CAPACITY, "append of " + std::to_string(tokens) + " tokens to a cache holding " +
+                                       std::to_string(cache->length) + " exceeds its capacity " +
+                                       std::to_string(cache->capacity));
+  const int64_t nblk = (tokens + kBlock - 1) / kBlock + 1;  // blocks touched from any start offset
+  if (nblk > 2147483647LL) return fail(PALU_ERR_UNSUPPORTED, "too many tokens in one append");
+  const int smem = encode_smem(cache->rank, cache->record_bytes).total;
+  int per_sm = 0;
+  st = kernel_occupancy(reinterpret_cast<const void*>(encode_append_kernel), 128, smem, &per_sm);
+  if (st != PALU_OK) return st;
+  const CacheView cv = make_view(cache);
+  encode_append_kernel<<<dim3((unsigned)nblk, cache->kv_heads, cache->batch), 128, smem,
+                         static_cast<cudaStream_t>(stream)>>>(cv, static_cast<const __half*>(x), tokens,
+                                                              cache->kv_heads);
+  st = cuda_check(cudaGetLastError(), "encode_append_kernel launch");
+  if (st != PALU_OK) return st;
+  cache->length += tokens;
+  return PALU_OK;
+}
+
+extern "C" palu_status palu_cache_stats(const palu_cache* c, palu_stats* s) {
+  palu_status st = check_cache(c, "cache");
+  if (st != PALU_OK) return st;
+  if (!s) return fail(PALU_ERR_INVALID_ARG, "stats is NULL");
+  std::memset(s, 0, sizeof(*s));
+  const double streams = (double)c->batch * c->kv_heads;
+  const int64_t n_full = c->length / kBlock, n_tail = c->length % kBlock;
+  s->length = c->length;
+  s->rank = c->rank;
+  s->n_hi = c->n_hi;
+  const double code_bits = c->quantize ? (double)(c->n_hi * 4 + (c->rank - c->n_hi) * 2) : 16.0 * c->rank;
+  if (c->quantize) {
+    s->code_bytes = streams * n_full * kBlock * code_bits / 8.0;
+    s->meta_bytes = streams * n_full * c->rank * 4.0;
+    s->tail_bytes = streams * n_tail * c->rank * 4.0;
+    s->record_bytes = streams * n_full * (double)c->record_bytes;
+  } else {
+    s->code_bytes = streams * c->length * c->rank * 2.0;
+    s->record_bytes = streams * ((c->length + kBlock - 1) / kBlock) * (double)c->record_bytes;
+  }
+  s->basis_bytes = 4.0 * c->n_groups * (double)c->rank * kHeadDim + 4.0 * c->n_groups * kHeadDim;
+  s->fp16_bytes = streams * c->length * kHeadDim * 2.0;
+  s->effective_bits = code_bits / kHeadDim;
+  s->bits_with_meta = c->quantize ? (code_bits + c->rank * 32.0 / kBlock) / kHeadDim : s->effective_bits;
+  return PALU_OK;
+}
+
+extern "C" palu_status palu_cache_sync(palu_cache* c, uint32_t* device_error, void* stream) {
+  palu_status st = check_cache(c, "cache");
+  if (st != PALU_OK) return st;
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  st = cuda_check(cudaStreamSynchronize(strm), "cudaStreamSynchronize");
+  if (st != PALU_OK) return st;
+  StateHeader h;
+  st = cuda_check(cudaMemcpy(&h, c->state, sizeof(h), cudaMemcpyDeviceToHost), "read cache state");
+  if (st != PALU_OK) return st;
+  c->length = h.length;
+  if (device_error) *device_error = h.err;
+  if (h.err) {
+    const unsigned int zero = 0;
+    cudaMemcpy(static_cast<uint8_t*>(c->state) + offsetof(StateHeader, err), &zero, sizeof(zero),
+               cudaMemcpyHostToDevice);
+    return fail(PALU_ERR_DEVICE, "device error word 0x" + [](unsigned v) {
+      char b[16];
+      snprintf(b, sizeof(b), "%x", v);
+      return std::string(b);
+    }(h.err) + " (1 capacity, 2 copy wait timeout, 4 K/V length mismatch, 8 eigen-solver not converged)");
+  }
+  return PALU_OK;
+}

@@ -1,0 +1,503 @@
+// Basis fit of one tensor (K or V) of one layer.
+//
+// Method (page "PALU — True Low-Rank Latent Storage for Keys and Values",
+// "How it works", prefill steps 1-3): split the KV heads into contiguous
+// groups, stack each group's heads along the token axis, take a truncated SVD
+// of the mean-centred rows -> shared basis V_g (D x r) and mean mu_g; the rank
+// is explicit or set by an energy threshold, and one rank (the minimum over
+// groups) is kept for all groups.
+//
+// The right singular vectors of X_c are the eigenvectors of the centred Gram
+// matrix X_c^T X_c = X^T X - n mu mu^T.  GB300 plan:
+//   1. gram_kernel: X^T X and the column sums of row chunks (one CTA per SM)
+//      on tensor cores.  fp16 operands are exact; each 16-row product is
+//      promoted from its fresh fp32 accumulator into an error-free fp32 pair,
+//      so the chunk sums carry ~48-bit accuracy.  Rows are staged through
+//      swizzled shared memory by cp.async.
+//   2. reduce_kernel: chunk partials summed in fp64, centred in fp64.
+//   3. jacobi_kernel: one CTA per group diagonalises the 128x128 matrix with
+//      parallel-ordered cyclic Jacobi rotations (64 disjoint pairs per round),
+//      A in fp64 and the rotations accumulated in fp32, all in shared memory;
+//      then eigenvalues sorted descending and each direction's sign fixed so
+//      its largest-magnitude entry is positive.
+//   4. host: energy-threshold rank per group, r = minimum.
+#include <math.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "palu_internal.cuh"
+
+namespace palu {
+
+constexpr int kGramTile = 64;     // rows per shared-memory stage
+constexpr int kGramStages = 3;
+constexpr int kGramThreads = 256;
+
+struct GramParams {
+  const __half* x;
+  float* part;      // [n_g][n_chunks][2][128][128]  (hi, lo)
+  float* colpart;   // [n_g][n_chunks][2][128]
+  long long seq, rows_g, chunk_rows;
+  int Hkv, hg, n_chunks;
+};
+
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
+  const int sz = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(sz) : "memory");
+}
+
+// smem tile: 64 rows x 128 halves (256 B per row); 16-byte chunk ch of row r is
+// stored at chunk (ch ^ (r & 7)) so ldmatrix row gathers are conflict-free.
+__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int ch) {
+  return base + row * 256 + ((ch ^ (row & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(kGramThreads) gram_kernel(const GramParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, c4 = lane & 3;
+  const int chunk = blockIdx.x, grp = blockIdx.y;
+  const long long R0 = (long long)chunk * p.chunk_rows;
+  const long long R1 = min(R0 + p.chunk_rows, p.rows_g);
+  const int n_tiles = (int)((R1 - R0 + kGramTile - 1) / kGramTile);
+  const uint32_t sbase = smem_addr(smem);
+
+  auto load_tile = [&](int tile, int stage) {
+#pragma unroll
+    for (int i = 0; i < (kGramTile * 16) / kGramThreads; ++i) {
+      const int idx = tid + i * kGramThreads;
+      const int row = idx >> 4, ch = idx & 15;
+      const long long R = R0 + (long long)tile * kGramTile + row;
+      const bool valid = R < R1;
+      const long long Rc = valid ? R : R0;
+      const long long bb = Rc / ((long long)p.hg * p.seq);
+      const long long rem = Rc % ((long long)p.hg * p.seq);
+      const long long hh = rem / p.seq, t = rem % p.seq;
+      const __half* src = p.x + ((bb * p.Hkv + (long long)grp * p.hg + hh) * p.seq + t) * kHeadDim + ch * 8;
+      uint8_t* dst = smem + stage * (kGramTile * 256) + row * 256 + ((ch ^ (row & 7)) << 4);
+      cp_async16_zfill(dst, src, valid);
+    }
+  };
+
+  const int wm = warp >> 1, wn = warp & 1;  // C rows [32 wm, +32), cols [64 wn, +64)
+  // Each 16-row tensor-core product starts from a zero accumulator and is then
+  // added into an unevaluated fp32 pair (hi, lo) with an error-free sum, so
+  // the only rounding left is that of one 16-term product sum: long fp32
+  // accumulation chains would lose the ~1e-9 relative accuracy the trailing
+  // retained directions of a decaying spectrum need.
+  float Ch[2][8][4], Cl[2][8][4];
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int b = 0; b < 8; ++b)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) Ch[a][b][e] = Cl[a][b][e] = 0.f;
+  float Sh[2][4], Sl[2][4];  // column sums: X^T * ones (kept by warps with wn == 0)
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) Sh[a][e] = Sl[a][e] = 0.f;
+  const uint32_t ones = (g8 == 0) ? 0x3C003C00u : 0u;  // B[k][n] = 1 for n = 0
+
+#pragma unroll
+  for (int s = 0; s < kGramStages - 1; ++s) {
+    if (s < n_tiles) load_tile(s, s);
+    cp_async_commit();
+  }
+  for (int tile = 0; tile < n_tiles; ++tile) {
+    cp_async_wait<kGramStages - 2>();
+    __syncthreads();
+    const int nxt = tile + kGramStages - 1;
+    if (nxt < n_tiles) load_tile(nxt, nxt % kGramStages);
+    cp_async_commit();
+    const uint32_t st = sbase + (tile % kGramStages) * (kGramTile * 256);
+    const int mat = lane >> 3, rr = lane & 7;
+#pragma unroll 1
+    for (int ks = 0; ks < kGramTile / 16; ++ks) {
+      const int k0 = 16 * ks;
+      uint32_t A[2][4];
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi) {
+        const int m0 = 32 * wm + 16 * mi;
+        // matrices: (k0-7, m0-7), (k0-7, m8-15), (k8-15, m0-7), (k8-15, m8-15)
+        const int row = k0 + rr + ((mat >> 1) << 3);
+        const int ch = (m0 >> 3) + (mat & 1);
+        ldsm_x4_t(A[mi][0], A[mi][1], A[mi][2], A[mi][3], tile_addr(st, row, ch));
+      }
+      uint32_t Bf[8][2];
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        const int n0 = 64 * wn + 16 * np;
+        // matrices: (k0-7, n0-7), (k8-15, n0-7), (k0-7, n8-15), (k8-15, n8-15)
+        const int row = k0 + rr + ((mat & 1) << 3);
+        const int ch = (n0 >> 3) + (mat >> 1);
+        ldsm_x4_t(Bf[2 * np][0], Bf[2 * np][1], Bf[2 * np + 1][0], Bf[2 * np + 1][1], tile_addr(st, row, ch));
+      }
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi) {
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          float T[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_f16(T, A[mi][0], A[mi][1], A[mi][2], A[mi][3], Bf[nt][0], Bf[nt][1]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float s, err;
+            two_sum(Ch[mi][nt][e], T[e], s, err);
+            Ch[mi][nt][e] = s;
+            Cl[mi][nt][e] = __fadd_rn(Cl[mi][nt][e], err);
+          }
+        }
+        if (wn == 0) {
+          float T[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_f16(T, A[mi][0], A[mi][1], A[mi][2], A[mi][3], ones, ones);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float s, err;
+            two_sum(Sh[mi][e], T[e], s, err);
+            Sh[mi][e] = s;
+            Sl[mi][e] = __fadd_rn(Sl[mi][e], err);
+          }
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+
+  float* dst = p.part + ((size_t)grp * p.n_chunks + chunk) * 2 * kHeadDim * kHeadDim;
+#pragma unroll
+  for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int m = 32 * wm + 16 * mi + g8 + 8 * (e >> 1);
+        const int n = 64 * wn + 8 * nt + 2 * c4 + (e & 1);
+        dst[m * kHeadDim + n] = Ch[mi][nt][e];
+        dst[kHeadDim * kHeadDim + m * kHeadDim + n] = Cl[mi][nt][e];
+      }
+  if (wn == 0 && c4 == 0) {
+    float* cdst = p.colpart + ((size_t)grp * p.n_chunks + chunk) * 2 * kHeadDim;
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi) {
+      cdst[32 * wm + 16 * mi + g8] = Sh[mi][0];
+      cdst[32 * wm + 16 * mi + g8 + 8] = Sh[mi][2];
+      cdst[kHeadDim + 32 * wm + 16 * mi + g8] = Sl[mi][0];
+      cdst[kHeadDim + 32 * wm + 16 * mi + g8 + 8] = Sl[mi][2];
+    }
+  }
+}
+
+// grid (64, n_g), 256 threads: G[i][j] = sum_c (hi + lo) - colsum_i colsum_j / n, in fp64
+__global__ void gram_reduce_kernel(const float* __restrict__ part, const float* __restrict__ colpart, int n_chunks,
+                                   double n_rows, double* G, float* mu) {
+  const int grp = blockIdx.y;
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  const int i = e / kHeadDim, j = e % kHeadDim;
+  const float* pp = part + (size_t)grp * n_chunks * 2 * kHeadDim * kHeadDim;
+  const float* cp = colpart + (size_t)grp * n_chunks * 2 * kHeadDim;
+  double s = 0.0, si = 0.0, sj = 0.0;
+  for (int c = 0; c < n_chunks; ++c) {
+    const float* pc = pp + (size_t)c * 2 * kHeadDim * kHeadDim;
+    const float* cc = cp + (size_t)c * 2 * kHeadDim;
+    s += (double)pc[e] + (double)pc[kHeadDim * kHeadDim + e];
+    si += (double)cc[i] + (double)cc[kHeadDim + i];
+    sj += (double)cc[j] + (double)cc[kHeadDim + j];
+  }
+  G[(size_t)grp * kHeadDim * kHeadDim + e] = s - si * sj / n_rows;
+  if (i == 0) mu[(size_t)grp * kHeadDim + j] = (float)(sj / n_rows);
+}
+
+constexpr int kJacThreads = 512;
+constexpr int kLdA = kHeadDim + 1;  // padded rows (fp64 and fp32)
+constexpr int kMaxSweeps = 40;
+
+// Pairs of round `rnd` (0..126) of the round-robin (circle) ordering of 128 indices.
+__device__ __forceinline__ void rr_pair(int rnd, int i, int& p, int& q) {
+  const int n1 = kHeadDim - 1;
+  if (i == 0) {
+    p = rnd;
+    q = n1;
+  } else {
+    p = (rnd + i) % n1;
+    q = (rnd - i + n1) % n1;
+  }
+  if (p > q) {
+    const int t = p;
+    p = q;
+    q = t;
+  }
+}
+
+__global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const double* __restrict__ G, float* basis,
+                                                             double* eigvals, unsigned int* err) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  double* A = reinterpret_cast<double*>(smem);                                    // [128][129]
+  float* V = reinterpret_cast<float*>(smem + sizeof(double) * kHeadDim * kLdA);   // [128][129]
+  double* cs = reinterpret_cast<double*>(smem + sizeof(double) * kHeadDim * kLdA + sizeof(float) * kHeadDim * kLdA);
+  double* sn = cs + 64;
+  int* pp = reinterpret_cast<int*>(sn + 64);
+  int* qq = pp + 64;
+  int* cnt = qq + 64;          // rotations this sweep
+  double* red = reinterpret_cast<double*>(cnt + 4);  // [kJacThreads]
+  int* order = reinterpret_cast<int*>(red + kJacThreads);  // [128]
+
+  const int tid = threadIdx.x, grp = blockIdx.x;
+  const double* Gg = G + (size_t)grp * kHeadDim * kHeadDim;
+  double fro = 0.0;
+  for (int e = tid; e < kHeadDim * kHeadDim; e += kJacThreads) {
+    const int i = e / kHeadDim, j = e % kHeadDim;
+    const double a = Gg[e];
+    A[i * kLdA + j] = a;
+    V[i * kLdA + j] = (i == j) ? 1.f : 0.f;
+    fro += a * a;
+  }
+  red[tid] = fro;
+  __syncthreads();
+  for (int s = kJacThreads / 2; s > 0; s >>= 1) {
+    if (tid < s) red[tid] += red[tid + s];
+    __syncthreads();
+  }
+  const double floor_abs = 1e-16 * sqrt(red[0]);
+  __syncthreads();
+
+  int sweep = 0;
+  for (; sweep < kMaxSweeps; ++sweep) {
+    if (tid == 0) *cnt = 0;
+    __syncthreads();
+    for (int rnd = 0; rnd < kHeadDim - 1; ++rnd) {
+      if (tid < 64) {
+        int p, q;
+        rr_pair(rnd, tid, p, q);
+        const double apq = A[p * kLdA + q], app = A[p * kLdA + p], aqq = A[q * kLdA + q];
+        double c = 1.0, s = 0.0;
+        if (fabs(apq) > fmax(1e-15 * sqrt(fabs(app * aqq)), floor_abs)) {
+          const double theta = (aqq - app) / (2.0 * apq);
+          const double t = (theta >= 0.0 ? 1.0 : -1.0) / (fabs(theta) + sqrt(theta * theta + 1.0));
+          c = 1.0 / sqrt(t * t + 1.0);
+          s = t * c;
+          atomicAdd(cnt, 1);
+        }
+        pp[tid] = p;
+        qq[tid] = q;
+        cs[tid] = c;
+        sn[tid] = s;
+      }
+      __syncthreads();
+      // A <- J^T A (rows p, q)
+      for (int e = tid; e < 64 * kHeadDim; e += kJacThreads) {
+        const int i = e / kHeadDim, k = e % kHeadDim;
+        const double s = sn[i];
+        if (s != 0.0) {
+          const double c = cs[i];
+          const int p = pp[i], q = qq[i];
+          const double ap = A[p * kLdA + k], aq = A[q * kLdA + k];
+          A[p * kLdA + k] = c * ap - s * aq;
+          A[q * kLdA + k] = s * ap + c * aq;
+        }
+      }
+      __syncthreads();
+      // A <- A J (columns p, q) and V <- V J
+      for (int e = tid; e < 64 * kHeadDim; e += kJacThreads) {
+        const int i = e % 64, k = e / 64;
+        const double s = sn[i];
+        if (s != 0.0) {
+          const double c = cs[i];
+          const int p = pp[i], q = qq[i];
+          const double ap = A[k * kLdA + p], aq = A[k * kLdA + q];
+          A[k * kLdA + p] = c * ap - s * aq;
+          A[k * kLdA + q] = s * ap + c * aq;
+          const float cf = (float)c, sf = (float)s;
+          const float vp = V[k * kLdA + p], vq = V[k * kLdA + q];
+          V[k * kLdA + p] = cf * vp - sf * vq;
+          V[k * kLdA + q] = sf * vp + cf * vq;
+        }
+      }
+      __syncthreads();
+      if (tid < 64 && sn[tid] != 0.0) {
+        A[pp[tid] * kLdA + qq[tid]] = 0.0;
+        A[qq[tid] * kLdA + pp[tid]] = 0.0;
+      }
+      __syncthreads();
+    }
+    if (*cnt == 0) break;
+    __syncthreads();
+  }
+  if (tid == 0 && sweep == kMaxSweeps) atomicOr(err, PALU_DEVERR_NOT_CONVERGED);
+
+  // sort by descending eigenvalue (stable: ties keep index order)
+  if (tid < kHeadDim) {
+    const double li = A[tid * kLdA + tid];
+    int pos = 0;
+    for (int j = 0; j < kHeadDim; ++j) {
+      const double lj = A[j * kLdA + j];
+      pos += (lj > li) || (lj == li && j < tid);
+    }
+    order[pos] = tid;
+  }
+  __syncthreads();
+  if (tid < kHeadDim) {
+    const int src = order[tid];
+    // canonical sign: largest-magnitude entry positive (first index among ties)
+    int arg = 0;
+    float best = -1.f;
+    for (int d = 0; d < kHeadDim; ++d) {
+      const float a = fabsf(V[d * kLdA + src]);
+      if (a > best) {
+        best = a;
+        arg = d;
+      }
+    }
+    const float sgn = V[arg * kLdA + src] < 0.f ? -1.f : 1.f;
+    float* bg = basis + (size_t)grp * kHeadDim * kHeadDim;
+    for (int d = 0; d < kHeadDim; ++d) bg[d * kHeadDim + tid] = sgn * V[d * kLdA + src];
+    eigvals[(size_t)grp * kHeadDim + tid] = fmax(A[src * kLdA + src], 0.0);
+  }
+}
+
+static size_t jacobi_smem() {
+  return sizeof(double) * kHeadDim * kLdA + sizeof(float) * kHeadDim * kLdA + sizeof(double) * 128 +
+         sizeof(int) * 128 + sizeof(int) * 4 + sizeof(double) * kJacThreads + sizeof(int) * kHeadDim;
+}
+
+struct FitLayout {
+  int n_chunks;
+  long long chunk_rows;
+  size_t part_off, col_off, G_off, err_off, total;
+};
+
+// Rows per chunk: enough chunks for one CTA per SM over all groups, in whole
+// 64-row tiles, between 64 and 16384 rows.
+static FitLayout fit_layout(int n_groups, long long rows_g) {
+  FitLayout f;
+  const long long sms = device_sm_count();
+  long long per = (rows_g * n_groups + sms - 1) / sms;
+  per = (per + kGramTile - 1) / kGramTile * kGramTile;
+  f.chunk_rows = std::max<long long>(kGramTile, std::min<long long>(16384, per));
+  f.n_chunks = (int)((rows_g + f.chunk_rows - 1) / f.chunk_rows);
+  f.part_off = 0;
+  f.col_off = align_up(f.part_off + sizeof(float) * 2 * (size_t)n_groups * f.n_chunks * kHeadDim * kHeadDim, 256);
+  f.G_off = align_up(f.col_off + sizeof(float) * 2 * (size_t)n_groups * f.n_chunks * kHeadDim, 256);
+  f.err_off = align_up(f.G_off + sizeof(double) * (size_t)n_groups * kHeadDim * kHeadDim, 256);
+  f.total = f.err_off + 256;
+  return f;
+}
+
+// energy-threshold rank (same definition as the method's "retain 90% of
+// singular value energy"; sigma or sigma^2 reading), clamped to [1, D]
+static int energy_rank(const double* lam, int D, double tau, int mode) {
+  std::vector<double> cum(D);
+  double run = 0.0;
+  for (int i = 0; i < D; ++i) {
+    const double l = lam[i] > 0.0 ? lam[i] : 0.0;
+    run += (mode == PALU_ENERGY_SIGMA) ? sqrt(l) : l;
+    cum[i] = run;
+  }
+  const double total = cum[D - 1];
+  if (!(total > 0.0)) return 1;
+  for (int i = 0; i < D; ++i)
+    if (cum[i] / total >= tau) return std::max(1, i + 1);
+  return D;
+}
+
+static palu_status check_fit_args(const palu_config* cfg, int64_t batch, int32_t kv_heads, int64_t seq) {
+  if (!cfg) return fail(PALU_ERR_INVALID_ARG, "config is NULL");
+  if (cfg->head_dim != kHeadDim) return fail(PALU_ERR_UNSUPPORTED, "head_dim must be 128");
+  if (cfg->n_head_groups < 1 || kv_heads < 1 || kv_heads % cfg->n_head_groups != 0)
+    return fail(PALU_ERR_INVALID_ARG, "kv_heads must be a positive multiple of n_head_groups");
+  if (batch < 1 || seq < 1) return fail(PALU_ERR_INVALID_ARG, "batch and seq must be >= 1");
+  if (cfg->rank < 0) return fail(PALU_ERR_INVALID_ARG, "rank must be >= 0");
+  if (cfg->rank == 0 && !(cfg->energy_threshold > 0.0 && cfg->energy_threshold <= 1.0))
+    return fail(PALU_ERR_INVALID_ARG, "energy_threshold must be in (0, 1]");
+  if (cfg->energy_mode != PALU_ENERGY_SIGMA && cfg->energy_mode != PALU_ENERGY_SIGMA2)
+    return fail(PALU_ERR_INVALID_ARG, "energy_mode must be PALU_ENERGY_SIGMA or PALU_ENERGY_SIGMA2");
+  const long long rows_g = batch * (long long)(kv_heads / cfg->n_head_groups) * seq;
+  if (rows_g < 2) return fail(PALU_ERR_INVALID_ARG, "need at least 2 rows per head group");
+  if (rows_g / kGramTile > 2147483647LL) return fail(PALU_ERR_UNSUPPORTED, "prefill too large");
+  return PALU_OK;
+}
+
+}  // namespace palu
+
+using namespace palu;
+
+extern "C" palu_status palu_fit_workspace_size(const palu_config* cfg, int64_t batch, int32_t kv_heads, int64_t seq,
+                                               size_t* bytes) {
+  palu_status st = check_fit_args(cfg, batch, kv_heads, seq);
+  if (st != PALU_OK) return st;
+  if (!bytes) return fail(PALU_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = fit_layout(cfg->n_head_groups, batch * (long long)(kv_heads / cfg->n_head_groups) * seq).total;
+  return PALU_OK;
+}
+
+extern "C" palu_status palu_fit(const palu_config* cfg, const void* x, int64_t batch, int32_t kv_heads, int64_t seq,
+                                void* workspace, size_t workspace_bytes, float* basis, float* mu, double* eigvals,
+                                int32_t* rank_out, int32_t* group_ranks, void* stream) {
+  palu_status st = check_fit_args(cfg, batch, kv_heads, seq);
+  if (st != PALU_OK) return st;
+  if (!x || !workspace || !basis || !mu || !eigvals || !rank_out)
+    return fail(PALU_ERR_INVALID_ARG, "x, workspace, basis, mu, eigvals and rank_out must be non-NULL");
+  if (((uintptr_t)x & 15) || ((uintptr_t)workspace & 255))
+    return fail(PALU_ERR_INVALID_ARG, "x must be 16-byte and workspace 256-byte aligned");
+  const int ng = cfg->n_head_groups;
+  const int hg = kv_heads / ng;
+  const long long rows_g = batch * (long long)hg * seq;
+  const FitLayout fl = fit_layout(ng, rows_g);
+  if (workspace_bytes < fl.total)
+    return fail(PALU_ERR_INVALID_ARG, "fit workspace too small: need " + std::to_string(fl.total) + " bytes");
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  unsigned int* err = reinterpret_cast<unsigned int*>(ws + fl.err_off);
+  st = cuda_check(cudaMemsetAsync(err, 0, sizeof(unsigned int), strm), "memset");
+  if (st != PALU_OK) return st;
+
+  GramParams gp;
+  gp.x = static_cast<const __half*>(x);
+  gp.part = reinterpret_cast<float*>(ws + fl.part_off);
+  gp.colpart = reinterpret_cast<float*>(ws + fl.col_off);
+  gp.seq = seq;
+  gp.rows_g = rows_g;
+  gp.Hkv = kv_heads;
+  gp.hg = hg;
+  gp.n_chunks = fl.n_chunks;
+  gp.chunk_rows = fl.chunk_rows;
+  const int gram_smem = kGramStages * kGramTile * 256;
+  st = cuda_check(cudaFuncSetAttribute(gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, gram_smem),
+                  "gram smem attr");
+  if (st != PALU_OK) return st;
+  gram_kernel<<<dim3(fl.n_chunks, ng), kGramThreads, gram_smem, strm>>>(gp);
+  st = cuda_check(cudaGetLastError(), "gram_kernel launch");
+  if (st != PALU_OK) return st;
+  double* G = reinterpret_cast<double*>(ws + fl.G_off);
+  gram_reduce_kernel<<<dim3(kHeadDim * kHeadDim / 256, ng), 256, 0, strm>>>(gp.part, gp.colpart, fl.n_chunks,
+                                                                             (double)rows_g, G, mu);
+  st = cuda_check(cudaGetLastError(), "gram_reduce_kernel launch");
+  if (st != PALU_OK) return st;
+  const size_t jsm = jacobi_smem();
+  st = cuda_check(cudaFuncSetAttribute(jacobi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)jsm),
+                  "jacobi smem attr");
+  if (st != PALU_OK) return st;
+  jacobi_kernel<<<ng, kJacThreads, jsm, strm>>>(G, basis, eigvals, err);
+  st = cuda_check(cudaGetLastError(), "jacobi_kernel launch");
+  if (st != PALU_OK) return st;
+
+  std::vector<double> lam((size_t)ng * kHeadDim);
+  unsigned int herr = 0;
+  st = cuda_check(cudaMemcpyAsync(lam.data(), eigvals, sizeof(double) * lam.size(), cudaMemcpyDeviceToHost, strm),
+                  "copy eigenvalues");
+  if (st != PALU_OK) return st;
+  st = cuda_check(cudaMemcpyAsync(&herr, err, sizeof(herr), cudaMemcpyDeviceToHost, strm), "copy error word");
+  if (st != PALU_OK) return st;
+  st = cuda_check(cudaStreamSynchronize(strm), "cudaStreamSynchronize(fit)");
+  if (st != PALU_OK) return st;
+  if (herr) return fail(PALU_ERR_DEVICE, "eigen-solver did not converge within its sweep limit");
+  int rmin = kHeadDim;
+  for (int g = 0; g < ng; ++g) {
+    const int rg = cfg->rank > 0 ? std::min(cfg->rank, kHeadDim)
+                                 : energy_rank(lam.data() + (size_t)g * kHeadDim, kHeadDim, cfg->energy_threshold,
+                                               cfg->energy_mode);
+    if (group_ranks) group_ranks[g] = rg;
+    rmin = std::min(rmin, rg);
+  }
+  *rank_out = rmin;
+  return PALU_OK;
+}

@@ -1,0 +1,286 @@
+"""Thin ctypes binding of libpalu (include/palu.h).
+
+Argument marshalling only: every step of the fit, append and decode runs in
+the library's CUDA kernels.  PyTorch provides device memory and the current
+stream.  If the library is missing the import of any entry point raises; there
+is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import c_double, c_float, c_int32, c_int64, c_size_t, c_uint32, c_void_p, POINTER
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpalu.so")
+
+PALU_OK = 0
+PALU_ENERGY_SIGMA = 0
+PALU_ENERGY_SIGMA2 = 1
+PALU_ROLE_KEY = 0
+PALU_ROLE_VALUE = 1
+PALU_DEVERR_CAPACITY = 1
+PALU_DEVERR_TIMEOUT = 2
+PALU_DEVERR_LENGTH_MISMATCH = 4
+PALU_DEVERR_NOT_CONVERGED = 8
+STATUS_NAMES = {0: "PALU_OK", 1: "PALU_ERR_INVALID_ARG", 2: "PALU_ERR_UNSUPPORTED", 3: "PALU_ERR_CAPACITY",
+                4: "PALU_ERR_NOT_INITIALIZED", 5: "PALU_ERR_CUDA", 6: "PALU_ERR_DEVICE"}
+
+
+class palu_config(ctypes.Structure):
+    _fields_ = [("head_dim", c_int32), ("n_head_groups", c_int32), ("rank", c_int32), ("energy_mode", c_int32),
+                ("energy_threshold", c_double), ("hi_fraction", c_double), ("hi_bit", c_int32),
+                ("lo_bit", c_int32), ("group_size", c_int32), ("quantize", c_int32)]
+
+
+class palu_cache(ctypes.Structure):
+    _fields_ = [("magic", c_int32), ("role", c_int32), ("head_dim", c_int32), ("rank", c_int32),
+                ("n_hi", c_int32), ("n_groups", c_int32), ("heads_per_group", c_int32), ("quantize", c_int32),
+                ("batch", c_int32), ("kv_heads", c_int32), ("n_hi_oct", c_int32), ("n_lo_oct", c_int32),
+                ("n_oct", c_int32), ("record_bytes", c_int32), ("capacity", c_int64), ("n_blk_cap", c_int64),
+                ("blocks", c_void_p), ("tail", c_void_p), ("state", c_void_p), ("length", c_int64)]
+
+
+class palu_stats(ctypes.Structure):
+    _fields_ = [("length", c_int64), ("rank", c_int32), ("n_hi", c_int32), ("code_bytes", c_double),
+                ("meta_bytes", c_double), ("tail_bytes", c_double), ("record_bytes", c_double),
+                ("basis_bytes", c_double), ("fp16_bytes", c_double), ("effective_bits", c_double),
+                ("bits_with_meta", c_double)]
+
+
+_P = POINTER
+_SIGNATURES = {
+    "palu_last_error": (ctypes.c_char_p, []),
+    "palu_version": (ctypes.c_char_p, []),
+    "palu_config_default": (c_int32, [_P(palu_config)]),
+    "palu_fit_workspace_size": (c_int32, [_P(palu_config), c_int64, c_int32, c_int64, _P(c_size_t)]),
+    "palu_fit": (c_int32, [_P(palu_config), c_void_p, c_int64, c_int32, c_int64, c_void_p, c_size_t, c_void_p,
+                           c_void_p, c_void_p, _P(c_int32), _P(c_int32), c_void_p]),
+    "palu_cache_size": (c_int32, [_P(palu_config), c_int32, c_int32, c_int64, c_int32, c_int64, _P(c_size_t),
+                                  _P(c_size_t), _P(c_size_t)]),
+    "palu_cache_init": (c_int32, [_P(palu_cache), _P(palu_config), c_int32, c_int32, c_int64, c_int32, c_int64,
+                                  c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "palu_encode_append": (c_int32, [_P(palu_cache), c_void_p, c_int64, c_void_p]),
+    "palu_decode_workspace_size": (c_int32, [_P(palu_cache), _P(palu_cache), c_int32, _P(c_size_t)]),
+    "palu_decode_attn": (c_int32, [_P(palu_cache), _P(palu_cache), c_void_p, c_int32, c_float, c_void_p, c_int32,
+                                   c_void_p, c_size_t, c_void_p]),
+    "palu_cache_stats": (c_int32, [_P(palu_cache), _P(palu_stats)]),
+    "palu_cache_sync": (c_int32, [_P(palu_cache), _P(c_uint32), c_void_p]),
+    "palu_fp16_decode_workspace_size": (c_int32, [c_int64, c_int32, c_int64, c_int32, _P(c_size_t)]),
+    "palu_fp16_decode_attn": (c_int32, [c_void_p, c_void_p, c_int64, c_int32, c_int64, c_int64, c_void_p, c_int32,
+                                        c_float, c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded libpalu.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libpalu.so not found at {LIB_PATH}; build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = l
+    return _lib
+
+
+class PaluError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def _check(status):
+    if status != PALU_OK:
+        raise PaluError(status, lib().palu_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ------------------------------------------------------------------ entry points
+
+def palu_last_error() -> str:
+    return lib().palu_last_error().decode()
+
+
+def palu_version() -> str:
+    return lib().palu_version().decode()
+
+
+def palu_config_default(**overrides) -> palu_config:
+    cfg = palu_config()
+    _check(lib().palu_config_default(ctypes.byref(cfg)))
+    for k, v in overrides.items():
+        setattr(cfg, k, v)
+    return cfg
+
+
+def palu_fit_workspace_size(cfg, batch, kv_heads, seq) -> int:
+    n = c_size_t()
+    _check(lib().palu_fit_workspace_size(ctypes.byref(cfg), batch, kv_heads, seq, ctypes.byref(n)))
+    return n.value
+
+
+def palu_fit(cfg, x, workspace, basis, mu, eigvals, stream=None):
+    """x fp16 [B, Hkv, S, D] (cuda); outputs basis fp32 [n_g, D, D], mu fp32 [n_g, D],
+    eigvals fp64 [n_g, D] (cuda).  Returns (rank, group_ranks)."""
+    B, H, S, _ = x.shape
+    r = c_int32()
+    gr = (c_int32 * cfg.n_head_groups)()
+    _check(lib().palu_fit(ctypes.byref(cfg), _ptr(x), B, H, S, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                          _ptr(basis), _ptr(mu), _ptr(eigvals), ctypes.byref(r), gr, _stream(stream)))
+    return r.value, list(gr)
+
+
+def palu_cache_size(cfg, role, rank, batch, kv_heads, capacity):
+    a, b, c = c_size_t(), c_size_t(), c_size_t()
+    _check(lib().palu_cache_size(ctypes.byref(cfg), role, rank, batch, kv_heads, capacity, ctypes.byref(a),
+                                 ctypes.byref(b), ctypes.byref(c)))
+    return a.value, b.value, c.value
+
+
+def palu_cache_init(cfg, role, rank, batch, kv_heads, capacity, basis, basis_ld, mu, blocks, tail, state,
+                    stream=None) -> palu_cache:
+    c = palu_cache()
+    _check(lib().palu_cache_init(ctypes.byref(c), ctypes.byref(cfg), role, rank, batch, kv_heads, capacity,
+                                 _ptr(basis), basis_ld, _ptr(mu), _ptr(blocks), _ptr(tail), _ptr(state),
+                                 _stream(stream)))
+    return c
+
+
+def palu_encode_append(cache: palu_cache, x, tokens=None, stream=None):
+    T = x.shape[2] if tokens is None else tokens
+    _check(lib().palu_encode_append(ctypes.byref(cache), _ptr(x), T, _stream(stream)))
+
+
+def palu_decode_workspace_size(k: palu_cache, v: palu_cache, q_heads: int) -> int:
+    n = c_size_t()
+    _check(lib().palu_decode_workspace_size(ctypes.byref(k), ctypes.byref(v), q_heads, ctypes.byref(n)))
+    return n.value
+
+
+def palu_decode_attn(k, v, q, out, workspace, softmax_scale=0.0, stream=None):
+    _check(lib().palu_decode_attn(ctypes.byref(k), ctypes.byref(v), _ptr(q), q.shape[1], softmax_scale, _ptr(out),
+                                  1 if out.dtype == torch.float32 else 0, _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def palu_cache_stats(cache) -> dict:
+    s = palu_stats()
+    _check(lib().palu_cache_stats(ctypes.byref(cache), ctypes.byref(s)))
+    return {name: getattr(s, name) for name, _ in palu_stats._fields_}
+
+
+def palu_cache_sync(cache, stream=None) -> int:
+    """Synchronise and refresh cache.length; raises PaluError if the device error word was set."""
+    e = c_uint32()
+    _check(lib().palu_cache_sync(ctypes.byref(cache), ctypes.byref(e), _stream(stream)))
+    return e.value
+
+
+def palu_fp16_decode_workspace_size(batch, kv_heads, seq_cap, q_heads) -> int:
+    n = c_size_t()
+    _check(lib().palu_fp16_decode_workspace_size(batch, kv_heads, seq_cap, q_heads, ctypes.byref(n)))
+    return n.value
+
+
+def palu_fp16_decode_attn(k, v, seq, q, out, workspace, softmax_scale=0.0, stream=None):
+    B, H, cap, _ = k.shape
+    _check(lib().palu_fp16_decode_attn(_ptr(k), _ptr(v), B, H, seq, cap, _ptr(q), q.shape[1], softmax_scale,
+                                       _ptr(out), 1 if out.dtype == torch.float32 else 0, _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+# ------------------------------------------------------------------ buffer helpers
+
+def _dev_bytes(n, device):
+    return torch.empty(max(int(n), 256), dtype=torch.uint8, device=device)
+
+
+class LatentCache:
+    """One (layer, K or V) cache with its device buffers allocated by torch."""
+
+    def __init__(self, cfg, role, rank, batch, kv_heads, capacity, basis, mu, basis_ld=None, stream=None):
+        dev = basis.device
+        blk, tail, state = palu_cache_size(cfg, role, rank, batch, kv_heads, capacity)
+        self.blocks = _dev_bytes(blk, dev)
+        self.tail = _dev_bytes(tail, dev) if tail else None
+        self.state = _dev_bytes(state, dev)
+        ld = basis.shape[-1] if basis_ld is None else basis_ld
+        self.c = palu_cache_init(cfg, role, rank, batch, kv_heads, capacity, basis, ld, mu, self.blocks,
+                                 self.tail, self.state, stream)
+
+    @property
+    def length(self):
+        return self.c.length
+
+    def append(self, x, stream=None):
+        palu_encode_append(self.c, x, x.shape[2], stream)
+
+    def stats(self):
+        return palu_cache_stats(self.c)
+
+    def sync(self, stream=None):
+        return palu_cache_sync(self.c, stream)
+
+    def record_array(self):
+        """Block records as a host uint8 array [B, Hkv, n_blk_cap, record_bytes]."""
+        c = self.c
+        n = c.batch * c.kv_heads * c.n_blk_cap * c.record_bytes
+        return self.blocks[:n].cpu().numpy().reshape(c.batch, c.kv_heads, c.n_blk_cap, c.record_bytes)
+
+    def tail_array(self):
+        c = self.c
+        if self.tail is None:
+            return None
+        n = c.batch * c.kv_heads * 32 * c.rank * 4
+        return self.tail[:n].cpu().numpy().view("float32").reshape(c.batch, c.kv_heads, 32, c.rank)
+
+    def basis_array(self):
+        """The stored basis as [n_g, D, r] and mean [n_g, D] (host fp32)."""
+        c = self.c
+        ng, r = c.n_groups, c.rank
+        st = self.state.cpu().numpy()
+        basis_off = 256
+        mu_off = -(-(basis_off + 4 * ng * r * 128) // 256) * 256
+        bT = st[basis_off:basis_off + 4 * ng * r * 128].view("float32").reshape(ng, r, 128)
+        mu = st[mu_off:mu_off + 4 * ng * 128].view("float32").reshape(ng, 128)
+        return bT.transpose(0, 2, 1).copy(), mu.copy()
+
+
+def fit(cfg, x, stream=None):
+    """Run palu_fit on x fp16 [B, Hkv, S, D]; returns (basis, mu, eigvals, rank, group_ranks)."""
+    B, H, S, D = x.shape
+    ng = cfg.n_head_groups
+    ws = _dev_bytes(palu_fit_workspace_size(cfg, B, H, S), x.device)
+    basis = torch.empty(ng, D, D, dtype=torch.float32, device=x.device)
+    mu = torch.empty(ng, D, dtype=torch.float32, device=x.device)
+    eig = torch.empty(ng, D, dtype=torch.float64, device=x.device)
+    r, gr = palu_fit(cfg, x, ws, basis, mu, eig, stream)
+    return basis, mu, eig, r, gr
+
+
+def decode(kc: LatentCache, vc: LatentCache, q, out_dtype=torch.float32, softmax_scale=0.0, stream=None,
+           workspace=None, out=None):
+    """Decode attention; returns out [B, Hq, D]."""
+    if workspace is None:
+        workspace = _dev_bytes(palu_decode_workspace_size(kc.c, vc.c, q.shape[1]), q.device)
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    palu_decode_attn(kc.c, vc.c, q, out, workspace, softmax_scale, stream)
+    return out

@@ -1,0 +1,135 @@
+"""The C-ABI library loads, exports every symbol declared in include/palu.h,
+its structs match the binding's, and host-side validation works (no GPU)."""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "palu.h")
+
+
+@pytest.fixture(scope="session")
+def palu():
+    from rank_latent_kv_gb300 import palu as P
+    if not os.path.exists(P.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    P.lib()
+    return P
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(palu_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("palu_fit", "palu_encode_append", "palu_decode_attn", "palu_cache_init", "palu_last_error"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(palu):
+    out = subprocess.run(["nm", "-D", "--defined-only", palu.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (palu_[a-z0-9_]+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(palu.lib(), n)
+    assert set(palu._SIGNATURES) == set(declared_functions())
+
+
+def test_struct_layouts_match_the_header(palu):
+    """Compile a tiny C program against palu.h and compare sizes/offsets with ctypes."""
+    prog = r'''
+#include <stdio.h>
+#include <stddef.h>
+#include "palu.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(palu_config), sizeof(palu_cache), sizeof(palu_stats),
+         offsetof(palu_config, energy_threshold), offsetof(palu_cache, capacity), offsetof(palu_cache, length),
+         offsetof(palu_stats, code_bytes));
+  return 0;
+}'''
+    with tempfile.TemporaryDirectory() as d:
+        src = os.path.join(d, "t.c")
+        exe = os.path.join(d, "t")
+        open(src, "w").write(prog)
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), src, "-o", exe], check=True)
+        vals = list(map(int, subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()))
+    assert vals == [ctypes.sizeof(palu.palu_config), ctypes.sizeof(palu.palu_cache), ctypes.sizeof(palu.palu_stats),
+                    palu.palu_config.energy_threshold.offset, palu.palu_cache.capacity.offset,
+                    palu.palu_cache.length.offset, palu.palu_stats.code_bytes.offset]
+
+
+def test_defaults_follow_the_page(palu):
+    cfg = palu.palu_config_default()
+    assert (cfg.head_dim, cfg.n_head_groups, cfg.rank, cfg.hi_bit, cfg.lo_bit, cfg.group_size, cfg.quantize) == \
+           (128, 4, 0, 4, 2, 32, 1)
+    assert cfg.energy_threshold == 0.90 and cfg.hi_fraction == 0.25
+    assert "sm_103a" in palu.palu_version()
+
+
+def test_cache_size_matches_the_layout(palu):
+    import oracle as O
+    cfg = palu.palu_config_default()
+    for role in (palu.PALU_ROLE_KEY, palu.PALU_ROLE_VALUE):
+        for r in (1, 27, 32, 52, 74, 128):
+            blk, tail, state = palu.palu_cache_size(cfg, role, r, 2, 8, 100)
+            rec = O.Layout(role, r, O.n_hi_channels(r)).record_bytes
+            assert blk == -(-(2 * 8 * 4 * rec) // 256) * 256
+            assert tail == -(-(4 * 2 * 8 * 32 * r) // 256) * 256
+            assert state % 256 == 0 and state >= 4 * 4 * r * 128
+    cfg.quantize = 0
+    blk, tail, _ = palu.palu_cache_size(cfg, palu.PALU_ROLE_VALUE, 32, 1, 8, 64)
+    assert blk == 8 * 2 * 4 * 512 and tail == 0
+
+
+@pytest.mark.parametrize("change,status", [
+    (dict(head_dim=64), 2), (dict(group_size=16), 2), (dict(hi_bit=8), 2), (dict(n_head_groups=3), 1),
+    (dict(hi_fraction=1.5), 1)])
+def test_host_validation_errors(palu, change, status):
+    cfg = palu.palu_config_default(**change)
+    with pytest.raises(palu.PaluError) as e:
+        palu.palu_cache_size(cfg, palu.PALU_ROLE_KEY, 32, 1, 8, 64)
+    assert e.value.status == status
+    assert palu.palu_last_error()
+
+
+def test_rank_and_role_validation(palu):
+    cfg = palu.palu_config_default()
+    for bad in (0, 129):
+        with pytest.raises(palu.PaluError):
+            palu.palu_cache_size(cfg, palu.PALU_ROLE_KEY, bad, 1, 8, 64)
+    cfg.quantize = 0
+    with pytest.raises(palu.PaluError) as e:
+        palu.palu_cache_size(cfg, palu.PALU_ROLE_KEY, 32, 1, 8, 64)
+    assert "value caches only" in str(e.value)
+
+
+def test_fit_workspace_and_validation(palu):
+    cfg = palu.palu_config_default()
+    n = palu.palu_fit_workspace_size(cfg, 1, 8, 4096)
+    assert n >= 4 * 2 * 128 * 128 * 4 + 4 * 128 * 128 * 8     # >= one (hi, lo) chunk per group + fp64 Gram
+    with pytest.raises(palu.PaluError):
+        palu.palu_fit_workspace_size(palu.palu_config_default(energy_threshold=0.0), 1, 8, 64)
+    with pytest.raises(palu.PaluError):
+        palu.palu_fit_workspace_size(cfg, 1, 6, 64)
+
+
+def test_uninitialised_cache_is_rejected(palu):
+    c = palu.palu_cache()
+    st = palu.palu_stats()
+    assert palu.lib().palu_cache_stats(ctypes.byref(c), ctypes.byref(st)) == 4
+    assert "not initialised" in palu.palu_last_error()
+
+
+def test_fp16_comparator_validation(palu):
+    with pytest.raises(palu.PaluError):
+        palu.palu_fp16_decode_workspace_size(1, 4, 128, 40)   # 10 query heads per KV head
