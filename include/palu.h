@@ -190,6 +190,14 @@ palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v, const voi
                              int32_t q_heads, float softmax_scale, void* out, int32_t out_fp32,
                              void* workspace, size_t workspace_bytes, void* stream);
 
+/* Roll the cache back to `length` tokens (e.g. to reuse a prompt prefix or
+ * drop rejected speculative tokens).  Allowed when length is a multiple of 32
+ * (a block boundary) or lies inside the current partial block, i.e. whenever
+ * no already-quantized block has to be reopened; 0 <= length <= current
+ * length.  Sets the device-side length with a one-thread kernel, so it can be
+ * captured in a graph together with appends. */
+palu_status palu_cache_truncate(palu_cache* cache, int64_t length, void* stream);
+
 /* Byte accounting of a cache (section "Evidence": compressed bytes against
  * fp16 bytes; section "Effective bit-width").  Host only. */
 palu_status palu_cache_stats(const palu_cache* cache, palu_stats* stats);

@@ -40,28 +40,29 @@ int device_sm_count() {
 
 palu_status kernel_occupancy(const void* kernel, int threads, int smem, int* per_sm) {
   static std::map<std::tuple<const void*, int, int, int>, int> cache;
+  static std::map<std::pair<const void*, int>, int> attr_max;  // dynamic smem limit set per kernel and device
   int dev = 0;
   palu_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
   if (st != PALU_OK) return st;
   const auto key = std::make_tuple(kernel, threads, smem, dev);
-  {
-    std::lock_guard<std::mutex> lock(g_mu);
-    auto it = cache.find(key);
-    if (it != cache.end()) {
-      *per_sm = it->second;
-      return PALU_OK;
-    }
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *per_sm = it->second;
+    return PALU_OK;
   }
-  if (smem > 48 * 1024) {
+  // the limit is a property of the kernel: only ever raise it, never lower it
+  int& cur = attr_max[std::make_pair(kernel, dev)];
+  if (smem > 48 * 1024 && smem > cur) {
     st = cuda_check(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                     "cudaFuncSetAttribute(max dynamic shared memory)");
     if (st != PALU_OK) return st;
+    cur = smem;
   }
   int n = 0;
   st = cuda_check(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem), "occupancy query");
   if (st != PALU_OK) return st;
   n = n > 0 ? n : 1;
-  std::lock_guard<std::mutex> lock(g_mu);
   cache[key] = n;
   *per_sm = n;
   return PALU_OK;

@@ -321,6 +321,15 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
   }
 }
 
+// Sets the device length (the host has checked that no quantized block is reopened).
+__global__ void cache_truncate_kernel(StateHeader* hdr, long long length) {
+  if (length > hdr->length) {
+    hdr->err |= PALU_DEVERR_CAPACITY;
+    return;
+  }
+  hdr->length = length;
+}
+
 // ------------------------------------------------------------------ host
 static int64_t n_hi_of(const palu_config* cfg, int r) {
   const double v = ceil(cfg->hi_fraction * (double)r - 1e-9);
@@ -470,6 +479,23 @@ extern "C" palu_status palu_encode_append(palu_cache* cache, const void* x, int6
   st = cuda_check(cudaGetLastError(), "encode_append_kernel launch");
   if (st != PALU_OK) return st;
   cache->length += tokens;
+  return PALU_OK;
+}
+
+extern "C" palu_status palu_cache_truncate(palu_cache* cache, int64_t length, void* stream) {
+  palu_status st = check_cache(cache, "cache");
+  if (st != PALU_OK) return st;
+  if (length < 0 || length > cache->length)
+    return fail(PALU_ERR_INVALID_ARG, "truncate length must be in [0, current length]");
+  const int64_t open_block = (cache->length / kBlock) * kBlock;
+  if (cache->quantize && length % kBlock != 0 && length < open_block)
+    return fail(PALU_ERR_INVALID_ARG,
+                "truncate to a length inside an already quantized 32-token block is not possible; use a multiple of 32");
+  cache_truncate_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<StateHeader*>(cache->state), length);
+  st = cuda_check(cudaGetLastError(), "cache_truncate_kernel launch");
+  if (st != PALU_OK) return st;
+  cache->length = length;
   return PALU_OK;
 }
 

@@ -407,7 +407,6 @@ __global__ void __launch_bounds__(128) latent_combine_kernel(const DecodeParams 
   __shared__ float cq_s[8];
   __shared__ float s_s[8][kBlock];
   __shared__ float o_s[kMaxRank];
-  __shared__ float ML_s[2];
   const int tid = threadIdx.x;
   const int kh = blockIdx.x, b = blockIdx.y;
   const int Gq = p.Gq, rvp = p.rvp, mstride = 2 + rvp;
@@ -505,7 +504,6 @@ __global__ void __launch_bounds__(128) latent_combine_kernel(const DecodeParams 
     }
     __syncthreads();
   }
-  (void)ML_s;
 }
 
 // ------------------------------------------------------------------ host

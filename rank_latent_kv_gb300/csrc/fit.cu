@@ -10,7 +10,10 @@
 // The right singular vectors of X_c are the eigenvectors of the centred Gram
 // matrix X_c^T X_c = X^T X - n mu mu^T.  GB300 plan:
 //   1. gram_kernel: X^T X and the column sums of row chunks (one CTA per SM)
-//      on tensor cores.  fp16 operands are exact; each 16-row product is
+//      on tensor cores (prefills above 64K rows per group; smaller ones use
+//      gram_exact_kernel, exact accumulation on CUDA cores, because at small
+//      row counts the rounding of each 16-row product sum is not yet averaged
+//      down).  fp16 operands are exact; each 16-row product is
 //      promoted from its fresh fp32 accumulator into an error-free fp32 pair,
 //      so the chunk sums carry ~48-bit accuracy.  Rows are staged through
 //      swizzled shared memory by cp.async.
@@ -187,6 +190,90 @@ __global__ void __launch_bounds__(kGramThreads) gram_kernel(const GramParams p) 
   }
 }
 
+// Exact Gram for small prefills: fp16 x fp16 products are exact in fp32 and
+// are summed error-free into (hi, lo) pairs, so the chunk sums carry ~48-bit
+// accuracy with no per-product-sum rounding.  Thread t owns the 8x8 block
+// (t / 16, t % 16) of the 128x128 Gram; rows are staged as fp32 in shared
+// memory, 64 at a time.  Same output layout as gram_kernel.
+constexpr long long kExactGramRows = 65536;  // rows per group up to which this path is used
+
+__global__ void __launch_bounds__(256) gram_exact_kernel(const GramParams p) {
+  __shared__ __align__(16) float xs[kGramTile][kHeadDim + 4];
+  const int tid = threadIdx.x, chunk = blockIdx.x, grp = blockIdx.y;
+  const long long R0 = (long long)chunk * p.chunk_rows;
+  const long long R1 = min(R0 + p.chunk_rows, p.rows_g);
+  const int bi = tid >> 4, bj = tid & 15;
+  float H[8][8], L[8][8];
+#pragma unroll
+  for (int a = 0; a < 8; ++a)
+#pragma unroll
+    for (int b = 0; b < 8; ++b) H[a][b] = L[a][b] = 0.f;
+  float sh = 0.f, sl = 0.f;  // column sum of column tid (tid < 128)
+  for (long long base = R0; base < R1; base += kGramTile) {
+    const int nrows = (int)min((long long)kGramTile, R1 - base);
+    __syncthreads();
+    for (int i = tid; i < kGramTile * (kHeadDim / 8); i += 256) {
+      const int row = i / (kHeadDim / 8), q = i % (kHeadDim / 8);
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (row < nrows) {
+        const long long R = base + row;
+        const long long bb = R / ((long long)p.hg * p.seq);
+        const long long rem = R % ((long long)p.hg * p.seq);
+        const long long hh = rem / p.seq, t = rem % p.seq;
+        const uint4 w = *reinterpret_cast<const uint4*>(
+            p.x + ((bb * p.Hkv + (long long)grp * p.hg + hh) * p.seq + t) * kHeadDim + 8 * q);
+        const __half2* h2 = reinterpret_cast<const __half2*>(&w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(h2[e]);
+          v[2 * e] = f.x;
+          v[2 * e + 1] = f.y;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) xs[row][8 * q + e] = v[e];
+    }
+    __syncthreads();
+    for (int r = 0; r < nrows; ++r) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&xs[r][8 * bi]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&xs[r][8 * bi + 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&xs[r][8 * bj]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&xs[r][8 * bj + 4]);
+      const float xa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float xb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          float s, e;
+          two_sum(H[a][b], __fmul_rn(xa[a], xb[b]), s, e);  // the product is exact
+          H[a][b] = s;
+          L[a][b] = __fadd_rn(L[a][b], e);
+        }
+      if (tid < kHeadDim) {
+        float s, e;
+        two_sum(sh, xs[r][tid], s, e);
+        sh = s;
+        sl = __fadd_rn(sl, e);
+      }
+    }
+  }
+  float* dst = p.part + ((size_t)grp * p.n_chunks + chunk) * 2 * kHeadDim * kHeadDim;
+#pragma unroll
+  for (int a = 0; a < 8; ++a)
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int m = 8 * bi + a, n = 8 * bj + b;
+      dst[m * kHeadDim + n] = H[a][b];
+      dst[kHeadDim * kHeadDim + m * kHeadDim + n] = L[a][b];
+    }
+  if (tid < kHeadDim) {
+    float* cdst = p.colpart + ((size_t)grp * p.n_chunks + chunk) * 2 * kHeadDim;
+    cdst[tid] = sh;
+    cdst[kHeadDim + tid] = sl;
+  }
+}
+
 // grid (64, n_g), 256 threads: G[i][j] = sum_c (hi + lo) - colsum_i colsum_j / n, in fp64
 __global__ void gram_reduce_kernel(const float* __restrict__ part, const float* __restrict__ colpart, int n_chunks,
                                    double n_rows, double* G, float* mu) {
@@ -230,7 +317,7 @@ __device__ __forceinline__ void rr_pair(int rnd, int i, int& p, int& q) {
 
 __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const double* __restrict__ G, float* basis,
                                                              double* eigvals, unsigned int* err) {
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem[];
   double* A = reinterpret_cast<double*>(smem);                                    // [128][129]
   float* V = reinterpret_cast<float*>(smem + sizeof(double) * kHeadDim * kLdA);   // [128][129]
   double* cs = reinterpret_cast<double*>(smem + sizeof(double) * kHeadDim * kLdA + sizeof(float) * kHeadDim * kLdA);
@@ -460,11 +547,15 @@ extern "C" palu_status palu_fit(const palu_config* cfg, const void* x, int64_t b
   gp.hg = hg;
   gp.n_chunks = fl.n_chunks;
   gp.chunk_rows = fl.chunk_rows;
-  const int gram_smem = kGramStages * kGramTile * 256;
-  st = cuda_check(cudaFuncSetAttribute(gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, gram_smem),
-                  "gram smem attr");
-  if (st != PALU_OK) return st;
-  gram_kernel<<<dim3(fl.n_chunks, ng), kGramThreads, gram_smem, strm>>>(gp);
+  if (rows_g <= kExactGramRows) {
+    gram_exact_kernel<<<dim3(fl.n_chunks, ng), 256, 0, strm>>>(gp);
+  } else {
+    const int gram_smem = kGramStages * kGramTile * 256;
+    int per_sm = 0;
+    st = kernel_occupancy(reinterpret_cast<const void*>(gram_kernel), kGramThreads, gram_smem, &per_sm);
+    if (st != PALU_OK) return st;
+    gram_kernel<<<dim3(fl.n_chunks, ng), kGramThreads, gram_smem, strm>>>(gp);
+  }
   st = cuda_check(cudaGetLastError(), "gram_kernel launch");
   if (st != PALU_OK) return st;
   double* G = reinterpret_cast<double*>(ws + fl.G_off);
@@ -473,9 +564,11 @@ extern "C" palu_status palu_fit(const palu_config* cfg, const void* x, int64_t b
   st = cuda_check(cudaGetLastError(), "gram_reduce_kernel launch");
   if (st != PALU_OK) return st;
   const size_t jsm = jacobi_smem();
-  st = cuda_check(cudaFuncSetAttribute(jacobi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)jsm),
-                  "jacobi smem attr");
-  if (st != PALU_OK) return st;
+  {
+    int per_sm = 0;
+    st = kernel_occupancy(reinterpret_cast<const void*>(jacobi_kernel), kJacThreads, (int)jsm, &per_sm);
+    if (st != PALU_OK) return st;
+  }
   jacobi_kernel<<<ng, kJacThreads, jsm, strm>>>(G, basis, eigvals, err);
   st = cuda_check(cudaGetLastError(), "jacobi_kernel launch");
   if (st != PALU_OK) return st;

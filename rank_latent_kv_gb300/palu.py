@@ -67,6 +67,7 @@ _SIGNATURES = {
     "palu_decode_attn": (c_int32, [_P(palu_cache), _P(palu_cache), c_void_p, c_int32, c_float, c_void_p, c_int32,
                                    c_void_p, c_size_t, c_void_p]),
     "palu_cache_stats": (c_int32, [_P(palu_cache), _P(palu_stats)]),
+    "palu_cache_truncate": (c_int32, [_P(palu_cache), c_int64, c_void_p]),
     "palu_cache_sync": (c_int32, [_P(palu_cache), _P(c_uint32), c_void_p]),
     "palu_fp16_decode_workspace_size": (c_int32, [c_int64, c_int32, c_int64, c_int32, _P(c_size_t)]),
     "palu_fp16_decode_attn": (c_int32, [c_void_p, c_void_p, c_int64, c_int32, c_int64, c_int64, c_void_p, c_int32,
@@ -186,6 +187,10 @@ def palu_cache_stats(cache) -> dict:
     return {name: getattr(s, name) for name, _ in palu_stats._fields_}
 
 
+def palu_cache_truncate(cache, length, stream=None):
+    _check(lib().palu_cache_truncate(ctypes.byref(cache), length, _stream(stream)))
+
+
 def palu_cache_sync(cache, stream=None) -> int:
     """Synchronise and refresh cache.length; raises PaluError if the device error word was set."""
     e = c_uint32()
@@ -237,6 +242,9 @@ class LatentCache:
 
     def sync(self, stream=None):
         return palu_cache_sync(self.c, stream)
+
+    def truncate(self, length, stream=None):
+        palu_cache_truncate(self.c, length, stream)
 
     def record_array(self):
         """Block records as a host uint8 array [B, Hkv, n_blk_cap, record_bytes]."""
