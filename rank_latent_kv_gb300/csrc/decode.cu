@@ -399,110 +399,123 @@ __global__ void __launch_bounds__(kThreads) latent_decode_kernel(const DecodePar
   }
 }
 
-// One CTA per (batch, KV head): merge chunk partials, add the tail tokens,
-// apply V^V^T and + mu^V, write the output rows of the KV head's query heads.
-__global__ void __launch_bounds__(128) latent_combine_kernel(const DecodeParams p, void* out, int out_fp32) {
+// One CTA of 8 warps per (batch, KV head); warp h finishes query head h:
+// merge the chunk partials (log-sum-exp), fold in the unquantized tail tokens
+// in fp32, then apply V^V^T and + mu^V once.  Every loop runs across lanes,
+// so the kernel is a handful of dependent memory round trips long.
+__global__ void __launch_bounds__(256) latent_combine_kernel(const DecodeParams p, void* out, int out_fp32) {
   __shared__ float q_s[8][kHeadDim];
   __shared__ float qt_s[8][kMaxRank];
-  __shared__ float cq_s[8];
-  __shared__ float s_s[8][kBlock];
-  __shared__ float o_s[kMaxRank];
-  const int tid = threadIdx.x;
+  __shared__ float ol_s[8][kMaxRank];
+  __shared__ float pt_s[8][kBlock];
+  const int tid = threadIdx.x, h = tid >> 5, lane = tid & 31;
   const int kh = blockIdx.x, b = blockIdx.y;
   const int Gq = p.Gq, rvp = p.rvp, mstride = 2 + rvp;
+  if (h >= Gq) return;
   const long long len = __ldcg(&p.k.hdr->length);
   const long long n_full = len / kBlock;
   const int n_tail = (int)(len % kBlock);
   const int gk = kh / p.k.heads_per_group, gv = kh / p.v.heads_per_group;
   const int rk = p.k.r, rv = p.v.r;
   const long long stream = (long long)b * p.Hkv + kh;
+  const float* wpart = p.ws + stream * p.n_chunks * (long long)Gq * mstride + (long long)h * mstride;
+  const long long cstride = (long long)Gq * mstride;
 
-  for (int i = tid; i < 8 * kHeadDim; i += 128) {
-    const int h = i / kHeadDim, d = i % kHeadDim;
-    q_s[h][d] = h < Gq ? __half2float(p.q[((long long)b * p.Hq + (long long)kh * Gq + h) * kHeadDim + d]) : 0.f;
-  }
-  __syncthreads();
+  // chunk maxima
+  float M = -INFINITY;
+  for (int ch = lane; ch < p.n_chunks; ch += 32) M = fmaxf(M, __ldcg(wpart + ch * cstride));
+  // tail scores: lane t < n_tail owns token t
+  float st = -INFINITY;
   if (n_tail > 0) {
-    for (int j = tid; j < rk; j += 128) {
-      float acc[8];
-#pragma unroll
-      for (int h = 0; h < 8; ++h) acc[h] = 0.f;
-      const float* row = p.k.basisT + ((size_t)gk * rk + j) * kHeadDim;
-      for (int d = 0; d < kHeadDim; ++d) {
-        const float vv = row[d];
-#pragma unroll
-        for (int h = 0; h < 8; ++h) acc[h] = fmaf(q_s[h][d], vv, acc[h]);
-      }
-#pragma unroll
-      for (int h = 0; h < 8; ++h) qt_s[h][j] = acc[h] * p.scale_log2;
-    }
-    if (tid < 8) {
-      float s = 0.f;
-      for (int d = 0; d < kHeadDim; ++d) s = fmaf(q_s[tid][d], p.k.mu[(size_t)gk * kHeadDim + d], s);
-      cq_s[tid] = s * p.scale_log2;
-    }
-    __syncthreads();
-    // tail scores
-    const float* tk = p.k.tail + stream * kBlock * rk;
-    for (int i = tid; i < Gq * n_tail; i += 128) {
-      const int h = i / n_tail, t = i % n_tail;
-      float s = 0.f;
-      for (int j = 0; j < rk; ++j) s = fmaf(qt_s[h][j], tk[t * rk + j], s);
-      s_s[h][t] = s + cq_s[h];
-    }
-    __syncthreads();
-  }
-
-  const float* wpart = p.ws + stream * p.n_chunks * (long long)Gq * mstride;
-  for (int h = 0; h < Gq; ++h) {
-    // chunk max and denominator (every thread computes them; cheap)
-    float M = -INFINITY;
-    for (int ch = 0; ch < p.n_chunks; ++ch) M = fmaxf(M, wpart[((long long)ch * Gq + h) * mstride]);
-    for (int t = 0; t < n_tail; ++t) M = fmaxf(M, s_s[h][t]);
-    float Lsum = 0.f;
-    for (int ch = 0; ch < p.n_chunks; ++ch) {
-      const float m = wpart[((long long)ch * Gq + h) * mstride];
-      if (m != -INFINITY) Lsum += wpart[((long long)ch * Gq + h) * mstride + 1] * ex2(m - M);
-    }
-    for (int t = 0; t < n_tail; ++t) Lsum += ex2(s_s[h][t] - M);
-    // latent accumulator per real value channel j
-    for (int j = tid; j < rv; j += 128) {
-      int pch = j;
-      if (p.v.quantize && j >= p.v.n_hi) pch = 8 * p.v.n_hi_oct + (j - p.v.n_hi);
+    const __half* qh = p.q + ((long long)b * p.Hq + (long long)kh * Gq + h) * kHeadDim;
+    for (int d = lane; d < kHeadDim; d += 32) q_s[h][d] = __half2float(qh[d]);
+    __syncwarp();
+    for (int j = lane; j < rk; j += 32) {
+      const float4* row = reinterpret_cast<const float4*>(p.k.basisT + ((size_t)gk * rk + j) * kHeadDim);
       float a = 0.f;
-      for (int ch = 0; ch < p.n_chunks; ++ch) {
-        const float m = wpart[((long long)ch * Gq + h) * mstride];
-        if (m != -INFINITY) a += wpart[((long long)ch * Gq + h) * mstride + 2 + pch] * ex2(m - M);
+#pragma unroll 8
+      for (int d4 = 0; d4 < kHeadDim / 4; ++d4) {
+        const float4 v = row[d4];
+        a = fmaf(q_s[h][4 * d4], v.x,
+                 fmaf(q_s[h][4 * d4 + 1], v.y, fmaf(q_s[h][4 * d4 + 2], v.z, fmaf(q_s[h][4 * d4 + 3], v.w, a))));
       }
+      qt_s[h][j] = a;
+    }
+    float c = 0.f;
+    for (int d = lane; d < kHeadDim; d += 32) c = fmaf(q_s[h][d], p.k.mu[(size_t)gk * kHeadDim + d], c);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    __syncwarp();
+    if (lane < n_tail) {
+      const float* tk = p.k.tail + (stream * kBlock + lane) * rk;
+      float a = 0.f;
+      for (int j = 0; j < rk; ++j) a = fmaf(qt_s[h][j], tk[j], a);
+      st = (a + c) * p.scale_log2;
+      M = fmaxf(M, st);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  // denominator
+  float L = 0.f;
+  for (int ch = lane; ch < p.n_chunks; ch += 32) {
+    const float m = __ldcg(wpart + ch * cstride);
+    if (m != -INFINITY) L += __ldcg(wpart + ch * cstride + 1) * ex2(m - M);
+  }
+  const float pt = lane < n_tail ? ex2(st - M) : 0.f;
+  pt_s[h][lane] = pt;
+  L += pt;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  const float invL = 1.f / L;
+  // latent accumulator per padded value channel, stored by real channel
+  for (int pch = lane; pch < rvp; pch += 32) {
+    const int j = padded_to_channel(pch, rv, p.v.n_hi, p.v.n_hi_oct, p.v.quantize);
+    float a = 0.f;
+    for (int ch = 0; ch < p.n_chunks; ++ch) {
+      const float m = __ldcg(wpart + ch * cstride);
+      if (m != -INFINITY) a = fmaf(__ldcg(wpart + ch * cstride + 2 + pch), ex2(m - M), a);
+    }
+    if (j >= 0) ol_s[h][j] = a;
+  }
+  __syncwarp();
+  if (n_tail > 0) {
+    for (int j = lane; j < rv; j += 32) {
+      float a = ol_s[h][j];
       for (int t = 0; t < n_tail; ++t) {
         float lv;
         if (p.v.quantize) {
           lv = p.v.tail[(stream * kBlock + t) * rv + j];
         } else {
           const uint8_t* rec = p.v.blocks + (stream * p.v.n_blk_cap + n_full) * p.v.rec_bytes;
-          const int octet = j >> 3, slot = j & 7;
           const int k = 2 * (t >> 4) + ((t & 15) >> 3);
-          const int ln = 4 * slot + ((t & 7) >> 1);
-          lv = __half2float(*reinterpret_cast<const __half*>(rec + 512 * octet + 16 * ln + 4 * k + 2 * (t & 1)));
+          const int ln = 4 * (j & 7) + ((t & 7) >> 1);
+          lv = __half2float(*reinterpret_cast<const __half*>(rec + 512 * (j >> 3) + 16 * ln + 4 * k + 2 * (t & 1)));
         }
-        a = fmaf(ex2(s_s[h][t] - M), lv, a);
+        a = fmaf(pt_s[h][t], lv, a);
       }
-      o_s[j] = a / Lsum;
+      ol_s[h][j] = a;
     }
-    __syncthreads();
-    // epilogue: out[d] = sum_j o_j V[d, j] + mu[d]
-    {
-      const int d = tid;
-      float o = p.v.mu[(size_t)gv * kHeadDim + d];
-      const float* bt = p.v.basisT + (size_t)gv * rv * kHeadDim;
-      for (int j = 0; j < rv; ++j) o = fmaf(o_s[j], bt[(size_t)j * kHeadDim + d], o);
-      const long long oi = ((long long)b * p.Hq + (long long)kh * Gq + h) * kHeadDim + d;
-      if (out_fp32)
-        static_cast<float*>(out)[oi] = o;
-      else
-        static_cast<__half*>(out)[oi] = __float2half_rn(o);
-    }
-    __syncthreads();
+  }
+  __syncwarp();
+  // epilogue: out[d] = (sum_j o_j V[d, j]) / L + mu[d]
+  const float* bt = p.v.basisT + (size_t)gv * rv * kHeadDim;
+  float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int j = 0; j < rv; ++j) {
+    const float oj = ol_s[h][j];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = fmaf(oj, bt[(size_t)j * kHeadDim + lane + 32 * e], o[e]);
+  }
+  const long long oi = ((long long)b * p.Hq + (long long)kh * Gq + h) * kHeadDim;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int d = lane + 32 * e;
+    const float v = fmaf(o[e], invL, p.v.mu[(size_t)gv * kHeadDim + d]);
+    if (out_fp32)
+      static_cast<float*>(out)[oi + d] = v;
+    else
+      static_cast<__half*>(out)[oi + d] = __float2half_rn(v);
   }
 }
 
@@ -616,6 +629,6 @@ extern "C" palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v
   kern<<<dim3(pl.n_chunks, k->kv_heads, k->batch), kThreads, pl.smem, strm>>>(p);
   st = cuda_check(cudaGetLastError(), "latent_decode_kernel launch");
   if (st != PALU_OK) return st;
-  latent_combine_kernel<<<dim3(k->kv_heads, k->batch), 128, 0, strm>>>(p, out, out_fp32);
+  latent_combine_kernel<<<dim3(k->kv_heads, k->batch), 256, 0, strm>>>(p, out, out_fp32);
   return cuda_check(cudaGetLastError(), "latent_combine_kernel launch");
 }
