@@ -198,6 +198,28 @@ palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v, const voi
  * captured in a graph together with appends. */
 palu_status palu_cache_truncate(palu_cache* cache, int64_t length, void* stream);
 
+/* palu_decode_attn without a caller workspace, for callers that cannot
+ * allocate device memory while decoding (a plugin whose host application owns
+ * every allocation, a serving loop that forbids allocation between steps, a
+ * process whose device memory is reserved in full by another pool).  The
+ * method's pages have no counterpart: this is a library convenience.
+ *   Same arguments and results as palu_decode_attn, minus the workspace.
+ *   The split-K partials live in a fixed 4 MiB device array inside the
+ *   library (held on every GPU that loads it, until exit); caches whose
+ *   partials need more (palu_decode_workspace_size > 4 MiB) are rejected with
+ *   PALU_ERR_UNSUPPORTED and a message giving both sizes.
+ *   The first call on a device looks up the array's device address with
+ *   cudaGetSymbolAddress; make that first call before any stream capture.
+ *   Nothing in the array needs to start at zero: each call writes every
+ *   partial before reading it, and the array keeps the last call's
+ *   contents.  All calls on one device share that device's copy, so calls
+ *   that may overlap on the GPU (e.g. issued on different streams) race and
+ *   must be serialised by the caller.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+palu_status palu_decode_attn_noalloc(const palu_cache* k, const palu_cache* v, const void* q,
+                                     int32_t q_heads, float softmax_scale, void* out, int32_t out_fp32,
+                                     void* stream);
+
 /* Byte accounting of a cache (section "Evidence": compressed bytes against
  * fp16 bytes; section "Effective bit-width").  Host only. */
 palu_status palu_cache_stats(const palu_cache* cache, palu_stats* stats);

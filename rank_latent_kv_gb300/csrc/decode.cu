@@ -33,6 +33,8 @@
 #include <math.h>
 
 #include <algorithm>
+#include <map>
+#include <mutex>
 
 #include "palu_internal.cuh"
 
@@ -631,4 +633,55 @@ extern "C" palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v
   if (st != PALU_OK) return st;
   latent_combine_kernel<<<dim3(k->kv_heads, k->batch), 256, 0, strm>>>(p, out, out_fp32);
   return cuda_check(cudaGetLastError(), "latent_combine_kernel launch");
+}
+
+// ------------------------------------------------------------------ allocation-free decode
+// Some callers cannot allocate device memory while they decode: a plugin whose
+// host application owns every device allocation, a serving loop that forbids
+// allocation between steps to keep latency predictable, or a process whose
+// device memory is already reserved in full by another pool.  For them
+// palu_decode_attn_noalloc keeps the split-K partials in this fixed array,
+// which every GPU that loads the library holds until the process exits.
+namespace palu {
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch on the current device, looked up once per
+// device.  In host code the array's name is only a stand-in for the symbol.
+static palu_status noalloc_scratch(void** ptr) {
+  static std::mutex mu;
+  static std::map<int, void*> addr;
+  int dev = 0;
+  palu_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != PALU_OK) return st;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = addr.find(dev);
+  if (it != addr.end()) {
+    *ptr = it->second;
+    return PALU_OK;
+  }
+  void* p = nullptr;
+  st = cuda_check(cudaGetSymbolAddress(&p, g_decode_scratch), "cudaGetSymbolAddress(decode scratch)");
+  if (st != PALU_OK) return st;
+  addr[dev] = p;
+  *ptr = p;
+  return PALU_OK;
+}
+}  // namespace palu
+
+extern "C" palu_status palu_decode_attn_noalloc(const palu_cache* k, const palu_cache* v, const void* q,
+                                                int32_t q_heads, float softmax_scale, void* out, int32_t out_fp32,
+                                                void* stream) {
+  DecodePlan pl;
+  palu_status st = plan_decode(k, v, q_heads, &pl);
+  if (st != PALU_OK) return st;
+  if (pl.ws_bytes > kNoAllocScratchBytes)
+    return fail(PALU_ERR_UNSUPPORTED, "palu_decode_attn_noalloc: these caches need " + std::to_string(pl.ws_bytes) +
+                                          " bytes of scratch but the library's fixed scratch holds " +
+                                          std::to_string(kNoAllocScratchBytes) +
+                                          "; call palu_decode_attn with a workspace instead");
+  void* ws = nullptr;
+  st = noalloc_scratch(&ws);
+  if (st != PALU_OK) return st;
+  return palu_decode_attn(k, v, q, q_heads, softmax_scale, out, out_fp32, ws, kNoAllocScratchBytes, stream);
 }

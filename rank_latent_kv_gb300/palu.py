@@ -66,6 +66,8 @@ _SIGNATURES = {
     "palu_decode_workspace_size": (c_int32, [_P(palu_cache), _P(palu_cache), c_int32, _P(c_size_t)]),
     "palu_decode_attn": (c_int32, [_P(palu_cache), _P(palu_cache), c_void_p, c_int32, c_float, c_void_p, c_int32,
                                    c_void_p, c_size_t, c_void_p]),
+    "palu_decode_attn_noalloc": (c_int32, [_P(palu_cache), _P(palu_cache), c_void_p, c_int32, c_float, c_void_p,
+                                           c_int32, c_void_p]),
     "palu_cache_stats": (c_int32, [_P(palu_cache), _P(palu_stats)]),
     "palu_cache_truncate": (c_int32, [_P(palu_cache), c_int64, c_void_p]),
     "palu_cache_sync": (c_int32, [_P(palu_cache), _P(c_uint32), c_void_p]),
@@ -179,6 +181,12 @@ def palu_decode_attn(k, v, q, out, workspace, softmax_scale=0.0, stream=None):
     _check(lib().palu_decode_attn(ctypes.byref(k), ctypes.byref(v), _ptr(q), q.shape[1], softmax_scale, _ptr(out),
                                   1 if out.dtype == torch.float32 else 0, _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def palu_decode_attn_noalloc(k, v, q, out, softmax_scale=0.0, stream=None):
+    """palu_decode_attn using the library's fixed device scratch (no workspace)."""
+    _check(lib().palu_decode_attn_noalloc(ctypes.byref(k), ctypes.byref(v), _ptr(q), q.shape[1], softmax_scale,
+                                          _ptr(out), 1 if out.dtype == torch.float32 else 0, _stream(stream)))
 
 
 def palu_cache_stats(cache) -> dict:
