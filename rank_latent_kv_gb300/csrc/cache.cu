@@ -42,6 +42,7 @@ __global__ void cache_init_kernel(const float* __restrict__ basis, int ld, const
     hdr->length = 0;
     hdr->err = 0;
     hdr->ticket = 0;
+    hdr->max_scale = 0;
   }
 }
 
@@ -246,6 +247,7 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
           const __half zh = __float2half_rn(mn);
           const float s32 = __half2float(sh), z32 = __half2float(zh);
           sz[j] = __halves2half2(sh, zh);
+          atomicMax(&cv.hdr->max_scale, __float_as_uint(s32));
           for (int t = 0; t < kBlock; ++t) {
             float q = 0.f;
             if (s32 != 0.f) {
@@ -410,6 +412,7 @@ __global__ void __launch_bounds__(128) encode_one_kernel(CacheView cv, const __h
         const __half zh = __float2half_rn(mn);
         const float s32 = __half2float(sh), z32 = __half2float(zh);
         sz[j] = __halves2half2(sh, zh);
+        atomicMax(&cv.hdr->max_scale, __float_as_uint(s32));
         for (int t = 0; t < kBlock; ++t) {
           float q = 0.f;
           if (s32 != 0.f) q = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(lat[t][j], z32), s32)), 0.f), qmax);
@@ -533,7 +536,7 @@ extern "C" palu_status palu_cache_size(const palu_config* cfg, int32_t role, int
   const bool quant = cfg->quantize || role == PALU_ROLE_KEY;
   if (block_bytes) *block_bytes = align_up((size_t)batch * kv_heads * n_blk * g.rec_bytes, 256);
   if (tail_bytes) *tail_bytes = quant ? align_up(sizeof(float) * (size_t)batch * kv_heads * kBlock * rank, 256) : 0;
-  if (state_bytes) *state_bytes = state_layout(cfg->n_head_groups, rank).total;
+  if (state_bytes) *state_bytes = state_layout(cfg->n_head_groups, rank, batch * (int64_t)kv_heads).total;
   return PALU_OK;
 }
 
@@ -573,9 +576,11 @@ extern "C" palu_status palu_cache_init(palu_cache* cache, const palu_config* cfg
   c.tail = quant ? static_cast<float*>(tail) : nullptr;
   c.state = state;
   c.length = 0;
-  const StateLayout sl = state_layout(c.n_groups, rank);
+  const StateLayout sl = state_layout(c.n_groups, rank, batch * (int64_t)kv_heads);
   uint8_t* s = static_cast<uint8_t*>(state);
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  st = cuda_check(cudaMemsetAsync(s + sl.tk_off, 0, sl.total - sl.tk_off, strm), "cudaMemsetAsync(tickets)");
+  if (st != PALU_OK) return st;
   cache_init_kernel<<<dim3(rank, c.n_groups), kHeadDim, 0, strm>>>(
       basis, basis_ld, mu, reinterpret_cast<float*>(s + sl.basis_off), reinterpret_cast<float*>(s + sl.mu_off),
       reinterpret_cast<float2*>(s + sl.mv_off), reinterpret_cast<StateHeader*>(s), rank);
