@@ -19,12 +19,25 @@ struct DecodePlan {
   DecodeKernel kern;
 };
 
-static DecodeKernel pick_kernel(int kc, int vc, bool vq) {
+static DecodeKernel pick_kernel(int ke, int ve, int kc, int vc, bool vq) {
+  if (ke <= 8 && ve <= 8) {
+    switch (ke) {
+      case 1: return decode_kernel_exact<1>(ve, vq);
+      case 2: return decode_kernel_exact<2>(ve, vq);
+      case 3: return decode_kernel_exact<3>(ve, vq);
+      case 4: return decode_kernel_exact<4>(ve, vq);
+      case 5: return decode_kernel_exact<5>(ve, vq);
+      case 6: return decode_kernel_exact<6>(ve, vq);
+      case 7: return decode_kernel_exact<7>(ve, vq);
+      case 8: return decode_kernel_exact<8>(ve, vq);
+      default: return nullptr;
+    }
+  }
   switch (kc) {
-    case 1: return decode_kernel_for<1>(vc, vq);
-    case 2: return decode_kernel_for<2>(vc, vq);
-    case 3: return decode_kernel_for<3>(vc, vq);
-    case 4: return decode_kernel_for<4>(vc, vq);
+    case 1: return decode_kernel_class<1>(vc, vq);
+    case 2: return decode_kernel_class<2>(vc, vq);
+    case 3: return decode_kernel_class<3>(vc, vq);
+    case 4: return decode_kernel_class<4>(vc, vq);
     default: return nullptr;
   }
 }
@@ -46,7 +59,7 @@ static palu_status plan_decode(const palu_cache* k, const palu_cache* v, int32_t
   pl->VQ = v->quantize != 0;
   if (pl->VQ && pl->VC != v->n_hi_oct) return fail(PALU_ERR_UNSUPPORTED, "unexpected value record layout");
   if (pl->KC != k->n_hi_oct) return fail(PALU_ERR_UNSUPPORTED, "unexpected key record layout");
-  pl->kern = pick_kernel(pl->KC, pl->VC, pl->VQ);
+  pl->kern = pick_kernel(k->n_oct, v->n_oct, pl->KC, pl->VC, pl->VQ);
   if (!pl->kern) return fail(PALU_ERR_UNSUPPORTED, "no decode kernel for this rank");
   const int rec_k = k->record_bytes, rec_v = v->record_bytes;
   pl->stage_bytes = 2 * (rec_k + rec_v);
@@ -55,21 +68,40 @@ static palu_status plan_decode(const palu_cache* k, const palu_cache* v, int32_t
   pl->ring_off = (int)align_up(kDecBarOff + 8 * (kDecWarps * pl->ns + 1), 128);
   const int64_t streams = (int64_t)k->batch * k->kv_heads;
   const int sms = device_sm_count();
-  const int64_t g_max = (int64_t)sms * 4;  // bound on the grid, for the partial slots
-  pl->seg_max = (int)((g_max + streams - 1) / streams + 1);
-  const int tv_bytes = v->quantize ? kBlock * v->rank * 4 : rec_v;
-  const size_t merge_bytes = (size_t)v->rank * 512 + (size_t)128 * k->rank + align_up(tv_bytes, 16) +
-                             (size_t)pl->seg_max * 64 + 8 * kBlock * 4 + 8 * kHeadDim * 4 + 32;
-  const size_t warp_merge = (size_t)kDecWarps * 8 * (2 + pl->rvp) * 4;
-  const size_t ring = std::max({(size_t)kDecWarps * pl->ns * pl->stage_bytes, warp_merge, merge_bytes});
-  pl->smem = (int)(pl->ring_off + ring);
-  if (pl->smem > 227 * 1024) return fail(PALU_ERR_UNSUPPORTED, "decode shared-memory plan exceeds 227 KB");
+  // shared memory: header, then the rings, which the merges reuse; the merge
+  // layout needs the partial slots per stream, which follow from the grid,
+  // which follows from the occupancy
+  const size_t rings = std::max((size_t)kDecWarps * pl->ns * pl->stage_bytes,
+                                (size_t)kDecWarps * 8 * (2 + pl->rvp) * 4);
   int per_sm = 0;
-  palu_status st = kernel_occupancy(reinterpret_cast<const void*>(pl->kern), kDecThreads, pl->smem, &per_sm);
+  palu_status st = kernel_occupancy(reinterpret_cast<const void*>(pl->kern), kDecThreads,
+                                    (int)(pl->ring_off + rings), &per_sm);
   if (st != PALU_OK) return st;
   int64_t grid = (int64_t)sms * std::min(per_sm, 4);
   grid = std::min<int64_t>(grid, std::max<int64_t>(streams, streams * k->n_blk_cap));
   pl->grid = (int)std::max<int64_t>(1, grid);
+  const int tv_bytes = v->quantize ? kBlock * v->rank * 4 : rec_v;
+  const size_t merge_fixed = (size_t)v->rank * 512 + (size_t)128 * k->rank + align_up(tv_bytes, 16) +
+                             8 * kBlock * 4 + 8 * kHeadDim * 4 + 32;
+  const size_t per_seg = (size_t)Gq * (2 + pl->rvp) * 4;
+  pl->seg_max = (int)((pl->grid + streams - 1) / streams + 1);
+  const size_t merge_budget = 200 * 1024 - (size_t)pl->ring_off;
+  if (merge_fixed + pl->seg_max * per_seg > merge_budget) {
+    // few streams: fewer CTAs, so that one stream's partials fit on chip
+    const int64_t seg_fit = (int64_t)((merge_budget - merge_fixed) / per_seg);
+    if (seg_fit < 2) return fail(PALU_ERR_UNSUPPORTED, "decode merge does not fit in shared memory");
+    pl->grid = (int)std::max<int64_t>(1, std::min<int64_t>(pl->grid, streams * (seg_fit - 1)));
+    pl->seg_max = (int)((pl->grid + streams - 1) / streams + 1);
+  }
+  const size_t merge_bytes = merge_fixed + pl->seg_max * per_seg;
+  pl->smem = (int)(pl->ring_off + std::max(rings, merge_bytes));
+  if (pl->smem > 227 * 1024) return fail(PALU_ERR_UNSUPPORTED, "decode shared-memory plan exceeds 227 KB");
+  if (merge_bytes > rings) {
+    st = kernel_occupancy(reinterpret_cast<const void*>(pl->kern), kDecThreads, pl->smem, &per_sm);
+    if (st != PALU_OK) return st;
+    // a smaller grid only lowers the number of partial slots a stream needs
+    pl->grid = (int)std::min<int64_t>(pl->grid, (int64_t)sms * std::min(per_sm, 4));
+  }
   pl->ws_bytes = align_up(sizeof(float) * (size_t)streams * pl->seg_max * Gq * (2 + pl->rvp), 256);
   return PALU_OK;
 }
