@@ -185,12 +185,13 @@ palu_status palu_decode_workspace_size(const palu_cache* k, const palu_cache* v,
  *        h / (q_heads / kv_heads).
  *   out  device [batch, q_heads, D], fp32 if out_fp32 else fp16.
  *   softmax_scale 0 selects 1/sqrt(D).
- *   workspace  device scratch of palu_decode_workspace_size bytes for the
- *        per-stream partial results; no initial contents are needed.
- * k and v must have the same batch, kv_heads and length.  One kernel launch;
- * the key cache's state holds one merge counter per (batch, KV head) stream
- * that each call leaves at zero, so calls on the same key cache must not
- * overlap on the GPU (issue them on one stream, as appends already are). */
+ *   workspace  device scratch of palu_decode_workspace_size bytes (packed
+ *        query factors and per-stream partial results); no initial contents
+ *        are needed.
+ * k and v must have the same batch, kv_heads and length.  Three kernel
+ * launches on `stream` (query factors, the split attention over the code
+ * blocks, the per-stream combine); calls that share a workspace must not
+ * overlap on the GPU. */
 palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v, const void* q,
                              int32_t q_heads, float softmax_scale, void* out, int32_t out_fp32,
                              void* workspace, size_t workspace_bytes, void* stream);

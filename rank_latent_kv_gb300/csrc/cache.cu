@@ -536,7 +536,7 @@ extern "C" palu_status palu_cache_size(const palu_config* cfg, int32_t role, int
   const bool quant = cfg->quantize || role == PALU_ROLE_KEY;
   if (block_bytes) *block_bytes = align_up((size_t)batch * kv_heads * n_blk * g.rec_bytes, 256);
   if (tail_bytes) *tail_bytes = quant ? align_up(sizeof(float) * (size_t)batch * kv_heads * kBlock * rank, 256) : 0;
-  if (state_bytes) *state_bytes = state_layout(cfg->n_head_groups, rank, batch * (int64_t)kv_heads).total;
+  if (state_bytes) *state_bytes = state_layout(cfg->n_head_groups, rank).total;
   return PALU_OK;
 }
 
@@ -576,11 +576,9 @@ extern "C" palu_status palu_cache_init(palu_cache* cache, const palu_config* cfg
   c.tail = quant ? static_cast<float*>(tail) : nullptr;
   c.state = state;
   c.length = 0;
-  const StateLayout sl = state_layout(c.n_groups, rank, batch * (int64_t)kv_heads);
+  const StateLayout sl = state_layout(c.n_groups, rank);
   uint8_t* s = static_cast<uint8_t*>(state);
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
-  st = cuda_check(cudaMemsetAsync(s + sl.tk_off, 0, sl.total - sl.tk_off, strm), "cudaMemsetAsync(tickets)");
-  if (st != PALU_OK) return st;
   cache_init_kernel<<<dim3(rank, c.n_groups), kHeadDim, 0, strm>>>(
       basis, basis_ld, mu, reinterpret_cast<float*>(s + sl.basis_off), reinterpret_cast<float*>(s + sl.mu_off),
       reinterpret_cast<float2*>(s + sl.mv_off), reinterpret_cast<StateHeader*>(s), rank);

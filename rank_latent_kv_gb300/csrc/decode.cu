@@ -11,11 +11,272 @@
 
 namespace palu {
 
+// ------------------------------------------------------------------ q-prep
+// One CTA per (batch, KV head) stream: q~ = q V^K and c = q . mu^K for its
+// query heads, scaled by softmax scale * log2 e, and for the decode kernel the
+// per-lane fp16 hi/lo factors prescaled by 2^e with
+// |q~| 2^e max(1, largest stored scale) < 2^14, so that every fp16 operand and
+// product of the score MMAs stays finite.
+__global__ void __launch_bounds__(256) latent_qprep_kernel(const DecodeParams p) {
+  __shared__ __align__(16) float q_s[8][kHeadDim];
+  __shared__ __align__(16) float mu_s[kHeadDim];
+  __shared__ float B_s[32 * 129];
+  __shared__ __align__(16) float qt_s[8][kHeadDim];
+  __shared__ float red_s[8], cq_s[8];
+  grid_dep_launch();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long X = blockIdx.x;
+  const int b = (int)(X / p.Hkv), kh = (int)(X % p.Hkv), Gq = p.Gq;
+  const int gk = kh / p.k.heads_per_group;
+  const int npch = 8 * p.k.n_oct;
+  const float* basis_g = p.k.basisT + (size_t)gk * p.k.r * kHeadDim;
+  {
+    const int h = tid >> 5, d4 = tid & 31;
+    float4 qv = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (h < Gq) {
+      const uint2 raw =
+          __ldg(reinterpret_cast<const uint2*>(p.q + ((long long)b * p.Hq + (long long)kh * Gq + h) * kHeadDim) + d4);
+      const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+      const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+      qv = make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+    *reinterpret_cast<float4*>(&q_s[h][4 * d4]) = qv;
+    if (tid < 32)
+      *reinterpret_cast<float4*>(&mu_s[4 * tid]) = __ldg(reinterpret_cast<const float4*>(p.k.mu + (size_t)gk * kHeadDim) + tid);
+    for (int i = tid; i < 8 * kHeadDim; i += 256)
+      if ((i & (kHeadDim - 1)) >= npch) qt_s[i >> 7][i & (kHeadDim - 1)] = 0.f;
+  }
+  float amax = 0.f;
+  for (int ch = 0; ch < npch; ch += 32) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = tid + 256 * u, r = i >> 5, c4 = i & 31, pch = ch + r;
+      const int j = pch < npch ? padded_to_channel(pch, p.k.r, p.k.n_hi, p.k.n_hi_oct, 1) : -1;
+      v[u] = j >= 0 ? __ldg(reinterpret_cast<const float4*>(basis_g + (size_t)j * kHeadDim) + c4)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (ch > 0) __syncthreads();  // the previous chunk's readers are done
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = tid + 256 * u, r = i >> 5, c4 = i & 31;
+      float* dst = B_s + r * 129 + 4 * c4;
+      dst[0] = v[u].x;
+      dst[1] = v[u].y;
+      dst[2] = v[u].z;
+      dst[3] = v[u].w;
+    }
+    __syncthreads();
+    const float* br = B_s + lane * 129;
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll 8
+    for (int d4 = 0; d4 < kHeadDim / 4; ++d4) {
+      const float4 q4 = *reinterpret_cast<const float4*>(&q_s[warp][4 * d4]);
+      a0 = fmaf(q4.x, br[4 * d4], fmaf(q4.y, br[4 * d4 + 1], a0));
+      a1 = fmaf(q4.z, br[4 * d4 + 2], fmaf(q4.w, br[4 * d4 + 3], a1));
+    }
+    const int pch = ch + lane;
+    const float qt = (warp < Gq && pch < npch) ? (a0 + a1) * p.scale_log2 : 0.f;
+    if (pch < kHeadDim) qt_s[warp][pch] = qt;
+    amax = fmaxf(amax, fabsf(qt));
+  }
+  {
+    float s = 0.f;
+    if (warp < Gq) {
+      const float4 qq = *reinterpret_cast<const float4*>(&q_s[warp][4 * lane]);
+      const float4 mm = *reinterpret_cast<const float4*>(&mu_s[4 * lane]);
+      s = fmaf(qq.x, mm.x, fmaf(qq.y, mm.y, fmaf(qq.z, mm.z, qq.w * mm.w)));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      s += __shfl_xor_sync(0xffffffffu, s, o);
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    }
+    if (lane == 0) {
+      red_s[warp] = amax;
+      cq_s[warp] = s * p.scale_log2;
+    }
+  }
+  __syncthreads();
+  // scaled q~ and c for the combine's tail tokens
+  for (int i = tid; i < 8 * kHeadDim; i += 256) p.qt[(size_t)X * 8 * kHeadDim + i] = qt_s[i >> 7][i & (kHeadDim - 1)];
+  if (tid < 8) p.cq[(size_t)X * 8 + tid] = cq_s[tid];
+  if (warp == 0) {
+    amax = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) amax = fmaxf(amax, red_s[w]);
+    const float max_s = __uint_as_float(__ldcg(&p.k.hdr->max_scale));
+    const float xm = amax * fmaxf(1.f, max_s);
+    int e = 0;
+    if (xm > 0.f) {
+      const int ex = (int)((__float_as_uint(xm) >> 23) & 0xFF) - 126;  // xm < 2^ex
+      e = min(max(14 - ex, -120), 120);
+    }
+    const float two_e = pow2i(e), inv2e = pow2i(-e);
+    const int g = lane >> 2, c = lane & 3, ko = p.qp_ko;
+    uint32_t* qp = p.qpack + ((size_t)X * 32 + lane) * p.qp_stride;
+    for (int o = 0; o < ko; ++o) {
+      const float x0 = 8 * o + 2 * c < kHeadDim ? qt_s[g][8 * o + 2 * c] * two_e : 0.f;
+      const float x1 = 8 * o + 2 * c + 1 < kHeadDim ? qt_s[g][8 * o + 2 * c + 1] * two_e : 0.f;
+      const uint32_t hi = pack_f16x2(x0, x1);
+      const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+      qp[o] = hi;
+      qp[ko + o] = pack_f16x2(x0 - hf.x, x1 - hf.y);
+    }
+    qp[2 * ko] = __float_as_uint(cq_s[2 * c] * two_e);
+    qp[2 * ko + 1] = __float_as_uint(cq_s[2 * c + 1] * two_e);
+    qp[2 * ko + 2] = __float_as_uint(two_e);
+    qp[2 * ko + 3] = __float_as_uint(inv2e);
+  }
+}
+
+// ------------------------------------------------------------------ combine
+// One CTA per stream, after the decode kernel: merge the stream's partials
+// (log-sum-exp), fold in the fp32 tail tokens, apply V^V^T and + mu^V.
+// Dynamic shared memory: V basis [rv][128], tails, partials, tail weights,
+// merged latents, denominators.
+__global__ void __launch_bounds__(256) latent_combine_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint64_t mbar;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long X = blockIdx.x;
+  const int b = (int)(X / p.Hkv), kh = (int)(X % p.Hkv), Gq = p.Gq;
+  const int rk = p.k.r, rv = p.v.r, ms = 2 + p.rvp;
+  const int gv = kh / p.v.heads_per_group;
+  const int rec_v = p.v.rec_bytes;
+  const int tv_bytes = p.v.quantize ? kBlock * rv * 4 : rec_v;
+  float* BV_s = reinterpret_cast<float*>(smem);                 // [rv][128]
+  float* TK_s = BV_s + (size_t)rv * kHeadDim;                    // [32][rk]
+  float* TV_s = TK_s + (size_t)kBlock * rk;                      // [32][rv] (or one fp16 record)
+  float* P_s = TV_s + (tv_bytes + 15) / 16 * 4;                  // [nseg][Gq][ms] partials
+  float* ST_s = P_s + (size_t)p.seg_max * Gq * ms;               // [8][32] tail scores, then weights
+  float* O_s = ST_s + 8 * kBlock;                                // [8][128] merged latents
+  float* L_s = O_s + 8 * kHeadDim;                               // [8]
+
+  // everything but the partials and q~ was written before the q-prep launch:
+  // fetch it while the decode kernel is still running
+  const long long len = __ldcg(&p.k.hdr->length);
+  const long long nf = len / kBlock;
+  const int n_tail = (int)(len % kBlock);
+  const long long T = p.streams * nf;
+  int nseg = 0;
+  if (T > 0) {
+    const long long G = min((long long)p.dec_grid, T);
+    nseg = (int)(block_owner(X * nf + nf - 1, T, G) - block_owner(X * nf, T, G) + 1);
+  }
+  if (tid == 0) {
+    mbar_init(&mbar, 1);
+    fence_mbar_init();
+    const uint32_t bytes = (uint32_t)rv * 512u + (n_tail > 0 ? (uint32_t)(kBlock * rk * 4 + tv_bytes) : 0u);
+    mbar_arrive_expect_tx(&mbar, bytes);
+    bulk_g2s(BV_s, p.v.basisT + (size_t)gv * rv * kHeadDim, (uint32_t)rv * 512u, &mbar);
+    if (n_tail > 0) {
+      bulk_g2s(TK_s, p.k.tail + (size_t)X * kBlock * rk, (uint32_t)(kBlock * rk * 4), &mbar);
+      const void* tv = p.v.quantize ? static_cast<const void*>(p.v.tail + (size_t)X * kBlock * rv)
+                                    : static_cast<const void*>(p.v.blocks + ((size_t)X * p.v.n_blk_cap + nf) * rec_v);
+      bulk_g2s(TV_s, tv, (uint32_t)tv_bytes, &mbar);
+    }
+  }
+  grid_dep_wait();  // the decode kernel's partials (and, through it, q~ and c)
+  const float* wsx = p.ws + (size_t)X * p.seg_max * Gq * ms;
+  for (int i = tid; i < nseg * Gq * ms; i += 256) P_s[i] = __ldcg(wsx + i);
+  __syncthreads();  // barrier initialised, partials staged
+  const bool got = mbar_wait_bounded(&mbar, 0);
+  if (!got && tid == 0) set_dev_error(p.k.hdr, PALU_DEVERR_TIMEOUT);
+  // tail scores (log2 units)
+  const float* qt = p.qt + (size_t)X * 8 * kHeadDim;
+  for (int i = tid; i < n_tail * 8; i += 256) {
+    const int t = i >> 3, h = i & 7;
+    float sc_t = -INFINITY;
+    if (h < Gq) {
+      sc_t = __ldcg(p.cq + (size_t)X * 8 + h);
+      for (int j2 = 0; j2 < rk; ++j2) {
+        const int pch = j2 < p.k.n_hi ? j2 : 8 * p.k.n_hi_oct + (j2 - p.k.n_hi);
+        sc_t = fmaf(__ldcg(qt + h * kHeadDim + pch), TK_s[t * rk + j2], sc_t);
+      }
+    }
+    ST_s[h * kBlock + t] = sc_t;
+  }
+  __syncthreads();
+  // warp h: max, weights (over the partials' m), denominator
+  if (warp < Gq) {
+    const int h = warp;
+    float M = -INFINITY;
+    for (int sg = lane; sg < nseg; sg += 32) M = fmaxf(M, P_s[(sg * Gq + h) * ms]);
+    const float st = lane < n_tail ? ST_s[h * kBlock + lane] : -INFINITY;
+    M = fmaxf(M, st);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    for (int sg = lane; sg < nseg; sg += 32) {
+      const float m = P_s[(sg * Gq + h) * ms];
+      const float w = m == -INFINITY ? 0.f : ex2(m - M);
+      L = fmaf(w, P_s[(sg * Gq + h) * ms + 1], L);
+      P_s[(sg * Gq + h) * ms] = w;
+    }
+    const float pt = lane < n_tail ? ex2(st - M) : 0.f;
+    L += pt;
+    __syncwarp();
+    ST_s[h * kBlock + lane] = pt;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) L_s[h] = L;
+  }
+  __syncthreads();
+  // merged latent per (head, real value channel)
+  for (int i = tid; i < Gq * p.rvp; i += 256) {
+    const int h = i / p.rvp, pch = i - h * p.rvp;
+    const int j2 = padded_to_channel(pch, rv, p.v.n_hi, p.v.n_hi_oct, p.v.quantize);
+    if (j2 < 0) continue;
+    float a = 0.f;
+    for (int sg = 0; sg < nseg; ++sg) a = fmaf(P_s[(sg * Gq + h) * ms], P_s[(sg * Gq + h) * ms + 2 + pch], a);
+    for (int t = 0; t < n_tail; ++t) {
+      float lv;
+      if (p.v.quantize) {
+        lv = TV_s[t * rv + j2];
+      } else {
+        const int kk = 2 * (t >> 4) + ((t & 15) >> 3);
+        const int ln = 4 * (j2 & 7) + ((t & 7) >> 1);
+        lv = __half2float(*reinterpret_cast<const __half*>(reinterpret_cast<const uint8_t*>(TV_s) + 512 * (j2 >> 3) +
+                                                           16 * ln + 4 * kk + 2 * (t & 1)));
+      }
+      a = fmaf(ST_s[h * kBlock + t], lv, a);
+    }
+    O_s[h * kHeadDim + j2] = a;
+  }
+  __syncthreads();
+  // out[h][d] = (sum_j o_hj V[d, j]) / L_h + mu[d]
+  {
+    const int d = tid & 127, h0 = (tid >> 7) * 4;
+    float o4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int j2 = 0; j2 < rv; ++j2) {
+      const float bv = BV_s[j2 * kHeadDim + d];
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) o4[hh] = fmaf(O_s[(h0 + hh) * kHeadDim + j2], bv, o4[hh]);
+    }
+    const float mu = __ldg(p.v.mu + (size_t)gv * kHeadDim + d);
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+      const int h = h0 + hh;
+      if (h < Gq) {
+        const float v = fmaf(o4[hh], 1.f / L_s[h], mu);
+        const long long oi = ((long long)b * p.Hq + (long long)kh * Gq + h) * kHeadDim + d;
+        if (p.out_fp32)
+          static_cast<float*>(p.out)[oi] = v;
+        else
+          static_cast<__half*>(p.out)[oi] = __float2half_rn(v);
+      }
+    }
+  }
+}
+
 struct DecodePlan {
   int KC, VC;
   bool VQ;
-  int ns, stage_bytes, ring_off, smem, grid, seg_max, rvp;
-  size_t ws_bytes;
+  int ns, stage_bytes, ring_off, smem, grid, seg_max, rvp, qp_ko, qp_stride;
+  size_t comb_smem;
+  size_t qpack_off, qt_off, cq_off, part_off, ws_bytes;
   DecodeKernel kern;
 };
 
@@ -61,48 +322,46 @@ static palu_status plan_decode(const palu_cache* k, const palu_cache* v, int32_t
   if (pl->KC != k->n_hi_oct) return fail(PALU_ERR_UNSUPPORTED, "unexpected key record layout");
   pl->kern = pick_kernel(k->n_oct, v->n_oct, pl->KC, pl->VC, pl->VQ);
   if (!pl->kern) return fail(PALU_ERR_UNSUPPORTED, "no decode kernel for this rank");
+  pl->qp_ko = (k->n_oct <= 8 && v->n_oct <= 8) ? k->n_oct : 4 * pl->KC;  // the kernel's key octets
+  pl->qp_stride = (2 * pl->qp_ko + 4 + 3) / 4 * 4;
   const int rec_k = k->record_bytes, rec_v = v->record_bytes;
   pl->stage_bytes = 2 * (rec_k + rec_v);
   pl->ns = pl->stage_bytes <= 2048 ? 4 : pl->stage_bytes <= 6144 ? 3 : 2;
   pl->rvp = 8 * v->n_oct;
-  pl->ring_off = (int)align_up(kDecBarOff + 8 * (kDecWarps * pl->ns + 1), 128);
+  pl->ring_off = (int)align_up(kDecBarOff + 8 * kDecWarps * pl->ns, 128);
   const int64_t streams = (int64_t)k->batch * k->kv_heads;
   const int sms = device_sm_count();
-  // shared memory: header, then the rings, which the merges reuse; the merge
-  // layout needs the partial slots per stream, which follow from the grid,
-  // which follows from the occupancy
   const size_t rings = std::max((size_t)kDecWarps * pl->ns * pl->stage_bytes,
                                 (size_t)kDecWarps * 8 * (2 + pl->rvp) * 4);
+  pl->smem = (int)(pl->ring_off + rings);
+  if (pl->smem > 227 * 1024) return fail(PALU_ERR_UNSUPPORTED, "decode shared-memory plan exceeds 227 KB");
   int per_sm = 0;
-  palu_status st = kernel_occupancy(reinterpret_cast<const void*>(pl->kern), kDecThreads,
-                                    (int)(pl->ring_off + rings), &per_sm);
+  palu_status st = kernel_occupancy(reinterpret_cast<const void*>(pl->kern), kDecThreads, pl->smem, &per_sm);
   if (st != PALU_OK) return st;
   int64_t grid = (int64_t)sms * std::min(per_sm, 4);
-  grid = std::min<int64_t>(grid, std::max<int64_t>(streams, streams * k->n_blk_cap));
+  grid = std::min<int64_t>(grid, std::max<int64_t>(1, streams * k->n_blk_cap));
   pl->grid = (int)std::max<int64_t>(1, grid);
+  // the combine stages one stream's partials on chip: with few streams, use
+  // fewer CTAs so that they fit
   const int tv_bytes = v->quantize ? kBlock * v->rank * 4 : rec_v;
-  const size_t merge_fixed = (size_t)v->rank * 512 + (size_t)128 * k->rank + align_up(tv_bytes, 16) +
-                             8 * kBlock * 4 + 8 * kHeadDim * 4 + 32;
+  const size_t comb_fixed = (size_t)v->rank * 512 + (size_t)128 * k->rank + align_up(tv_bytes, 16) +
+                            8 * kBlock * 4 + 8 * kHeadDim * 4 + 32;
   const size_t per_seg = (size_t)Gq * (2 + pl->rvp) * 4;
+  const size_t comb_budget = 200 * 1024;
   pl->seg_max = (int)((pl->grid + streams - 1) / streams + 1);
-  const size_t merge_budget = 200 * 1024 - (size_t)pl->ring_off;
-  if (merge_fixed + pl->seg_max * per_seg > merge_budget) {
-    // few streams: fewer CTAs, so that one stream's partials fit on chip
-    const int64_t seg_fit = (int64_t)((merge_budget - merge_fixed) / per_seg);
+  if (comb_fixed + pl->seg_max * per_seg > comb_budget) {
+    const int64_t seg_fit = (int64_t)((comb_budget - comb_fixed) / per_seg);
     if (seg_fit < 2) return fail(PALU_ERR_UNSUPPORTED, "decode merge does not fit in shared memory");
     pl->grid = (int)std::max<int64_t>(1, std::min<int64_t>(pl->grid, streams * (seg_fit - 1)));
     pl->seg_max = (int)((pl->grid + streams - 1) / streams + 1);
   }
-  const size_t merge_bytes = merge_fixed + pl->seg_max * per_seg;
-  pl->smem = (int)(pl->ring_off + std::max(rings, merge_bytes));
-  if (pl->smem > 227 * 1024) return fail(PALU_ERR_UNSUPPORTED, "decode shared-memory plan exceeds 227 KB");
-  if (merge_bytes > rings) {
-    st = kernel_occupancy(reinterpret_cast<const void*>(pl->kern), kDecThreads, pl->smem, &per_sm);
-    if (st != PALU_OK) return st;
-    // a smaller grid only lowers the number of partial slots a stream needs
-    pl->grid = (int)std::min<int64_t>(pl->grid, (int64_t)sms * std::min(per_sm, 4));
-  }
-  pl->ws_bytes = align_up(sizeof(float) * (size_t)streams * pl->seg_max * Gq * (2 + pl->rvp), 256);
+  pl->comb_smem = comb_fixed + pl->seg_max * per_seg;
+  // workspace: packed query factors, q~ and c per stream, partials
+  pl->qpack_off = 0;
+  pl->qt_off = align_up(pl->qpack_off + sizeof(uint32_t) * (size_t)streams * 32 * pl->qp_stride, 256);
+  pl->cq_off = align_up(pl->qt_off + sizeof(float) * (size_t)streams * 8 * kHeadDim, 256);
+  pl->part_off = align_up(pl->cq_off + sizeof(float) * (size_t)streams * 8, 256);
+  pl->ws_bytes = align_up(pl->part_off + sizeof(float) * (size_t)streams * pl->seg_max * Gq * (2 + pl->rvp), 256);
   return PALU_OK;
 }
 
@@ -138,7 +397,11 @@ extern "C" palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v
   p.v = make_view(v);
   p.q = static_cast<const __half*>(q);
   p.out = out;
-  p.ws = static_cast<float*>(workspace);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.qpack = reinterpret_cast<uint32_t*>(ws + pl.qpack_off);
+  p.qt = reinterpret_cast<float*>(ws + pl.qt_off);
+  p.cq = reinterpret_cast<float*>(ws + pl.cq_off);
+  p.ws = reinterpret_cast<float*>(ws + pl.part_off);
   p.out_fp32 = out_fp32;
   p.Hq = q_heads;
   p.Hkv = k->kv_heads;
@@ -148,12 +411,38 @@ extern "C" palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v
   p.stage_bytes = pl.stage_bytes;
   p.ring_off = pl.ring_off;
   p.seg_max = pl.seg_max;
+  p.qp_ko = pl.qp_ko;
+  p.qp_stride = pl.qp_stride;
+  p.dec_grid = pl.grid;
   p.streams = (long long)k->batch * k->kv_heads;
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)kHeadDim);
   p.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
-  pl.kern<<<pl.grid, kDecThreads, pl.smem, strm>>>(p);
-  return cuda_check(cudaGetLastError(), "latent_decode_kernel launch");
+  const unsigned int n_streams = (unsigned int)p.streams;
+  latent_qprep_kernel<<<n_streams, 256, 0, strm>>>(p);
+  st = cuda_check(cudaGetLastError(), "latent_qprep_kernel launch");
+  if (st != PALU_OK) return st;
+  int per_sm = 0;
+  st = kernel_occupancy(reinterpret_cast<const void*>(latent_combine_kernel), 256, (int)pl.comb_smem, &per_sm);
+  if (st != PALU_OK) return st;
+  // decode and combine each start while their predecessor finishes
+  // (programmatic dependent launch; each waits in-kernel for the results)
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.grid);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = strm;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  st = cuda_check(cudaLaunchKernelEx(&cfg, pl.kern, p), "latent_decode_kernel launch");
+  if (st != PALU_OK) return st;
+  cfg.gridDim = dim3(n_streams);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = pl.comb_smem;
+  return cuda_check(cudaLaunchKernelEx(&cfg, latent_combine_kernel, p), "latent_combine_kernel launch");
 }
 
 // ------------------------------------------------------------------ allocation-free decode

@@ -48,29 +48,28 @@ namespace palu {
 
 constexpr int kDecWarps = 8;
 constexpr int kDecThreads = 32 * kDecWarps;
-constexpr float kLazyTau = 8.f;     // log2 headroom before the running max is raised
-// shared-memory header of a decode CTA (byte offsets)
-constexpr int kDecQOff = 0;                           // q_s   fp32 [8][128]
-constexpr int kDecQtOff = 4096;                       // qt_s  fp32 [8][128] scaled q~ per padded key channel
-constexpr int kDecMuOff = 8192;                       // mu_s  fp32 [128]
-constexpr int kDecCqOff = 8704;                       // cq_s  fp32 [8]
-constexpr int kDecRedOff = 8736;                      // red_s fp32 [8]
-constexpr int kDecFlagOff = 8768;                     // flags int [4]
-constexpr int kDecBsOff = 8832;                       // B_s   fp32 [32][129] key basis rows (prologue)
-constexpr int kDecBarOff = kDecBsOff + 32 * 129 * 4;  // mbarriers: [warps][ns], then the merge barrier
+constexpr float kLazyTau = 8.f;   // log2 headroom before the running max is raised
+constexpr int kDecFlagOff = 0;    // decode CTA shared memory: flags int [4]
+constexpr int kDecBarOff = 64;    // then mbarriers [warps][ns]; the rings follow
 
 struct DecodeParams {
   CacheView k, v;
   const __half* q;
   void* out;
+  uint32_t* qpack;    // per stream and lane: Qh[ko], Ql[ko], CQ0, CQ1, 2^e, 2^-e  (qp_stride words)
+  float* qt;          // per stream: scaled q~ [8][128] per padded key channel
+  float* cq;          // per stream: scaled q . mu^K [8]
   float* ws;          // partials [streams][seg_max][Gq][2 + rvp]
   int out_fp32;
   int Hq, Hkv, Gq;
   int rvp;            // padded value channels = 8 * v.n_oct
   int ns;             // stages per warp ring
   int stage_bytes;    // 2 * (k.rec_bytes + v.rec_bytes)
-  int ring_off;       // shared-memory offset of the rings (reused by the merges)
+  int ring_off;       // shared-memory offset of the rings
   int seg_max;        // partial slots per stream
+  int qp_ko;          // key octets held per lane in qpack
+  int qp_stride;      // words per lane in qpack
+  int dec_grid;       // CTAs of the decode launch
   long long streams;  // batch * kv_heads
   float scale_log2;   // softmax scale * log2(e)
 };
@@ -109,6 +108,10 @@ __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Programmatic dependent launch: wait for the preceding launch's results /
+// let the next launch be scheduled.  Both are no-ops without the attribute.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ uint32_t ld32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 __device__ __forceinline__ uint32_t ld16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
 
@@ -121,20 +124,40 @@ __device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) 
 // mantissa of an fp16 power of two 2^E whose unit in the last place lines up
 // with the field's lowest bit gives 2^E + code, and one subtraction leaves the
 // code.
-__device__ __forceinline__ void unpack_hi(uint32_t w, uint32_t R[4]) {
+// (a & mask) | magic in one LOP3: the mask is an immediate, the magic comes
+// in a register (an instruction takes one 32-bit immediate at most)
+template <uint32_t kMask>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(kMask), "r"(magic));
+  return d;
+}
+struct Magic {
+  uint32_t m1024, m256, m64, m16;  // fp16x2 (2^E, 2^E) for E = 10, 8, 6, 4
+};
+__device__ __forceinline__ Magic make_magic() {
+  Magic m;
+  // through an opaque move so that the values stay in registers
+  asm("mov.b32 %0, 0x64006400;" : "=r"(m.m1024));
+  asm("mov.b32 %0, 0x5C005C00;" : "=r"(m.m256));
+  asm("mov.b32 %0, 0x54005400;" : "=r"(m.m64));
+  asm("mov.b32 %0, 0x4C004C00;" : "=r"(m.m16));
+  return m;
+}
+__device__ __forceinline__ void unpack_hi(uint32_t w, const Magic& mg, uint32_t R[4]) {
   const uint32_t w8 = w >> 8;
-  R[0] = sub_f16x2((w & 0x000F000Fu) | 0x64006400u, 0x64006400u);   // 1024 + c
-  R[1] = sub_f16x2((w & 0x00F000F0u) | 0x54005400u, 0x54005400u);   //   64 + c
-  R[2] = sub_f16x2((w8 & 0x000F000Fu) | 0x64006400u, 0x64006400u);
-  R[3] = sub_f16x2((w8 & 0x00F000F0u) | 0x54005400u, 0x54005400u);
+  R[0] = sub_f16x2(and_or<0x000F000Fu>(w, mg.m1024), mg.m1024);   // 1024 + c
+  R[1] = sub_f16x2(and_or<0x00F000F0u>(w, mg.m64), mg.m64);       //   64 + c
+  R[2] = sub_f16x2(and_or<0x000F000Fu>(w8, mg.m1024), mg.m1024);
+  R[3] = sub_f16x2(and_or<0x00F000F0u>(w8, mg.m64), mg.m64);
 }
 // hw: the octet's 16 bits (half 0 in bits 0-7, half 1 in bits 8-15).
-__device__ __forceinline__ void unpack_lo(uint32_t hw, uint32_t R[4]) {
+__device__ __forceinline__ void unpack_lo(uint32_t hw, const Magic& mg, uint32_t R[4]) {
   const uint32_t w = __byte_perm(hw, 0u, 0x4140);
-  R[0] = sub_f16x2((w & 0x00030003u) | 0x64006400u, 0x64006400u);   // 1024 + c
-  R[1] = sub_f16x2((w & 0x000C000Cu) | 0x5C005C00u, 0x5C005C00u);   //  256 + c
-  R[2] = sub_f16x2((w & 0x00300030u) | 0x54005400u, 0x54005400u);   //   64 + c
-  R[3] = sub_f16x2((w & 0x00C000C0u) | 0x4C004C00u, 0x4C004C00u);   //   16 + c
+  R[0] = sub_f16x2(and_or<0x00030003u>(w, mg.m1024), mg.m1024);   // 1024 + c
+  R[1] = sub_f16x2(and_or<0x000C000Cu>(w, mg.m256), mg.m256);     //  256 + c
+  R[2] = sub_f16x2(and_or<0x00300030u>(w, mg.m64), mg.m64);       //   64 + c
+  R[3] = sub_f16x2(and_or<0x00C000C0u>(w, mg.m16), mg.m16);       //   16 + c
 }
 
 // Record geometry of one cache as the kernel sees it.  C is the record class
@@ -192,23 +215,15 @@ __device__ __forceinline__ void mma16816_c(float d[4], uint32_t a0, uint32_t a1,
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
 }
-__device__ __forceinline__ void mma16816_0(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                           uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%10,%10,%10,%10};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
-}
-
 // One key octet of one block: exact codes, the B pair (hi, lo) of
 // Q~ * s for the lane's head g and channels 2c, 2c+1, and the zero points.
 template <class GK>
 __device__ __forceinline__ void key_octet(const uint8_t* kr, const GK& gk, int o, uint32_t qh, uint32_t ql,
-                                          int lane, int c, uint32_t R[4], uint32_t& bh, uint32_t& bl,
-                                          uint32_t& z) {
+                                          int lane, int c, const Magic& mg, uint32_t R[4], uint32_t& bh,
+                                          uint32_t& bl, uint32_t& z) {
   constexpr int KC = (GK::kMaxOct + 3) / 4;
-  if (o < KC) unpack_hi(ld32(kr + gk.word_off(o, lane)), R);
-  else unpack_lo(ld16(kr + gk.word_off(o, lane)), R);
+  if (o < KC) unpack_hi(ld32(kr + gk.word_off(o, lane)), mg, R);
+  else unpack_lo(ld16(kr + gk.word_off(o, lane)), mg, R);
   const uint32_t s2 = ld32(kr + gk.sz() + 16 * o + 4 * c);
   z = ld32(kr + gk.z() + 16 * o + 4 * c);
   bh = hmul2(qh, s2);
@@ -222,7 +237,8 @@ __device__ __forceinline__ void key_octet(const uint8_t* kr, const GK& gk, int o
 template <class GK>
 __device__ __forceinline__ void key_stage(const uint8_t* kr0, const uint8_t* kr1, const GK& gk,
                                           const uint32_t (&Qh)[GK::kMaxOct], const uint32_t (&Ql)[GK::kMaxOct],
-                                          const float (&CQ)[4], int lane, int c, float sc[2][2][4], float zc[4]) {
+                                          const float (&CQ)[4], const float (&Z4)[4], int lane, int c, const Magic& mg,
+                                          float sc[2][2][4], float zc[4]) {
   constexpr int KO = GK::kMaxOct;
 #pragma unroll
   for (int t = 0; t < (KO + 1) / 2; ++t) {
@@ -233,9 +249,9 @@ __device__ __forceinline__ void key_stage(const uint8_t* kr0, const uint8_t* kr1
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
       const uint8_t* kr = b ? kr1 : kr0;
-      key_octet(kr, gk, oa, Qh[oa], Ql[oa], lane, c, R[b][0], Bh[b][0], Bl[b][0], Z[b][0]);
+      key_octet(kr, gk, oa, Qh[oa], Ql[oa], lane, c, mg, R[b][0], Bh[b][0], Bl[b][0], Z[b][0]);
       if (pb) {
-        key_octet(kr, gk, ob, Qh[ob], Ql[ob], lane, c, R[b][1], Bh[b][1], Bl[b][1], Z[b][1]);
+        key_octet(kr, gk, ob, Qh[ob], Ql[ob], lane, c, mg, R[b][1], Bh[b][1], Bl[b][1], Z[b][1]);
       } else {
         R[b][1][0] = R[b][1][1] = R[b][1][2] = R[b][1][3] = 0u;
         Bh[b][1] = Bl[b][1] = Z[b][1] = 0u;
@@ -250,8 +266,8 @@ __device__ __forceinline__ void key_stage(const uint8_t* kr0, const uint8_t* kr1
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         if (t == 0)
-          mma16816_0(sc[b][m], R[b][0][2 * m], R[b][0][2 * m + 1], R[b][1][2 * m], R[b][1][2 * m + 1], Bh[b][0],
-                     Bh[b][1]);
+          mma16816_c(sc[b][m], R[b][0][2 * m], R[b][0][2 * m + 1], R[b][1][2 * m], R[b][1][2 * m + 1], Bh[b][0],
+                     Bh[b][1], Z4);
         else
           mma16816(sc[b][m], R[b][0][2 * m], R[b][0][2 * m + 1], R[b][1][2 * m], R[b][1][2 * m + 1], Bh[b][0],
                    Bh[b][1]);
@@ -265,17 +281,20 @@ __device__ __forceinline__ void key_stage(const uint8_t* kr0, const uint8_t* kr1
 // ---- one value octet: fp16 latents for the lane's channel g of octet o and
 // tokens (field k): registers k = 0..3.
 template <bool VQ, class GV>
-__device__ __forceinline__ void value_octet(const uint8_t* vr, int o, const GV& gv, int lane, int g,
+__device__ __forceinline__ void value_octet(const uint8_t* vr, int o, const GV& gv, int lane, int g, const Magic& mg,
                                             uint32_t L[4]) {
   if constexpr (VQ) {
     constexpr int VC = (GV::kMaxOct + 3) / 4;
     uint32_t F[4];
-    if (o < VC) unpack_hi(ld32(vr + gv.word_off(o, lane)), F);
-    else unpack_lo(ld16(vr + gv.word_off(o, lane)), F);
-    const uint32_t sz = ld32(vr + gv.sz() + 4 * (8 * o + g));
-    const uint32_t s2 = __byte_perm(sz, sz, 0x1010), z2 = __byte_perm(sz, sz, 0x3232);
+    if (o < VC) unpack_hi(ld32(vr + gv.word_off(o, lane)), mg, F);
+    else unpack_lo(ld16(vr + gv.word_off(o, lane)), mg, F);
+    const __half2 sz = *reinterpret_cast<const __half2*>(vr + gv.sz() + 4 * (8 * o + g));
+    const __half2 s2 = __low2half2(sz), z2 = __high2half2(sz);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) L[k] = fma_f16x2(F[k], s2, z2);
+    for (int k = 0; k < 4; ++k) {
+      const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&F[k]), s2, z2);
+      L[k] = *reinterpret_cast<const uint32_t*>(&r);
+    }
   } else {
     const uint4 w = *reinterpret_cast<const uint4*>(vr + 512 * o + 16 * lane);
     L[0] = w.x;
@@ -286,7 +305,7 @@ __device__ __forceinline__ void value_octet(const uint8_t* vr, int o, const GV& 
 }
 
 template <bool VQ, class GV>
-__device__ __forceinline__ void value_block(const uint8_t* vr, const GV& gv, int lane, int g,
+__device__ __forceinline__ void value_block(const uint8_t* vr, const GV& gv, int lane, int g, const Magic& mg,
                                             const uint32_t pb[2][2], float acc[(GV::kMaxOct + 1) / 2][4]) {
   constexpr int VO = GV::kMaxOct;
 #pragma unroll
@@ -295,9 +314,9 @@ __device__ __forceinline__ void value_block(const uint8_t* vr, const GV& gv, int
     if (t > 0 && !gv.present(oa)) continue;
     const bool pbr = ob < VO && gv.present(ob);
     uint32_t La[4], Lb[4];
-    value_octet<VQ>(vr, oa, gv, lane, g, La);
+    value_octet<VQ>(vr, oa, gv, lane, g, mg, La);
     if (pbr) {
-      value_octet<VQ>(vr, ob, gv, lane, g, Lb);
+      value_octet<VQ>(vr, ob, gv, lane, g, mg, Lb);
     } else {
       Lb[0] = Lb[1] = Lb[2] = Lb[3] = 0u;
     }
@@ -314,100 +333,93 @@ __device__ __forceinline__ long long block_owner(long long i, long long T, long 
 
 // ------------------------------------------------------------------ the kernel
 // KC, VC: key / value record classes; KE, VE: exact octet counts, or 0 when
-// the kernel serves every count of its class.
+// the kernel serves every count of its class.  Launched after the q-prep
+// kernel (programmatic dependent launch: the first copies are in flight
+// before the packed query factors are read) and before the combine kernel.
 template <int KC, int VC, bool VQ, int KE, int VE>
 __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_decode_kernel(const DecodeParams p) {
   using GK = Geom<KC, KE, true>;
   using GV = Geom<VC, VE, VQ>;
   constexpr int KO = GK::kMaxOct, VT = (GV::kMaxOct + 1) / 2;
   extern __shared__ __align__(128) uint8_t smem[];
-  float* q_s = reinterpret_cast<float*>(smem + kDecQOff);
-  float* qt_s = reinterpret_cast<float*>(smem + kDecQtOff);
-  float* mu_s = reinterpret_cast<float*>(smem + kDecMuOff);
-  float* cq_s = reinterpret_cast<float*>(smem + kDecCqOff);
-  float* red_s = reinterpret_cast<float*>(smem + kDecRedOff);
-  int* flag_s = reinterpret_cast<int*>(smem + kDecFlagOff);  // [0] timed out, [1] this CTA merges
-  float* B_s = reinterpret_cast<float*>(smem + kDecBsOff);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecBarOff);  // [warps][ns], then the merge barrier
+  int* flag_s = reinterpret_cast<int*>(smem + kDecFlagOff);  // [0] timed out
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecBarOff);
   uint8_t* ring = smem + p.ring_off;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+  grid_dep_launch();
   const long long len = __ldcg(&p.k.hdr->length);
   const long long nf = len / kBlock;
   const long long T = p.streams * nf;
   // split over at most T CTAs, so every CTA that takes part owns >= 1 block
   // and the CTAs covering a stream are consecutive
-  const long long G = T > 0 ? min((long long)gridDim.x, T) : (long long)gridDim.x, cta = blockIdx.x;
+  const long long G = min((long long)gridDim.x, T), cta = blockIdx.x;
+  if (tid == 0 && cta == 0 && __ldcg(&p.v.hdr->length) != len) set_dev_error(p.k.hdr, PALU_DEVERR_LENGTH_MISMATCH);
+  if (cta >= G) return;
+  const long long R0 = cta * T / G, R1 = (cta + 1) * T / G;
   const int ns = p.ns, Gq = p.Gq;
   GK geo_k;
   GV geo_v;
   geo_k.init(p.k);
   geo_v.init(p.v);
   const int rec_k = geo_k.rec(), rec_v = geo_v.rec();
-  uint64_t* mbar = bars + kDecWarps * ns;
 
-  if (tid == 0 && cta == 0 && __ldcg(&p.v.hdr->length) != len) set_dev_error(p.k.hdr, PALU_DEVERR_LENGTH_MISMATCH);
-  long long R0 = 0, R1 = 0;
-  if (T > 0) {
-    if (cta >= G) return;
-    R0 = cta * T / G;
-    R1 = (cta + 1) * T / G;
-    if (R0 >= R1) return;
-  } else if (cta >= p.streams) {
-    return;
-  }
-
-  // ---- one-time setup: zeroed rings (a stage's unused second block then
-  // holds finite bytes), barriers
-  {
-    uint4* r4 = reinterpret_cast<uint4*>(ring);
-    const int n16 = kDecWarps * ns * p.stage_bytes / 16;
-    for (int i = tid; i < n16; i += kDecThreads) r4[i] = make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
-  }
+  // ---- one-time setup: barriers
   if (tid == 0) {
-    for (int i = 0; i <= kDecWarps * ns; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < kDecWarps * ns; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
     flag_s[0] = 0;
   }
   __syncthreads();
 
-  const float max_s = __uint_as_float(__ldcg(&p.k.hdr->max_scale));
   uint8_t* wring = ring + (size_t)warp * ns * p.stage_bytes;
   uint64_t* wbar = bars + warp * ns;
-  int slot = 0;           // this warp's next ring slot and its phase parity
+  int slot = 0;  // this warp's next ring slot and its phase parity
   uint32_t par = 0;
-  uint32_t merge_par = 0;
+  bool first = true;
+  const Magic mg = make_magic();
+  // MMA operand quads of repeated constants, each value in its own register
+  // (a zero C operand and an all-ones A operand, fp16x2 (1, 1))
+  float Z4[4];
+  uint32_t O4[4];
+  asm volatile("mov.b32 %0, 0;" : "=f"(Z4[0]));
+  asm volatile("mov.b32 %0, 0;" : "=f"(Z4[1]));
+  asm volatile("mov.b32 %0, 0;" : "=f"(Z4[2]));
+  asm volatile("mov.b32 %0, 0;" : "=f"(Z4[3]));
+  asm volatile("mov.b32 %0, 0x3C003C00;" : "=r"(O4[0]));
+  asm volatile("mov.b32 %0, 0x3C003C00;" : "=r"(O4[1]));
+  asm volatile("mov.b32 %0, 0x3C003C00;" : "=r"(O4[2]));
+  asm volatile("mov.b32 %0, 0x3C003C00;" : "=r"(O4[3]));
 
-  long long X = T > 0 ? R0 / nf : cta;
-  for (;;) {
-    long long b0 = 0, b1 = 0, kslot = 0, nseg = 0;
-    if (T > 0) {
-      if (X * nf >= R1) break;
-      b0 = max(R0, X * nf) - X * nf;
-      b1 = min(R1, (X + 1) * nf) - X * nf;
-      const long long c0 = block_owner(X * nf, T, G);
-      nseg = block_owner(X * nf + nf - 1, T, G) - c0 + 1;
-      kslot = cta - c0;
-    } else if (X >= p.streams) {
-      break;
-    }
-    const int b = (int)(X / p.Hkv), kh = (int)(X % p.Hkv);
+  for (long long X = R0 / nf; X * nf < R1; ++X) {
+    const long long b0 = max(R0, X * nf) - X * nf, b1 = min(R1, (X + 1) * nf) - X * nf;
+    const long long kslot = cta - block_owner(X * nf, T, G);
     const bool dead = flag_s[0] != 0;
 
     // ---- this warp's contiguous share of the segment, two blocks per stage
-    const long long nseg_blk = b1 - b0;
+    const int nseg_blk = (int)(b1 - b0);
     const long long wb0 = b0 + warp * nseg_blk / kDecWarps, wb1 = b0 + (warp + 1) * nseg_blk / kDecWarps;
     const int n_my = (int)(wb1 - wb0), n_st = dead ? 0 : (n_my + 1) >> 1;
-    const uint8_t* kbase = p.k.blocks + (size_t)X * p.k.n_blk_cap * rec_k;
-    const uint8_t* vbase = p.v.blocks + (size_t)X * p.v.n_blk_cap * rec_v;
+    const uint8_t* kbase = p.k.blocks + ((size_t)X * p.k.n_blk_cap + wb0) * rec_k;
+    const uint8_t* vbase = p.v.blocks + ((size_t)X * p.v.n_blk_cap + wb0) * rec_v;
+    // stage i holds blocks 2i, 2i+1 of the warp's range; an odd last stage
+    // holds its block twice (the copy in the second slot is masked), so every
+    // byte the stage is read at is a real record
     auto issue = [&](int i, int s) {
-      const long long blk = wb0 + 2LL * i;
-      const int nb = (int)min(2LL, wb1 - blk);
-      uint8_t* dst = wring + (size_t)s * p.stage_bytes;
-      mbar_arrive_expect_tx(&wbar[s], (uint32_t)(nb * (rec_k + rec_v)));
-      bulk_g2s(dst, kbase + blk * rec_k, (uint32_t)(nb * rec_k), &wbar[s]);
-      bulk_g2s(dst + 2 * rec_k, vbase + blk * rec_v, (uint32_t)(nb * rec_v), &wbar[s]);
+      uint8_t* dst = wring + s * p.stage_bytes;
+      uint64_t* bar = &wbar[s];
+      const uint8_t* ks = kbase + (size_t)(2 * i) * rec_k;
+      const uint8_t* vs = vbase + (size_t)(2 * i) * rec_v;
+      mbar_arrive_expect_tx(bar, (uint32_t)(2 * (rec_k + rec_v)));
+      if (2 * i + 1 < n_my) {
+        bulk_g2s(dst, ks, (uint32_t)(2 * rec_k), bar);
+        bulk_g2s(dst + 2 * rec_k, vs, (uint32_t)(2 * rec_v), bar);
+      } else {
+        bulk_g2s(dst, ks, (uint32_t)rec_k, bar);
+        bulk_g2s(dst + rec_k, ks, (uint32_t)rec_k, bar);
+        bulk_g2s(dst + 2 * rec_k, vs, (uint32_t)rec_v, bar);
+        bulk_g2s(dst + 2 * rec_k + rec_v, vs, (uint32_t)rec_v, bar);
+      }
     };
     if (lane == 0) {
       int s = slot;
@@ -416,106 +428,29 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
         s = s + 1 == ns ? 0 : s + 1;
       }
     }
+    if (first) {
+      grid_dep_wait();  // the q-prep results
+      first = false;
+    }
 
-    // ---- prologue: q, mu^K and the key basis rows come in one batch of
-    // loads; then q~ = q V^K (scaled, per padded key channel, one warp per
-    // head, one lane per channel) and c = q . mu^K
-    const int gk = kh / p.k.heads_per_group;
-    const int npch = 8 * p.k.n_oct;
-    const float* basis_g = p.k.basisT + (size_t)gk * p.k.r * kHeadDim;
-    {
-      const int h = tid >> 5, d4 = tid & 31;
-      float4 qv = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (h < Gq) {
-        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(
-                                    p.q + ((long long)b * p.Hq + (long long)kh * Gq + h) * kHeadDim) + d4);
-        const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-        const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-        qv = make_float4(lo.x, lo.y, hi.x, hi.y);
-      }
-      *reinterpret_cast<float4*>(q_s + h * kHeadDim + 4 * d4) = qv;
-      if (tid < 32) *reinterpret_cast<float4*>(mu_s + 4 * tid) =
-          __ldg(reinterpret_cast<const float4*>(p.k.mu + (size_t)gk * kHeadDim) + tid);
-      for (int i = tid; i < 8 * kHeadDim; i += kDecThreads)
-        if ((i & (kHeadDim - 1)) >= npch) qt_s[i] = 0.f;
-    }
-    float amax = 0.f;
-    for (int ch = 0; ch < npch; ch += 32) {
-      float4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = tid + kDecThreads * u, r = i >> 5, c4 = i & 31, pch = ch + r;
-        const int j = pch < npch ? padded_to_channel(pch, p.k.r, p.k.n_hi, p.k.n_hi_oct, 1) : -1;
-        v[u] = j >= 0 ? __ldg(reinterpret_cast<const float4*>(basis_g + (size_t)j * kHeadDim) + c4)
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      if (ch > 0) __syncthreads();  // the previous chunk's readers are done
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = tid + kDecThreads * u, r = i >> 5, c4 = i & 31;
-        float* dst = B_s + r * 129 + 4 * c4;
-        dst[0] = v[u].x;
-        dst[1] = v[u].y;
-        dst[2] = v[u].z;
-        dst[3] = v[u].w;
-      }
-      __syncthreads();
-      const float* qh = q_s + warp * kHeadDim;
-      const float* br = B_s + lane * 129;
-      float a0 = 0.f, a1 = 0.f;
-#pragma unroll 8
-      for (int d4 = 0; d4 < kHeadDim / 4; ++d4) {
-        const float4 q4 = *reinterpret_cast<const float4*>(qh + 4 * d4);
-        a0 = fmaf(q4.x, br[4 * d4], fmaf(q4.y, br[4 * d4 + 1], a0));
-        a1 = fmaf(q4.z, br[4 * d4 + 2], fmaf(q4.w, br[4 * d4 + 3], a1));
-      }
-      const int pch = ch + lane;
-      const float qt = (warp < Gq && pch < npch) ? (a0 + a1) * p.scale_log2 : 0.f;
-      qt_s[warp * kHeadDim + pch] = qt;
-      amax = fmaxf(amax, fabsf(qt));
-    }
-    {
-      float s = 0.f;
-      if (warp < Gq) {
-        const float4 qq = *reinterpret_cast<const float4*>(q_s + warp * kHeadDim + 4 * lane);
-        const float4 mm = *reinterpret_cast<const float4*>(mu_s + 4 * lane);
-        s = fmaf(qq.x, mm.x, fmaf(qq.y, mm.y, fmaf(qq.z, mm.z, qq.w * mm.w)));
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        s += __shfl_xor_sync(0xffffffffu, s, o);
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      }
-      if (lane == 0) {
-        red_s[warp] = amax;
-        cq_s[warp] = s * p.scale_log2;
-      }
-    }
-    __syncthreads();
-    // 2^e with |q~| 2^e max(1, max_s) < 2^14: every fp16 operand and product in
-    // the score MMAs stays finite.
-    amax = 0.f;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) amax = fmaxf(amax, red_s[w]);
-    const float xm = amax * fmaxf(1.f, max_s);
-    int e = 0;
-    if (xm > 0.f) {
-      const int ex = (int)((__float_as_uint(xm) >> 23) & 0xFF) - 126;  // xm < 2^ex
-      e = min(max(14 - ex, -120), 120);
-    }
-    const float two_e = pow2i(e), inv2e = pow2i(-e);
+    // ---- the lane's query factors for this stream
     uint32_t Qh[KO], Ql[KO];
+    float CQ[4], two_e, inv2e;
+    {
+      const uint32_t* qp = p.qpack + ((size_t)X * 32 + lane) * p.qp_stride;
 #pragma unroll
-    for (int o = 0; o < KO; ++o) {
-      const float x0 = qt_s[g * kHeadDim + 8 * o + 2 * c] * two_e;
-      const float x1 = qt_s[g * kHeadDim + 8 * o + 2 * c + 1] * two_e;
-      Qh[o] = pack_f16x2(x0, x1);
-      const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&Qh[o]));
-      Ql[o] = pack_f16x2(x0 - hf.x, x1 - hf.y);
+      for (int o = 0; o < KO; ++o) {
+        Qh[o] = __ldcg(qp + o);
+        Ql[o] = __ldcg(qp + KO + o);
+      }
+      CQ[0] = __uint_as_float(__ldcg(qp + 2 * KO));
+      CQ[1] = __uint_as_float(__ldcg(qp + 2 * KO + 1));
+      // distinct registers for the repeated values, so the quad needs no copies
+      asm volatile("mov.b32 %0, %1;" : "=f"(CQ[2]) : "f"(CQ[0]));
+      asm volatile("mov.b32 %0, %1;" : "=f"(CQ[3]) : "f"(CQ[1]));
+      two_e = __uint_as_float(__ldcg(qp + 2 * KO + 2));
+      inv2e = __uint_as_float(__ldcg(qp + 2 * KO + 3));
     }
-    float CQ[4];
-    CQ[0] = CQ[2] = cq_s[2 * c] * two_e;
-    CQ[1] = CQ[3] = cq_s[2 * c + 1] * two_e;
 
     // ---- main loop
     float m_run[2] = {-INFINITY, -INFINITY}, thr[2] = {-INFINITY, -INFINITY};
@@ -523,7 +458,6 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
     float acc[VT][4];
 #pragma unroll
     for (int t = 0; t < VT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-    constexpr uint32_t kOnes = 0x3C003C00u;  // fp16x2 (1, 1)
     int done = 0;
     bool timed_out = false;
     for (int i = 0; i < n_st; ++i) {
@@ -532,12 +466,12 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
         timed_out = true;
         break;
       }
-      const uint8_t* kr = wring + (size_t)slot * p.stage_bytes;
+      const uint8_t* kr = wring + slot * p.stage_bytes;
       const uint8_t* vr = kr + 2 * rec_k;
-      const bool two = wb0 + 2LL * i + 1 < wb1;
+      const bool two = 2 * i + 1 < n_my;
 
       float sc[2][2][4], zc[4];
-      key_stage(kr, kr + rec_k, geo_k, Qh, Ql, CQ, lane, c, sc, zc);
+      key_stage(kr, kr + rec_k, geo_k, Qh, Ql, CQ, Z4, lane, c, mg, sc, zc);
       if (!two) {
 #pragma unroll
         for (int m = 0; m < 2; ++m) sc[1][m][0] = sc[1][m][1] = sc[1][m][2] = sc[1][m][3] = -INFINITY;
@@ -585,11 +519,11 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
           pb[bb][m][1] = movm_t(pack_f16x2(p2, p3));
         }
         // row sums on the tensor cores: all-ones A
-        mma16816(l_acc, kOnes, kOnes, kOnes, kOnes, pb[bb][0][0], pb[bb][0][1]);
-        mma16816(l_acc, kOnes, kOnes, kOnes, kOnes, pb[bb][1][0], pb[bb][1][1]);
+        mma16816(l_acc, O4[0], O4[1], O4[2], O4[3], pb[bb][0][0], pb[bb][0][1]);
+        mma16816(l_acc, O4[0], O4[1], O4[2], O4[3], pb[bb][1][0], pb[bb][1][1]);
       }
-      value_block<VQ>(vr, geo_v, lane, g, pb[0], acc);
-      value_block<VQ>(vr + rec_v, geo_v, lane, g, pb[1], acc);
+      value_block<VQ>(vr, geo_v, lane, g, mg, pb[0], acc);
+      value_block<VQ>(vr + rec_v, geo_v, lane, g, mg, pb[1], acc);
 
       __syncwarp();
       if (lane == 0 && i + ns < n_st) issue(i + ns, slot);
@@ -630,180 +564,34 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
         if (pch < p.rvp) mw[(2 * c + (e2 & 1)) * ms + 2 + pch] = acc[t][e2];
       }
     }
-    fence_proxy_async_smem();  // bulk copies will land on these bytes later
     __syncthreads();
     const bool bad = flag_s[0] != 0;
-    // merge-phase layout of the ring (only the stream's last contributor
-    // reads it): V basis, tails, the stream's partials, tail weights, merged
-    // latents, denominators
-    const int rk = p.k.r, rv = p.v.r;
-    const int n_tail = (int)(len % kBlock);
-    const int gv = kh / p.v.heads_per_group;
-    const int tv_bytes = p.v.quantize ? kBlock * rv * 4 : rec_v;
-    float* BV_s = reinterpret_cast<float*>(ring);                 // [rv][128]
-    float* TK_s = BV_s + (size_t)rv * kHeadDim;                    // [32][rk]
-    float* TV_s = TK_s + (size_t)kBlock * rk;                      // [32][rv] (or one fp16 record)
-    float* P_s = TV_s + (tv_bytes + 15) / 16 * 4;                  // [nseg][Gq][ms] partials
-    float* ST_s = P_s + (size_t)p.seg_max * Gq * ms;               // [8][32] tail scores, then weights
-    float* O_s = ST_s + 8 * kBlock;                                // [8][128] merged latents
-    float* L_s = O_s + 8 * kHeadDim;                               // [8]
-    if (T > 0) {
-      float* part = p.ws + ((size_t)X * p.seg_max + kslot) * (size_t)Gq * ms;
-      const float* mrg = reinterpret_cast<const float*>(ring);
-      for (int i = tid; i < Gq * ms; i += kDecThreads) {
-        const int h = i / ms, e2 = i - h * ms;
-        float out;
-        if (bad) {
-          out = e2 == 0 ? -INFINITY : 0.f;
-        } else {
-          float M = -INFINITY;
-#pragma unroll
-          for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, mrg[(w * 8 + h) * ms]);
-          if (e2 == 0) {
-            out = M;
-          } else {
-            out = 0.f;
-#pragma unroll
-            for (int w = 0; w < kDecWarps; ++w) {
-              const float mw_ = mrg[(w * 8 + h) * ms];
-              if (mw_ != -INFINITY) out = fmaf(mrg[(w * 8 + h) * ms + e2], ex2(mw_ - M), out);
-            }
-          }
-        }
-        part[i] = out;
-      }
-    }
-    __syncthreads();  // the warp partials are consumed; the ring is free
-    if (tid == 0) {
-      // the V basis and the tails, fetched before the ticket so that the
-      // last contributor finds them in place (the others just let them land)
-      const uint32_t bytes = (uint32_t)rv * 512u + (n_tail > 0 ? (uint32_t)(kBlock * rk * 4 + tv_bytes) : 0u);
-      mbar_arrive_expect_tx(mbar, bytes);
-      bulk_g2s(BV_s, p.v.basisT + (size_t)gv * rv * kHeadDim, (uint32_t)rv * 512u, mbar);
-      if (n_tail > 0) {
-        bulk_g2s(TK_s, p.k.tail + (size_t)X * kBlock * rk, (uint32_t)(kBlock * rk * 4), mbar);
-        const void* tv = p.v.quantize ? static_cast<const void*>(p.v.tail + (size_t)X * kBlock * rv)
-                                      : static_cast<const void*>(p.v.blocks + ((size_t)X * p.v.n_blk_cap + nf) * rec_v);
-        bulk_g2s(TV_s, tv, (uint32_t)tv_bytes, mbar);
-      }
-      int last = 1;
-      if (T > 0) {
-        // release: the CTA's partial (ordered by the barrier above) before the
-        // ticket; acquire: the other contributors' partials after it
-        __threadfence();
-        const unsigned int t = atomicAdd(&p.k.tickets[X], 1u);
-        last = t + 1 == (unsigned int)nseg;
-        if (last) {
-          p.k.tickets[X] = 0u;
-          __threadfence();
-        }
-      }
-      flag_s[1] = last;
-    }
-    __syncthreads();
-    const bool merger = flag_s[1] != 0;
-    const int nsg = T > 0 ? (int)nseg : 0;
-    if (merger) {
-      const float* wsx = p.ws + (size_t)X * p.seg_max * Gq * ms;
-      for (int i = tid; i < nsg * Gq * ms; i += kDecThreads) P_s[i] = __ldcg(wsx + i);
-    }
-    const bool got = mbar_wait_bounded(mbar, merge_par);
-    merge_par ^= 1u;
-    if (!got && tid == 0) set_dev_error(p.k.hdr, PALU_DEVERR_TIMEOUT);
-    __syncthreads();
-
-    // ---- the stream's last contributor: merge partials + tail, project, + mu
-    if (merger) {
-      // tail scores (log2 units)
-      for (int i = tid; i < n_tail * 8; i += kDecThreads) {
-        const int t = i >> 3, h = i & 7;
-        float sc_t = -INFINITY;
-        if (h < Gq) {
-          sc_t = cq_s[h];
-          for (int j2 = 0; j2 < rk; ++j2) {
-            const int pch = j2 < p.k.n_hi ? j2 : 8 * p.k.n_hi_oct + (j2 - p.k.n_hi);
-            sc_t = fmaf(qt_s[h * kHeadDim + pch], TK_s[t * rk + j2], sc_t);
-          }
-        }
-        ST_s[h * kBlock + t] = sc_t;
-      }
-      __syncthreads();
-      // warp h: max, weights (over the partials' m), denominator
-      if (warp < Gq) {
-        const int h = warp;
+    float* part = p.ws + ((size_t)X * p.seg_max + kslot) * (size_t)Gq * ms;
+    const float* mrg = reinterpret_cast<const float*>(ring);
+    for (int i = tid; i < Gq * ms; i += kDecThreads) {
+      const int h = i / ms, e2 = i - h * ms;
+      float out;
+      if (bad) {
+        out = e2 == 0 ? -INFINITY : 0.f;
+      } else {
         float M = -INFINITY;
-        for (int sg = lane; sg < nsg; sg += 32) M = fmaxf(M, P_s[(sg * Gq + h) * ms]);
-        const float st = lane < n_tail ? ST_s[h * kBlock + lane] : -INFINITY;
-        M = fmaxf(M, st);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float L = 0.f;
-        for (int sg = lane; sg < nsg; sg += 32) {
-          const float m = P_s[(sg * Gq + h) * ms];
-          const float w = m == -INFINITY ? 0.f : ex2(m - M);
-          L = fmaf(w, P_s[(sg * Gq + h) * ms + 1], L);
-          P_s[(sg * Gq + h) * ms] = w;
-        }
-        const float pt = lane < n_tail ? ex2(st - M) : 0.f;
-        L += pt;
-        __syncwarp();
-        ST_s[h * kBlock + lane] = pt;
+        for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, mrg[(w * 8 + h) * ms]);
+        if (e2 == 0) {
+          out = M;
+        } else {
+          out = 0.f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        if (lane == 0) L_s[h] = L;
-      }
-      __syncthreads();
-      // merged latent per (head, real value channel)
-      for (int i = tid; i < Gq * p.rvp; i += kDecThreads) {
-        const int h = i / p.rvp, pch = i - h * p.rvp;
-        const int j2 = padded_to_channel(pch, rv, p.v.n_hi, p.v.n_hi_oct, p.v.quantize);
-        if (j2 < 0) continue;
-        float a = 0.f;
-        for (int sg = 0; sg < nsg; ++sg) a = fmaf(P_s[(sg * Gq + h) * ms], P_s[(sg * Gq + h) * ms + 2 + pch], a);
-        for (int t = 0; t < n_tail; ++t) {
-          float lv;
-          if (p.v.quantize) {
-            lv = TV_s[t * rv + j2];
-          } else {
-            const int kk = 2 * (t >> 4) + ((t & 15) >> 3);
-            const int ln = 4 * (j2 & 7) + ((t & 7) >> 1);
-            lv = __half2float(*reinterpret_cast<const __half*>(reinterpret_cast<const uint8_t*>(TV_s) +
-                                                               512 * (j2 >> 3) + 16 * ln + 4 * kk + 2 * (t & 1)));
-          }
-          a = fmaf(ST_s[h * kBlock + t], lv, a);
-        }
-        O_s[h * kHeadDim + j2] = a;
-      }
-      __syncthreads();
-      // out[h][d] = (sum_j o_hj V[d, j]) / L_h + mu[d]
-      {
-        const int d = tid & 127, h0 = (tid >> 7) * 4;
-        float o4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-        for (int j2 = 0; j2 < rv; ++j2) {
-          const float bv = BV_s[j2 * kHeadDim + d];
-#pragma unroll
-          for (int hh = 0; hh < 4; ++hh) o4[hh] = fmaf(O_s[(h0 + hh) * kHeadDim + j2], bv, o4[hh]);
-        }
-        const float mu = __ldg(p.v.mu + (size_t)gv * kHeadDim + d);
-#pragma unroll
-        for (int hh = 0; hh < 4; ++hh) {
-          const int h = h0 + hh;
-          if (h < Gq) {
-            const float v = fmaf(o4[hh], 1.f / L_s[h], mu);
-            const long long oi = ((long long)b * p.Hq + (long long)kh * Gq + h) * kHeadDim + d;
-            if (p.out_fp32)
-              static_cast<float*>(p.out)[oi] = v;
-            else
-              static_cast<__half*>(p.out)[oi] = __float2half_rn(v);
+          for (int w = 0; w < kDecWarps; ++w) {
+            const float mw_ = mrg[(w * 8 + h) * ms];
+            if (mw_ != -INFINITY) out = fmaf(mrg[(w * 8 + h) * ms + e2], ex2(mw_ - M), out);
           }
         }
       }
+      part[i] = out;
     }
-    fence_proxy_async_smem();
+    fence_proxy_async_smem();  // the next segment's copies land on these bytes
     __syncthreads();
-    ++X;
-    if (T == 0) X += G - 1;
   }
 }
 

@@ -31,7 +31,6 @@ constexpr uint32_t kSpinLimit = 1u << 22;
 //   basisT         fp32 [n_groups][rank][D]   (row j = direction j)
 //   mu             fp32 [n_groups][D]
 //   mv             fp32 [n_groups][rank][2]   mu_g . V_g[:, j] as a float pair (hi, lo)
-//   tickets        u32  [batch * kv_heads]    decode merge counters (zero between calls)
 struct StateHeader {
   long long length;
   unsigned int err;
@@ -42,18 +41,17 @@ struct StateHeader {
 static_assert(sizeof(StateHeader) == 64, "state header size");
 
 struct StateLayout {
-  size_t basis_off, mu_off, mv_off, tk_off, total;
+  size_t basis_off, mu_off, mv_off, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline StateLayout state_layout(int n_groups, int rank, int64_t n_streams) {
+inline StateLayout state_layout(int n_groups, int rank) {
   StateLayout s;
   s.basis_off = 256;
   s.mu_off = align_up(s.basis_off + sizeof(float) * (size_t)n_groups * rank * kHeadDim, 256);
   s.mv_off = align_up(s.mu_off + sizeof(float) * (size_t)n_groups * kHeadDim, 256);
-  s.tk_off = align_up(s.mv_off + sizeof(float) * 2 * (size_t)n_groups * rank, 256);
-  s.total = align_up(s.tk_off + sizeof(uint32_t) * (size_t)n_streams, 256);
+  s.total = align_up(s.mv_off + sizeof(float) * 2 * (size_t)n_groups * rank, 256);
   return s;
 }
 
@@ -65,7 +63,6 @@ struct CacheView {
   const float* basisT;   // [n_g][r][D]
   const float* mu;       // [n_g][D]
   const float2* mv;      // [n_g][r]
-  unsigned int* tickets; // [batch * kv_heads]
   int64_t n_blk_cap;
   int64_t capacity;
   int r, n_hi, n_hi_oct, n_lo_oct, n_oct, rec_bytes;
@@ -74,7 +71,7 @@ struct CacheView {
 
 inline CacheView make_view(const palu_cache* c) {
   CacheView v;
-  StateLayout s = state_layout(c->n_groups, c->rank, (int64_t)c->batch * c->kv_heads);
+  StateLayout s = state_layout(c->n_groups, c->rank);
   uint8_t* st = static_cast<uint8_t*>(c->state);
   v.blocks = static_cast<uint8_t*>(c->blocks);
   v.tail = c->tail;
@@ -82,7 +79,6 @@ inline CacheView make_view(const palu_cache* c) {
   v.basisT = reinterpret_cast<const float*>(st + s.basis_off);
   v.mu = reinterpret_cast<const float*>(st + s.mu_off);
   v.mv = reinterpret_cast<const float2*>(st + s.mv_off);
-  v.tickets = reinterpret_cast<unsigned int*>(st + s.tk_off);
   v.n_blk_cap = c->n_blk_cap;
   v.capacity = c->capacity;
   v.r = c->rank;
