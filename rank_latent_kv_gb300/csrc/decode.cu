@@ -137,11 +137,11 @@ __global__ void __launch_bounds__(256) latent_qprep_kernel(const DecodeParams p)
 // merged latents, denominators.
 __global__ void __launch_bounds__(256) latent_combine_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ uint64_t mbar;
+  __shared__ uint64_t mbar, mbar_p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long X = blockIdx.x;
   const int b = (int)(X / p.Hkv), kh = (int)(X % p.Hkv), Gq = p.Gq;
-  const int rk = p.k.r, rv = p.v.r, ms = 2 + p.rvp;
+  const int rk = p.k.r, rv = p.v.r, ms = kPartHead + p.rvp;
   const int gv = kh / p.v.heads_per_group;
   const int rec_v = p.v.rec_bytes;
   const int tv_bytes = p.v.quantize ? kBlock * rv * 4 : rec_v;
@@ -161,11 +161,14 @@ __global__ void __launch_bounds__(256) latent_combine_kernel(const DecodeParams 
   const long long T = p.streams * nf;
   int nseg = 0;
   if (T > 0) {
-    const long long G = min((long long)p.dec_grid, T);
-    nseg = (int)(block_owner(X * nf + nf - 1, T, G) - block_owner(X * nf, T, G) + 1);
+    // the decode launch's warps that take part; one partial per CTA
+    const long long W = min((long long)p.dec_grid * kDecWarps, T);
+    nseg = (int)(block_owner(X * nf + nf - 1, T, W) / kDecWarps - block_owner(X * nf, T, W) / kDecWarps + 1);
   }
+  const float mu_v = __ldg(p.v.mu + (size_t)gv * kHeadDim + (tid & 127));
   if (tid == 0) {
     mbar_init(&mbar, 1);
+    mbar_init(&mbar_p, 1);
     fence_mbar_init();
     const uint32_t bytes = (uint32_t)rv * 512u + (n_tail > 0 ? (uint32_t)(kBlock * rk * 4 + tv_bytes) : 0u);
     mbar_arrive_expect_tx(&mbar, bytes);
@@ -178,10 +181,15 @@ __global__ void __launch_bounds__(256) latent_combine_kernel(const DecodeParams 
     }
   }
   grid_dep_wait();  // the decode kernel's partials (and, through it, q~ and c)
-  const float* wsx = p.ws + (size_t)X * p.seg_max * Gq * ms;
-  for (int i = tid; i < nseg * Gq * ms; i += 256) P_s[i] = __ldcg(wsx + i);
-  __syncthreads();  // barrier initialised, partials staged
-  const bool got = mbar_wait_bounded(&mbar, 0);
+  if (tid == 0) {
+    // the stream's partials are contiguous: one bulk copy
+    const uint32_t pbytes = (uint32_t)nseg * Gq * ms * 4u;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    mbar_arrive_expect_tx(&mbar_p, pbytes);
+    if (pbytes > 0) bulk_g2s(P_s, p.ws + (size_t)X * p.seg_max * Gq * ms, pbytes, &mbar_p);
+  }
+  __syncthreads();  // barriers initialised
+  const bool got = mbar_wait_bounded(&mbar, 0) && mbar_wait_bounded(&mbar_p, 0);
   if (!got && tid == 0) set_dev_error(p.k.hdr, PALU_DEVERR_TIMEOUT);
   // tail scores (log2 units)
   const float* qt = p.qt + (size_t)X * 8 * kHeadDim;
@@ -228,8 +236,20 @@ __global__ void __launch_bounds__(256) latent_combine_kernel(const DecodeParams 
     const int h = i / p.rvp, pch = i - h * p.rvp;
     const int j2 = padded_to_channel(pch, rv, p.v.n_hi, p.v.n_hi_oct, p.v.quantize);
     if (j2 < 0) continue;
-    float a = 0.f;
-    for (int sg = 0; sg < nseg; ++sg) a = fmaf(P_s[(sg * Gq + h) * ms], P_s[(sg * Gq + h) * ms + 2 + pch], a);
+    float a4[4] = {0.f, 0.f, 0.f, 0.f};
+    int sg = 0;
+    for (; sg + 4 <= nseg; sg += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float* pr = P_s + ((size_t)(sg + u) * Gq + h) * ms;
+        a4[u] = fmaf(pr[0], pr[kPartHead + pch], a4[u]);
+      }
+    }
+    for (; sg < nseg; ++sg) {
+      const float* pr = P_s + ((size_t)sg * Gq + h) * ms;
+      a4[0] = fmaf(pr[0], pr[kPartHead + pch], a4[0]);
+    }
+    float a = (a4[0] + a4[1]) + (a4[2] + a4[3]);
     for (int t = 0; t < n_tail; ++t) {
       float lv;
       if (p.v.quantize) {
@@ -249,13 +269,22 @@ __global__ void __launch_bounds__(256) latent_combine_kernel(const DecodeParams 
   {
     const int d = tid & 127, h0 = (tid >> 7) * 4;
     float o4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int j2 = 0; j2 < rv; ++j2) {
+    int j2 = 0;
+    for (; j2 + 4 <= rv; j2 += 4) {
+      const float b0 = BV_s[j2 * kHeadDim + d], b1 = BV_s[(j2 + 1) * kHeadDim + d];
+      const float b2 = BV_s[(j2 + 2) * kHeadDim + d], b3 = BV_s[(j2 + 3) * kHeadDim + d];
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) {
+        const float4 o = *reinterpret_cast<const float4*>(O_s + (h0 + hh) * kHeadDim + j2);
+        o4[hh] = fmaf(o.x, b0, fmaf(o.y, b1, fmaf(o.z, b2, fmaf(o.w, b3, o4[hh]))));
+      }
+    }
+    for (; j2 < rv; ++j2) {
       const float bv = BV_s[j2 * kHeadDim + d];
 #pragma unroll
       for (int hh = 0; hh < 4; ++hh) o4[hh] = fmaf(O_s[(h0 + hh) * kHeadDim + j2], bv, o4[hh]);
     }
-    const float mu = __ldg(p.v.mu + (size_t)gv * kHeadDim + d);
+    const float mu = mu_v;
 #pragma unroll
     for (int hh = 0; hh < 4; ++hh) {
       const int h = h0 + hh;
@@ -274,7 +303,7 @@ __global__ void __launch_bounds__(256) latent_combine_kernel(const DecodeParams 
 struct DecodePlan {
   int KC, VC;
   bool VQ;
-  int ns, stage_bytes, ring_off, smem, grid, seg_max, rvp, qp_ko, qp_stride;
+  int ns, stage_bytes, ring_off, wp_off, smem, grid, seg_max, rvp, qp_ko, qp_stride;
   size_t comb_smem;
   size_t qpack_off, qt_off, cq_off, part_off, ws_bytes;
   DecodeKernel kern;
@@ -331,37 +360,43 @@ static palu_status plan_decode(const palu_cache* k, const palu_cache* v, int32_t
   pl->ring_off = (int)align_up(kDecBarOff + 8 * kDecWarps * pl->ns, 128);
   const int64_t streams = (int64_t)k->batch * k->kv_heads;
   const int sms = device_sm_count();
-  const size_t rings = std::max((size_t)kDecWarps * pl->ns * pl->stage_bytes,
-                                (size_t)kDecWarps * 8 * (2 + pl->rvp) * 4);
-  pl->smem = (int)(pl->ring_off + rings);
+  const size_t rings = (size_t)kDecWarps * pl->ns * pl->stage_bytes;
+  pl->wp_off = (int)align_up(pl->ring_off + rings, 16);
+  pl->smem = (int)(pl->wp_off + (size_t)kDecWarps * 2 * Gq * (kPartHead + pl->rvp) * 4);
   if (pl->smem > 227 * 1024) return fail(PALU_ERR_UNSUPPORTED, "decode shared-memory plan exceeds 227 KB");
   int per_sm = 0;
   palu_status st = kernel_occupancy(reinterpret_cast<const void*>(pl->kern), kDecThreads, pl->smem, &per_sm);
   if (st != PALU_OK) return st;
   int64_t grid = (int64_t)sms * std::min(per_sm, 4);
   grid = std::min<int64_t>(grid, std::max<int64_t>(1, streams * k->n_blk_cap));
+  // at least one warp per stream, so that no warp's range spans more than two
+  // streams (extra CTAs, if any, simply run in a second wave)
+  grid = std::max<int64_t>(grid, (streams + kDecWarps - 1) / kDecWarps);
   pl->grid = (int)std::max<int64_t>(1, grid);
-  // the combine stages one stream's partials on chip: with few streams, use
-  // fewer CTAs so that they fit
+  // the combine stages one stream's partials on chip (one per CTA that
+  // touches the stream: at most ceil(CTAs / streams) + 1); with few streams,
+  // use fewer CTAs so that they fit
   const int tv_bytes = v->quantize ? kBlock * v->rank * 4 : rec_v;
   const size_t comb_fixed = (size_t)v->rank * 512 + (size_t)128 * k->rank + align_up(tv_bytes, 16) +
                             8 * kBlock * 4 + 8 * kHeadDim * 4 + 32;
-  const size_t per_seg = (size_t)Gq * (2 + pl->rvp) * 4;
+  const size_t per_seg = (size_t)Gq * (kPartHead + pl->rvp) * 4;
   const size_t comb_budget = 200 * 1024;
   pl->seg_max = (int)((pl->grid + streams - 1) / streams + 1);
   if (comb_fixed + pl->seg_max * per_seg > comb_budget) {
     const int64_t seg_fit = (int64_t)((comb_budget - comb_fixed) / per_seg);
     if (seg_fit < 2) return fail(PALU_ERR_UNSUPPORTED, "decode merge does not fit in shared memory");
     pl->grid = (int)std::max<int64_t>(1, std::min<int64_t>(pl->grid, streams * (seg_fit - 1)));
+    pl->grid = (int)std::max<int64_t>(pl->grid, (streams + kDecWarps - 1) / kDecWarps);
     pl->seg_max = (int)((pl->grid + streams - 1) / streams + 1);
   }
   pl->comb_smem = comb_fixed + pl->seg_max * per_seg;
+  if (pl->comb_smem > 227 * 1024) return fail(PALU_ERR_UNSUPPORTED, "decode merge does not fit in shared memory");
   // workspace: packed query factors, q~ and c per stream, partials
   pl->qpack_off = 0;
   pl->qt_off = align_up(pl->qpack_off + sizeof(uint32_t) * (size_t)streams * 32 * pl->qp_stride, 256);
   pl->cq_off = align_up(pl->qt_off + sizeof(float) * (size_t)streams * 8 * kHeadDim, 256);
   pl->part_off = align_up(pl->cq_off + sizeof(float) * (size_t)streams * 8, 256);
-  pl->ws_bytes = align_up(pl->part_off + sizeof(float) * (size_t)streams * pl->seg_max * Gq * (2 + pl->rvp), 256);
+  pl->ws_bytes = align_up(pl->part_off + sizeof(float) * (size_t)streams * pl->seg_max * Gq * (kPartHead + pl->rvp), 256);
   return PALU_OK;
 }
 
@@ -410,6 +445,7 @@ extern "C" palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v
   p.ns = pl.ns;
   p.stage_bytes = pl.stage_bytes;
   p.ring_off = pl.ring_off;
+  p.wp_off = pl.wp_off;
   p.seg_max = pl.seg_max;
   p.qp_ko = pl.qp_ko;
   p.qp_stride = pl.qp_stride;

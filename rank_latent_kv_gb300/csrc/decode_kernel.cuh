@@ -51,6 +51,10 @@ constexpr int kDecThreads = 32 * kDecWarps;
 constexpr float kLazyTau = 8.f;   // log2 headroom before the running max is raised
 constexpr int kDecFlagOff = 0;    // decode CTA shared memory: flags int [4]
 constexpr int kDecBarOff = 64;    // then mbarriers [warps][ns]; the rings follow
+// A partial (per segment and query head): m, l, two pad words, then the
+// latent accumulator per padded value channel; 16-byte multiple, so one
+// stream's partials move as a single bulk copy.
+constexpr int kPartHead = 4;
 
 struct DecodeParams {
   CacheView k, v;
@@ -59,13 +63,14 @@ struct DecodeParams {
   uint32_t* qpack;    // per stream and lane: Qh[ko], Ql[ko], CQ0, CQ1, 2^e, 2^-e  (qp_stride words)
   float* qt;          // per stream: scaled q~ [8][128] per padded key channel
   float* cq;          // per stream: scaled q . mu^K [8]
-  float* ws;          // partials [streams][seg_max][Gq][2 + rvp]
+  float* ws;          // partials [streams][seg_max][Gq][kPartHead + rvp]
   int out_fp32;
   int Hq, Hkv, Gq;
   int rvp;            // padded value channels = 8 * v.n_oct
   int ns;             // stages per warp ring
   int stage_bytes;    // 2 * (k.rec_bytes + v.rec_bytes)
   int ring_off;       // shared-memory offset of the rings
+  int wp_off;         // shared-memory offset of the warps' partials [warps][2][Gq][kPartHead + rvp]
   int seg_max;        // partial slots per stream
   int qp_ko;          // key octets held per lane in qpack
   int qp_stride;      // words per lane in qpack
@@ -342,8 +347,8 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
   using GV = Geom<VC, VE, VQ>;
   constexpr int KO = GK::kMaxOct, VT = (GV::kMaxOct + 1) / 2;
   extern __shared__ __align__(128) uint8_t smem[];
-  int* flag_s = reinterpret_cast<int*>(smem + kDecFlagOff);  // [0] timed out
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecBarOff);
+  int* flag_s = reinterpret_cast<int*>(smem + kDecFlagOff);  // [0..15] stream of each warp's segments
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecBarOff);  // [warps][ns]
   uint8_t* ring = smem + p.ring_off;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
@@ -351,12 +356,14 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
   const long long len = __ldcg(&p.k.hdr->length);
   const long long nf = len / kBlock;
   const long long T = p.streams * nf;
-  // split over at most T CTAs, so every CTA that takes part owns >= 1 block
-  // and the CTAs covering a stream are consecutive
-  const long long G = min((long long)gridDim.x, T), cta = blockIdx.x;
-  if (tid == 0 && cta == 0 && __ldcg(&p.v.hdr->length) != len) set_dev_error(p.k.hdr, PALU_DEVERR_LENGTH_MISMATCH);
-  if (cta >= G) return;
-  const long long R0 = cta * T / G, R1 = (cta + 1) * T / G;
+  if (tid == 0 && blockIdx.x == 0 && __ldcg(&p.v.hdr->length) != len)
+    set_dev_error(p.k.hdr, PALU_DEVERR_LENGTH_MISMATCH);
+  // every warp works on its own: the flat range of full blocks is split over
+  // at most T warps, so each warp that takes part owns >= 1 block and the
+  // warps covering a stream are consecutive
+  const long long W = min((long long)gridDim.x * kDecWarps, T);
+  const long long gw = (long long)blockIdx.x * kDecWarps + warp;
+  const long long R0 = gw < W ? gw * T / W : 0, R1 = gw < W ? (gw + 1) * T / W : 0;
   const int ns = p.ns, Gq = p.Gq;
   GK geo_k;
   GV geo_v;
@@ -368,9 +375,11 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
   if (tid == 0) {
     for (int i = 0; i < kDecWarps * ns; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
-    flag_s[0] = 0;
   }
   __syncthreads();
+  const int ms = kPartHead + p.rvp;
+  float* wp = reinterpret_cast<float*>(smem + p.wp_off) + (size_t)warp * 2 * Gq * ms;
+  if (lane < 2) flag_s[2 * warp + lane] = -1;
 
   uint8_t* wring = ring + (size_t)warp * ns * p.stage_bytes;
   uint64_t* wbar = bars + warp * ns;
@@ -391,34 +400,54 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
   asm volatile("mov.b32 %0, 0x3C003C00;" : "=r"(O4[2]));
   asm volatile("mov.b32 %0, 0x3C003C00;" : "=r"(O4[3]));
 
-  for (long long X = R0 / nf; X * nf < R1; ++X) {
-    const long long b0 = max(R0, X * nf) - X * nf, b1 = min(R1, (X + 1) * nf) - X * nf;
-    const long long kslot = cta - block_owner(X * nf, T, G);
-    const bool dead = flag_s[0] != 0;
-
-    // ---- this warp's contiguous share of the segment, two blocks per stage
-    const int nseg_blk = (int)(b1 - b0);
-    const long long wb0 = b0 + warp * nseg_blk / kDecWarps, wb1 = b0 + (warp + 1) * nseg_blk / kDecWarps;
-    const int n_my = (int)(wb1 - wb0), n_st = dead ? 0 : (n_my + 1) >> 1;
+  bool timed_out = false;
+  int seg = 0;
+  for (long long X = R0 < R1 ? R0 / nf : 0; R0 < R1 && X * nf < R1; ++X, ++seg) {
+    if (seg >= 2) {  // the launch plan gives every warp at most two streams
+      set_dev_error(p.k.hdr, PALU_DEVERR_CAPACITY);
+      break;
+    }
+    // ---- this warp's segment of stream X, two blocks per stage
+    const long long wb0 = max(R0, X * nf) - X * nf, wb1 = min(R1, (X + 1) * nf) - X * nf;
+    const int n_my = (int)(wb1 - wb0), n_st = timed_out ? 0 : (n_my + 1) >> 1;
+    // Stage i holds blocks 2i, 2i+1 of the warp's range.  Every stage reads
+    // two real records, so that no byte the compute touches is stale: an odd
+    // last stage takes the pair that ends at its block (its first slot, a
+    // block counted already, is masked), or, for a one-block range, the pair
+    // that starts there (second slot masked); a stream of one full block
+    // cannot pair up, and its stage copies the block twice.
+    const long long blk_last = (long long)nf - 1;  // last full block of the stream
+    int odd_shift = 0, odd_mask = 1;               // odd last stage: source shift, slot to mask
+    if (n_my & 1) {
+      if (n_my >= 2 || wb0 >= 1) {
+        odd_shift = -1;
+        odd_mask = 0;
+      } else if (blk_last >= 1) {
+        odd_shift = 0;
+        odd_mask = 1;
+      } else {
+        odd_shift = 1;  // marker: duplicate
+        odd_mask = 1;
+      }
+    }
     const uint8_t* kbase = p.k.blocks + ((size_t)X * p.k.n_blk_cap + wb0) * rec_k;
     const uint8_t* vbase = p.v.blocks + ((size_t)X * p.v.n_blk_cap + wb0) * rec_v;
-    // stage i holds blocks 2i, 2i+1 of the warp's range; an odd last stage
-    // holds its block twice (the copy in the second slot is masked), so every
-    // byte the stage is read at is a real record
     auto issue = [&](int i, int s) {
       uint8_t* dst = wring + s * p.stage_bytes;
       uint64_t* bar = &wbar[s];
-      const uint8_t* ks = kbase + (size_t)(2 * i) * rec_k;
-      const uint8_t* vs = vbase + (size_t)(2 * i) * rec_v;
+      const bool odd_last = 2 * i + 1 >= n_my;
+      const long long sb = 2LL * i + ((odd_last && odd_shift < 0) ? -1 : 0);
+      const uint8_t* ks = kbase + sb * rec_k;
+      const uint8_t* vs = vbase + sb * rec_v;
       mbar_arrive_expect_tx(bar, (uint32_t)(2 * (rec_k + rec_v)));
-      if (2 * i + 1 < n_my) {
-        bulk_g2s(dst, ks, (uint32_t)(2 * rec_k), bar);
-        bulk_g2s(dst + 2 * rec_k, vs, (uint32_t)(2 * rec_v), bar);
-      } else {
+      if (odd_last && odd_shift > 0) {
         bulk_g2s(dst, ks, (uint32_t)rec_k, bar);
         bulk_g2s(dst + rec_k, ks, (uint32_t)rec_k, bar);
         bulk_g2s(dst + 2 * rec_k, vs, (uint32_t)rec_v, bar);
         bulk_g2s(dst + 2 * rec_k + rec_v, vs, (uint32_t)rec_v, bar);
+      } else {
+        bulk_g2s(dst, ks, (uint32_t)(2 * rec_k), bar);
+        bulk_g2s(dst + 2 * rec_k, vs, (uint32_t)(2 * rec_v), bar);
       }
     };
     if (lane == 0) {
@@ -459,7 +488,6 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
 #pragma unroll
     for (int t = 0; t < VT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
     int done = 0;
-    bool timed_out = false;
     for (int i = 0; i < n_st; ++i) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&wbar[slot], par));
       if (!ok) {
@@ -468,13 +496,17 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
       }
       const uint8_t* kr = wring + slot * p.stage_bytes;
       const uint8_t* vr = kr + 2 * rec_k;
-      const bool two = 2 * i + 1 < n_my;
+      const int masked = 2 * i + 1 < n_my ? -1 : odd_mask;  // slot whose scores are dropped
 
       float sc[2][2][4], zc[4];
       key_stage(kr, kr + rec_k, geo_k, Qh, Ql, CQ, Z4, lane, c, mg, sc, zc);
-      if (!two) {
+      if (masked >= 0) {
 #pragma unroll
-        for (int m = 0; m < 2; ++m) sc[1][m][0] = sc[1][m][1] = sc[1][m][2] = sc[1][m][3] = -INFINITY;
+        for (int bb = 0; bb < 2; ++bb)
+          if (bb == masked) {
+#pragma unroll
+            for (int m = 0; m < 2; ++m) sc[bb][m][0] = sc[bb][m][1] = sc[bb][m][2] = sc[bb][m][3] = -INFINITY;
+          }
       }
 
       // lazy online softmax over the stage's 64 tokens (raw units: 2^e * log2);
@@ -531,7 +563,7 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
       par ^= slot == 0 ? 1u : 0u;
       done = i + 1;
     }
-    if (timed_out) {
+    if (timed_out && n_st > 0) {
       // drain this warp's copies still in flight (bounded), then report
       if (lane == 0) {
         set_dev_error(p.k.hdr, PALU_DEVERR_TIMEOUT);
@@ -542,56 +574,69 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
           s = s + 1 == ns ? 0 : s + 1;
           pr ^= s == 0 ? 1u : 0u;
         }
-        atomicOr(&flag_s[0], 1);
       }
+      __syncwarp();
     }
 
-    // ---- merge the 8 warps of the CTA into the segment's partial
-    __syncthreads();  // every warp is done with the ring
-    const int ms = 2 + p.rvp;
-    float* mw = reinterpret_cast<float*>(ring) + warp * 8 * ms;
+    // ---- the warp's partial for this segment (running max and sum per
+    // head, latent accumulator per padded value channel), kept on chip
+    float* part = wp + (size_t)seg * Gq * ms;
+    if (lane == 0) flag_s[2 * warp + seg] = (int)X;
     if (g == 0) {
-      mw[(2 * c) * ms + 0] = n_my > 0 ? m_run[0] : -INFINITY;
-      mw[(2 * c) * ms + 1] = l_acc[0];
-      mw[(2 * c + 1) * ms + 0] = n_my > 0 ? m_run[1] : -INFINITY;
-      mw[(2 * c + 1) * ms + 1] = l_acc[1];
+      if (2 * c < Gq) {
+        part[(2 * c) * ms + 0] = timed_out ? -INFINITY : m_run[0];
+        part[(2 * c) * ms + 1] = timed_out ? 0.f : l_acc[0];
+      }
+      if (2 * c + 1 < Gq) {
+        part[(2 * c + 1) * ms + 0] = timed_out ? -INFINITY : m_run[1];
+        part[(2 * c + 1) * ms + 1] = timed_out ? 0.f : l_acc[1];
+      }
     }
 #pragma unroll
     for (int t = 0; t < VT; ++t) {
 #pragma unroll
       for (int e2 = 0; e2 < 4; ++e2) {
-        const int pch = 16 * t + g + 8 * (e2 >> 1);
-        if (pch < p.rvp) mw[(2 * c + (e2 & 1)) * ms + 2 + pch] = acc[t][e2];
+        const int pch = 16 * t + g + 8 * (e2 >> 1), h = 2 * c + (e2 & 1);
+        if (pch < p.rvp && h < Gq) part[h * ms + kPartHead + pch] = timed_out ? 0.f : acc[t][e2];
       }
     }
-    __syncthreads();
-    const bool bad = flag_s[0] != 0;
-    float* part = p.ws + ((size_t)X * p.seg_max + kslot) * (size_t)Gq * ms;
-    const float* mrg = reinterpret_cast<const float*>(ring);
+  }
+
+  // ---- merge the CTA's warps per stream (log-sum-exp) into one partial per
+  // (stream, CTA); the CTAs covering a stream are consecutive
+  __syncthreads();
+  int xlo = 0x7fffffff, xhi = -1;
+#pragma unroll
+  for (int i = 0; i < 2 * kDecWarps; ++i) {
+    const int x = flag_s[i];
+    if (x >= 0) {
+      xlo = min(xlo, x);
+      xhi = max(xhi, x);
+    }
+  }
+  const float* wpa = reinterpret_cast<const float*>(smem + p.wp_off);
+  for (int x = xlo; x <= xhi; ++x) {
+    const long long cslot = (long long)blockIdx.x - block_owner((long long)x * nf, T, W) / kDecWarps;
+    float* out = p.ws + ((size_t)x * p.seg_max + cslot) * (size_t)Gq * ms;
     for (int i = tid; i < Gq * ms; i += kDecThreads) {
       const int h = i / ms, e2 = i - h * ms;
-      float out;
-      if (bad) {
-        out = e2 == 0 ? -INFINITY : 0.f;
-      } else {
-        float M = -INFINITY;
+      float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, mrg[(w * 8 + h) * ms]);
-        if (e2 == 0) {
-          out = M;
-        } else {
-          out = 0.f;
+      for (int k = 0; k < 2 * kDecWarps; ++k)
+        if (flag_s[k] == x) M = fmaxf(M, wpa[((size_t)k * Gq + h) * ms]);
+      float v = 0.f;
+      if (e2 == 0) {
+        v = M;
+      } else if (e2 == 1 || e2 >= kPartHead) {
 #pragma unroll
-          for (int w = 0; w < kDecWarps; ++w) {
-            const float mw_ = mrg[(w * 8 + h) * ms];
-            if (mw_ != -INFINITY) out = fmaf(mrg[(w * 8 + h) * ms + e2], ex2(mw_ - M), out);
-          }
+        for (int k = 0; k < 2 * kDecWarps; ++k) {
+          if (flag_s[k] != x) continue;
+          const float mk = wpa[((size_t)k * Gq + h) * ms];
+          if (mk != -INFINITY) v = fmaf(wpa[((size_t)k * Gq + h) * ms + e2], ex2(mk - M), v);
         }
       }
-      part[i] = out;
+      out[i] = v;
     }
-    fence_proxy_async_smem();  // the next segment's copies land on these bytes
-    __syncthreads();
   }
 }
 
