@@ -51,9 +51,18 @@ palu_status kernel_occupancy(const void* kernel, int threads, int smem, int* per
     *per_sm = it->second;
     return PALU_OK;
   }
-  // the limit is a property of the kernel: only ever raise it, never lower it
+  // the limit is a property of the kernel: only ever raise it, never lower it.
+  // Beyond 48 KB of static plus dynamic shared memory a block needs it.
+  static std::map<std::pair<const void*, int>, int> static_smem;
+  auto sit = static_smem.find(std::make_pair(kernel, dev));
+  if (sit == static_smem.end()) {
+    cudaFuncAttributes fa;
+    st = cuda_check(cudaFuncGetAttributes(&fa, kernel), "cudaFuncGetAttributes");
+    if (st != PALU_OK) return st;
+    sit = static_smem.emplace(std::make_pair(kernel, dev), (int)fa.sharedSizeBytes).first;
+  }
   int& cur = attr_max[std::make_pair(kernel, dev)];
-  if (smem > 48 * 1024 && smem > cur) {
+  if (smem + sit->second > 48 * 1024 && smem > cur) {
     st = cuda_check(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                     "cudaFuncSetAttribute(max dynamic shared memory)");
     if (st != PALU_OK) return st;

@@ -324,13 +324,20 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
 }
 
 // Decode-time append of a single token per stream: one CTA per (KV head,
-// batch).  Each warp computes whole latent channels cooperatively: lane l
+// batch).  The group's basis rows come into shared memory with one bulk copy
+// (dynamic shared memory, rank * 512 bytes).  Each warp computes whole latent
+// channels cooperatively: lane l
 // holds x[4l..4l+3] and the matching entries of the basis row, forms exact
 // products and float-pair partial sums, and a butterfly of error-free sums
 // combines the 32 partials; then mu_g . V_g[:, j] is subtracted and the
 // result rounded once to fp32.  If the token completes a 32-token block the
 // block is quantized and packed exactly as in encode_append_kernel.
-__global__ void __launch_bounds__(128) encode_one_kernel(CacheView cv, const __half* __restrict__ x, int Hkv) {
+constexpr int kEncOneThreads = 256;
+__global__ void __launch_bounds__(kEncOneThreads) encode_one_kernel(CacheView cv, const __half* __restrict__ x,
+                                                                    int Hkv) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  float* bas = reinterpret_cast<float*>(dsm);  // [r][128]
+  __shared__ uint64_t bar;
   __shared__ float lat[kBlock][kMaxRank + 1];
   __shared__ uint8_t codes[kBlock * kMaxRank];
   __shared__ __half2 sz[kMaxRank];
@@ -338,15 +345,24 @@ __global__ void __launch_bounds__(128) encode_one_kernel(CacheView cv, const __h
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x, b = blockIdx.y;
   const int r = cv.r;
+  const int grp = h / cv.heads_per_group;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar, (uint32_t)r * 512u);
+    bulk_g2s(bas, cv.basisT + (size_t)grp * r * kHeadDim, (uint32_t)r * 512u, &bar);
+  }
   const long long p0 = __ldcg(&cv.hdr->length);
   const unsigned int n_cta = gridDim.x * gridDim.y;
+  __syncthreads();  // barrier initialised
+  const bool got = mbar_wait_bounded(&bar, 0);  // also drains the copy before any early exit
+  if (!got && tid == 0) set_dev_error(cv.hdr, PALU_DEVERR_TIMEOUT);
   if (p0 + 1 > cv.capacity) {
     if (h == 0 && b == 0 && tid == 0) set_dev_error(cv.hdr, PALU_DEVERR_CAPACITY);
     return;  // nothing written, length unchanged (no CTA takes a ticket)
   }
   const int pos = (int)(p0 % kBlock);
   const long long blk = p0 / kBlock;
-  const int grp = h / cv.heads_per_group;
   const long long sidx = (long long)b * Hkv + h;
 
   float xv[4];
@@ -359,8 +375,8 @@ __global__ void __launch_bounds__(128) encode_one_kernel(CacheView cv, const __h
     xv[2] = c.x;
     xv[3] = c.y;
   }
-  for (int j = warp; j < r; j += 4) {  // warp-uniform trip count
-    const float4 v = reinterpret_cast<const float4*>(cv.basisT + ((size_t)grp * r + j) * kHeadDim)[lane];
+  for (int j = warp; j < r; j += kEncOneThreads / 32) {  // warp-uniform trip count
+    const float4 v = reinterpret_cast<const float4*>(bas + (size_t)j * kHeadDim)[lane];
     const float vv[4] = {v.x, v.y, v.z, v.w};
     float S = 0.f, E = 0.f;
 #pragma unroll
@@ -607,7 +623,11 @@ extern "C" palu_status palu_encode_append(palu_cache* cache, const void* x, int6
   const int64_t nblk = (tokens + kBlock - 1) / kBlock + 1;  // blocks touched from any start offset
   if (nblk > 2147483647LL) return fail(PALU_ERR_UNSUPPORTED, "too many tokens in one append");
   if (tokens == 1) {
-    encode_one_kernel<<<dim3(cache->kv_heads, cache->batch), 128, 0, static_cast<cudaStream_t>(stream)>>>(
+    const int smem1 = cache->rank * 512;
+    int per_sm1 = 0;
+    st = kernel_occupancy(reinterpret_cast<const void*>(encode_one_kernel), kEncOneThreads, smem1, &per_sm1);
+    if (st != PALU_OK) return st;
+    encode_one_kernel<<<dim3(cache->kv_heads, cache->batch), kEncOneThreads, smem1, static_cast<cudaStream_t>(stream)>>>(
         make_view(cache), static_cast<const __half*>(x), cache->kv_heads);
     st = cuda_check(cudaGetLastError(), "encode_one_kernel launch");
     if (st != PALU_OK) return st;
