@@ -171,19 +171,27 @@ def peaks():
     return 6800.0, "fallback"
 
 
+DECODE_SOURCES = ("decode_kernel.cuh", "decode.cu")
+
+
+def decode_source_sha():
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        h.update(open(os.path.join(ROOT, "rank_latent_kv_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
 def traffic_record():
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel source (null otherwise)."""
+    """DRAM bytes per decode-kernel launch from the committed ncu summary, if
+    it was taken on the current decode sources (null otherwise)."""
     path = os.path.join(ROOT, "profiles", "latent_decode_qwen7b.md")
-    src = os.path.join(ROOT, "rank_latent_kv_gb300", "csrc", "decode.cu")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(decode\.cu sha256 ([0-9a-f]{12,64})\)", txt)
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(decode sources sha256 ([0-9a-f]{12,64})\)", txt)
     if not m:
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    return float(m.group(1)) if sha.startswith(m.group(2)) else None
+    return float(m.group(1)) if decode_source_sha().startswith(m.group(2)) else None
 
 
 # ------------------------------------------------------------------ CPU oracle leg
@@ -435,8 +443,10 @@ def run_palu(args, w, world, rank, local):
                    "l2": "inputs larger than L2: %.2f GB of caches read per step" % (
                        L * bytes_launch / 1e9),
                    "episode_resets_in_timed_region": n_resets},
-        "gpu_launches": K * L * 4 + n_resets * L * 2,
-        "roofline": {"bound": "hbm", "kernel": "palu_decode_attn (split-K decode + combine)",
+        # per layer and step: two one-token appends, q-prep, decode, combine;
+        # per episode reset: two truncates per layer
+        "gpu_launches": K * L * 5 + n_resets * L * 2,
+        "roofline": {"bound": "hbm", "kernel": "palu_decode_attn (q-prep + split decode + combine)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "traffic": traffic_record(),
                      "algorithmic_bytes_per_launch": bytes_launch, "avg_launch_us": avg_launch * 1e3,

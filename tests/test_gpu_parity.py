@@ -192,6 +192,29 @@ def test_decode_ranks(P, rk, rv):
     run_decode_case(P, B=1, Hkv=4, Gq=3, S=257, rk=rk, rv=rv, seed=rk + rv)
 
 
+def _rank_for_octets(n):
+    """Smallest rank whose mixed-bit record has n octets (oracle layout)."""
+    for r in range(1, 129):
+        if O.Layout(O.ROLE_KEY, r, O.n_hi_channels(r)).n_oct == n:
+            return r
+    raise ValueError(n)
+
+
+# every key octet count 1..8 (kernels specialised on the exact count) against
+# a spread of value octet counts
+@pytest.mark.parametrize("ko,vo", [(k, v) for k in range(1, 9) for v in (1 + (3 * k) % 8, 9 - k)])
+def test_decode_exact_octet_kernels(P, ko, vo):
+    rk, rv = _rank_for_octets(ko), _rank_for_octets(vo)
+    run_decode_case(P, B=1, Hkv=2, Gq=4, S=200, rk=rk, rv=rv, n_groups=1, seed=10 * ko + vo, steps=1)
+
+
+# contexts long enough that warps stream several two-block stages and the
+# warps' ranges cross from one (batch, KV head) stream into the next
+@pytest.mark.parametrize("B,Hkv,S", [(1, 8, 20011), (2, 4, 50017)])
+def test_decode_multi_block_warps(P, B, Hkv, S):
+    run_decode_case(P, B=B, Hkv=Hkv, Gq=3, S=S, rk=30, rv=53, n_groups=2, seed=S, steps=1)
+
+
 @pytest.mark.parametrize("S", [1, 5, 31, 32, 33, 64, 95, 1000, 4099])
 def test_decode_lengths(P, S):
     run_decode_case(P, B=1, Hkv=2, Gq=3, S=S, rk=16, rv=24, n_groups=1, seed=S, steps=1)
