@@ -196,6 +196,22 @@ palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v, const voi
                              int32_t q_heads, float softmax_scale, void* out, int32_t out_fp32,
                              void* workspace, size_t workspace_bytes, void* stream);
 
+/* One decode step of one layer: append one token of k and one of v to every
+ * (batch, KV head) stream (decode steps 1-2), then attend with q over every
+ * cached token including the new one (decode step 3); the same results as
+ * palu_encode_append(k, k_new, 1), palu_encode_append(v, v_new, 1) and
+ * palu_decode_attn(k, v, q, ...) in that order.  The "fused per-step
+ * pipeline" of this library: three kernel launches instead of five (the two
+ * appends and the query factors share one launch).
+ *   k_new, v_new  device fp16 [batch, kv_heads, D] (one token per stream).
+ *   q, out, softmax_scale, out_fp32, workspace  as for palu_decode_attn
+ *        (workspace of palu_decode_workspace_size bytes).
+ * Errors: as palu_encode_append (capacity: PALU_ERR_CAPACITY, nothing
+ * launched) and palu_decode_attn.  Updates k->length and v->length. */
+palu_status palu_decode_step(palu_cache* k, palu_cache* v, const void* k_new, const void* v_new,
+                             const void* q, int32_t q_heads, float softmax_scale, void* out, int32_t out_fp32,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
 /* Roll the cache back to `length` tokens (e.g. to reuse a prompt prefix or
  * drop rejected speculative tokens).  Allowed when length is a multiple of 32
  * (a block boundary) or lies inside the current partial block, i.e. whenever

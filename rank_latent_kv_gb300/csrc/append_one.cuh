@@ -1,0 +1,231 @@
+// Single-token append (decode steps 1-2 of page "PALU — True Low-Rank Latent
+// Storage for Keys and Values", "How it works"): project the new token into
+// the stored group basis, L = (x - mu_g) V_g, keep it in the fp32 tail, and
+// when it completes a 32-token block quantize and pack the block (asymmetric
+// min/max per channel, blog post "VeloxQuant-MLX 0.8.0 adds KIVI", "What KIVI
+// is"; LSB-first fields, blog post "How I built VeloxQuant-MLX", "The
+// Bit-Packing Problem").  Shared by the one-token append kernel and the fused
+// decode-step prologue.
+#pragma once
+
+#include "palu_internal.cuh"
+
+namespace palu {
+
+// Position of code (t, j) inside a quantized record: byte offset and shift.
+// Mirrors the layout definition: channel j -> (octet, slot); (token, slot)
+// -> (lane, field k, half); 4-bit octets are u32 words per lane, 2-bit octets
+// u16 halfwords per lane (paired), LSB-first fields.
+__device__ __forceinline__ void code_pos(int role, int n_hi, int n_hi_oct, int n_lo_oct, int t, int j, int& byte,
+                                         int& shift) {
+  int octet, slot;
+  if (j < n_hi) {
+    octet = j >> 3;
+    slot = j & 7;
+  } else {
+    const int jj = j - n_hi;
+    octet = n_hi_oct + (jj >> 3);
+    slot = jj & 7;
+  }
+  const int k = 2 * (t >> 4) + ((t & 15) >> 3);
+  int g, c, half;
+  if (role == PALU_ROLE_KEY) {
+    g = t & 7;
+    c = slot >> 1;
+    half = slot & 1;
+  } else {
+    g = slot;
+    c = (t & 7) >> 1;
+    half = t & 1;
+  }
+  const int lane = 4 * g + c;
+  int unit, bit;
+  if (octet < n_hi_oct) {
+    unit = 128 * octet + 4 * lane;
+    bit = 4 * k + 16 * half;
+  } else {
+    const int lo = octet - n_hi_oct;
+    const int npair = n_lo_oct >> 1;
+    unit = 128 * n_hi_oct + (lo < 2 * npair ? 128 * (lo >> 1) + 4 * lane + 2 * (lo & 1) : 128 * npair + 2 * lane);
+    bit = 2 * k + 8 * half;
+  }
+  byte = unit + (bit >> 3);
+  shift = bit & 7;
+}
+
+__device__ __forceinline__ int latent_off(int t, int j) {
+  const int octet = j >> 3, slot = j & 7;
+  const int k = 2 * (t >> 4) + ((t & 15) >> 3);
+  const int lane = 4 * slot + ((t & 7) >> 1);
+  return 512 * octet + 16 * lane + 4 * k + 2 * (t & 1);
+}
+
+// Shared-memory scratch of one single-token append, carved from a caller's
+// buffer: the group's basis rows [r][128] (first, 128-byte aligned, filled by
+// the caller), block latents [32][r+1], codes [32][r], (scale, zero) [r],
+// and one record.
+struct AppendSmem {
+  float* bas;
+  float* lat;
+  uint8_t* codes;
+  __half2* sz;
+  uint8_t* rec;
+};
+__host__ __device__ inline size_t append_smem_bytes(int r, int rec_bytes) {
+  auto a16 = [](size_t x) { return (x + 15) / 16 * 16; };
+  return a16((size_t)r * kHeadDim * 4) + a16((size_t)kBlock * (r + 1) * 4) + a16((size_t)kBlock * r) +
+         a16((size_t)r * 4) + a16((size_t)rec_bytes);
+}
+__device__ __forceinline__ AppendSmem append_smem(uint8_t* base, int r, int rec_bytes) {
+  auto a16 = [](size_t x) { return (x + 15) / 16 * 16; };
+  AppendSmem s;
+  size_t o = 0;
+  s.bas = reinterpret_cast<float*>(base + o);
+  o += a16((size_t)r * kHeadDim * 4);
+  s.lat = reinterpret_cast<float*>(base + o);
+  o += a16((size_t)kBlock * (r + 1) * 4);
+  s.codes = base + o;
+  o += a16((size_t)kBlock * r);
+  s.sz = reinterpret_cast<__half2*>(base + o);
+  o += a16((size_t)r * 4);
+  s.rec = base + o;
+  (void)rec_bytes;
+  return s;
+}
+
+// Appends one token (x: this stream's D fp16 values) at position p0 of stream
+// (b, h).  Every thread of the CTA calls it; sm.bas must hold the group's
+// basis rows.  Each warp computes whole latent channels: lane l holds
+// x[4l..4l+3] and the matching entries of the basis row, forms exact products
+// and float-pair partial sums, and a butterfly of error-free sums combines
+// the 32 partials; then mu_g . V_g[:, j] (a float pair) is subtracted and the
+// result rounded once to fp32.  Returns, in every thread, the largest fp16
+// scale of the block this token completed (0 if none).
+__device__ __forceinline__ float append_one_token(const CacheView& cv, const __half* __restrict__ x, long long p0, int h, int b,
+                                  int Hkv, const AppendSmem& sm) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+  const int r = cv.r, ld = r + 1;
+  const int pos = (int)(p0 % kBlock);
+  const long long blk = p0 / kBlock;
+  const int grp = h / cv.heads_per_group;
+  const long long sidx = (long long)b * Hkv + h;
+  float* lat = sm.lat;
+  __shared__ float smax;
+  if (tid == 0) smax = 0.f;
+
+  float xv[4];
+  {
+    const uint2 w = *reinterpret_cast<const uint2*>(x + 4 * lane);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+    const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+    xv[0] = a.x;
+    xv[1] = a.y;
+    xv[2] = c.x;
+    xv[3] = c.y;
+  }
+  for (int j = warp; j < r; j += nwarps) {  // warp-uniform trip count
+    const float4 v = reinterpret_cast<const float4*>(sm.bas + (size_t)j * kHeadDim)[lane];
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+    float S = 0.f, E = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float pp, pe, s2, se;
+      two_prod(xv[i], vv[i], pp, pe);
+      two_sum(S, pp, s2, se);
+      S = s2;
+      E = __fadd_rn(E, __fadd_rn(se, pe));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
+      const float E2 = __shfl_xor_sync(0xffffffffu, E, o);
+      float s3, err;
+      two_sum(S, S2, s3, err);
+      S = s3;
+      E = __fadd_rn(__fadd_rn(E, E2), err);
+    }
+    if (lane == 0) {
+      const float2 m = cv.mv[(size_t)grp * r + j];
+      float a, ae;
+      two_sum(S, -m.x, a, ae);
+      lat[pos * ld + j] = __fadd_rn(a, __fadd_rn(__fsub_rn(E, m.y), ae));
+    }
+  }
+  __syncthreads();
+
+  if (!cv.quantize) {
+    uint8_t* gdst = cv.blocks + (sidx * cv.n_blk_cap + blk) * cv.rec_bytes;
+    for (int j = tid; j < r; j += blockDim.x)
+      *reinterpret_cast<__half*>(gdst + latent_off(pos, j)) = __float2half_rn(lat[pos * ld + j]);
+    return 0.f;
+  }
+  float* tail = cv.tail + sidx * kBlock * r;
+  if (pos < kBlock - 1) {
+    for (int j = tid; j < r; j += blockDim.x) tail[pos * r + j] = lat[pos * ld + j];
+    return 0.f;
+  }
+  // the token completes the block: quantize and pack it like a prefill block
+  uint8_t* rec = sm.rec;
+  for (int i = tid; i < (kBlock - 1) * r; i += blockDim.x) lat[(i / r) * ld + (i % r)] = tail[i];
+  for (int i = tid; i < cv.rec_bytes / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(rec)[i] = 0u;
+  __syncthreads();
+  for (int j = tid; j < r; j += blockDim.x) {
+    float mn = lat[j], mx = lat[j];
+    for (int t = 1; t < kBlock; ++t) {
+      mn = fminf(mn, lat[t * ld + j]);
+      mx = fmaxf(mx, lat[t * ld + j]);
+    }
+    const float qmax = j < cv.n_hi ? 15.f : 3.f;
+    const __half sh = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), qmax));
+    const __half zh = __float2half_rn(mn);
+    const float s32 = __half2float(sh), z32 = __half2float(zh);
+    sm.sz[j] = __halves2half2(sh, zh);
+    atomicMax(&cv.hdr->max_scale, __float_as_uint(s32));
+    atomicMax(reinterpret_cast<unsigned int*>(&smax), __float_as_uint(s32));
+    for (int t = 0; t < kBlock; ++t) {
+      float q = 0.f;
+      if (s32 != 0.f) q = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(lat[t * ld + j], z32), s32)), 0.f), qmax);
+      sm.codes[t * r + j] = (uint8_t)q;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < kBlock * r; i += blockDim.x) {
+    const int t = i / r, j = i % r;
+    int byte, shift;
+    code_pos(cv.role, cv.n_hi, cv.n_hi_oct, cv.n_lo_oct, t, j, byte, shift);
+    atomicOr(reinterpret_cast<unsigned int*>(rec + (byte & ~3)), (unsigned int)sm.codes[i] << (8 * (byte & 3) + shift));
+  }
+  const int n_pad = 8 * cv.n_oct;
+  const int szb = 128 * cv.n_hi_oct + 64 * cv.n_lo_oct;
+  __half* r16 = reinterpret_cast<__half*>(rec + szb);
+  for (int pch = tid; pch < n_pad; pch += blockDim.x) {
+    const int j = padded_to_channel(pch, r, cv.n_hi, cv.n_hi_oct, 1);
+    const __half2 v = j >= 0 ? sm.sz[j] : __halves2half2(__float2half(0.f), __float2half(0.f));
+    if (cv.role == PALU_ROLE_KEY) {
+      r16[pch] = __low2half(v);
+      r16[n_pad + pch] = __high2half(v);
+    } else {
+      r16[2 * pch] = __low2half(v);
+      r16[2 * pch + 1] = __high2half(v);
+    }
+  }
+  __syncthreads();
+  uint8_t* gdst = cv.blocks + (sidx * cv.n_blk_cap + blk) * cv.rec_bytes;
+  for (int i = tid; i < cv.rec_bytes / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(gdst)[i] = reinterpret_cast<const uint4*>(rec)[i];
+  return smax;
+}
+
+// Called by one thread of each of the n_cta CTAs that appended at p0, after
+// its CTA's writes: the last to arrive advances the length.
+__device__ __forceinline__ void publish_length(const CacheView& cv, long long p0, unsigned int n_cta) {
+  __threadfence();
+  const unsigned int t = atomicAdd(&cv.hdr->ticket, 1u);
+  if (t == n_cta - 1) {
+    cv.hdr->length = p0 + 1;
+    cv.hdr->ticket = 0u;
+    __threadfence();
+  }
+}
+
+}  // namespace palu

@@ -12,7 +12,7 @@
 #include <algorithm>
 #include <cstring>
 
-#include "palu_internal.cuh"
+#include "append_one.cuh"
 
 namespace palu {
 
@@ -64,54 +64,6 @@ __host__ __device__ inline EncodeSmem encode_smem(int r, int rec_bytes) {
   s.rec_off = s.sz_off + align16(4 * r);                               // record
   s.total = s.rec_off + align16(rec_bytes);
   return s;
-}
-
-// Position of code (t, j) inside a quantized record: byte offset and shift.
-// Mirrors the layout definition: channel j -> (octet, slot); (token, slot)
-// -> (lane, field k, half); 4-bit octets are u32 words per lane, 2-bit octets
-// u16 halfwords per lane (paired), LSB-first fields.
-__device__ __forceinline__ void code_pos(int role, int n_hi, int n_hi_oct, int n_lo_oct, int t, int j, int& byte,
-                                         int& shift) {
-  int octet, slot;
-  if (j < n_hi) {
-    octet = j >> 3;
-    slot = j & 7;
-  } else {
-    const int jj = j - n_hi;
-    octet = n_hi_oct + (jj >> 3);
-    slot = jj & 7;
-  }
-  const int k = 2 * (t >> 4) + ((t & 15) >> 3);
-  int g, c, half;
-  if (role == PALU_ROLE_KEY) {
-    g = t & 7;
-    c = slot >> 1;
-    half = slot & 1;
-  } else {
-    g = slot;
-    c = (t & 7) >> 1;
-    half = t & 1;
-  }
-  const int lane = 4 * g + c;
-  int unit, bit;
-  if (octet < n_hi_oct) {
-    unit = 128 * octet + 4 * lane;
-    bit = 4 * k + 16 * half;
-  } else {
-    const int lo = octet - n_hi_oct;
-    const int npair = n_lo_oct >> 1;
-    unit = 128 * n_hi_oct + (lo < 2 * npair ? 128 * (lo >> 1) + 4 * lane + 2 * (lo & 1) : 128 * npair + 2 * lane);
-    bit = 2 * k + 8 * half;
-  }
-  byte = unit + (bit >> 3);
-  shift = bit & 7;
-}
-
-__device__ __forceinline__ int latent_off(int t, int j) {
-  const int octet = j >> 3, slot = j & 7;
-  const int k = 2 * (t >> 4) + ((t & 15) >> 3);
-  const int lane = 4 * slot + ((t & 7) >> 1);
-  return 512 * octet + 16 * lane + 4 * k + 2 * (t & 1);
 }
 
 // grid (blocks touched, kv_heads, batch), 128 threads.
@@ -324,36 +276,25 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
 }
 
 // Decode-time append of a single token per stream: one CTA per (KV head,
-// batch).  The group's basis rows come into shared memory with one bulk copy
-// (dynamic shared memory, rank * 512 bytes).  Each warp computes whole latent
-// channels cooperatively: lane l
-// holds x[4l..4l+3] and the matching entries of the basis row, forms exact
-// products and float-pair partial sums, and a butterfly of error-free sums
-// combines the 32 partials; then mu_g . V_g[:, j] is subtracted and the
-// result rounded once to fp32.  If the token completes a 32-token block the
-// block is quantized and packed exactly as in encode_append_kernel.
+// batch).  The group's basis rows come into shared memory with one bulk copy;
+// append_one_token (append_one.cuh) does the rest.  The last CTA to finish
+// publishes the new length.
 constexpr int kEncOneThreads = 256;
 __global__ void __launch_bounds__(kEncOneThreads) encode_one_kernel(CacheView cv, const __half* __restrict__ x,
                                                                     int Hkv) {
   extern __shared__ __align__(128) uint8_t dsm[];
-  float* bas = reinterpret_cast<float*>(dsm);  // [r][128]
   __shared__ uint64_t bar;
-  __shared__ float lat[kBlock][kMaxRank + 1];
-  __shared__ uint8_t codes[kBlock * kMaxRank];
-  __shared__ __half2 sz[kMaxRank];
-  __shared__ __align__(16) uint8_t rec[128 * 16 + 4 * 128];  // largest quantized record: 128 channels, all 4-bit
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int h = blockIdx.x, b = blockIdx.y;
   const int r = cv.r;
-  const int grp = h / cv.heads_per_group;
+  const AppendSmem sm = append_smem(dsm, r, cv.rec_bytes);
   if (tid == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
     mbar_arrive_expect_tx(&bar, (uint32_t)r * 512u);
-    bulk_g2s(bas, cv.basisT + (size_t)grp * r * kHeadDim, (uint32_t)r * 512u, &bar);
+    bulk_g2s(sm.bas, cv.basisT + (size_t)(h / cv.heads_per_group) * r * kHeadDim, (uint32_t)r * 512u, &bar);
   }
   const long long p0 = __ldcg(&cv.hdr->length);
-  const unsigned int n_cta = gridDim.x * gridDim.y;
   __syncthreads();  // barrier initialised
   const bool got = mbar_wait_bounded(&bar, 0);  // also drains the copy before any early exit
   if (!got && tid == 0) set_dev_error(cv.hdr, PALU_DEVERR_TIMEOUT);
@@ -361,118 +302,9 @@ __global__ void __launch_bounds__(kEncOneThreads) encode_one_kernel(CacheView cv
     if (h == 0 && b == 0 && tid == 0) set_dev_error(cv.hdr, PALU_DEVERR_CAPACITY);
     return;  // nothing written, length unchanged (no CTA takes a ticket)
   }
-  const int pos = (int)(p0 % kBlock);
-  const long long blk = p0 / kBlock;
-  const long long sidx = (long long)b * Hkv + h;
-
-  float xv[4];
-  {
-    const uint2 w = *reinterpret_cast<const uint2*>(x + sidx * kHeadDim + 4 * lane);
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
-    const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
-    xv[0] = a.x;
-    xv[1] = a.y;
-    xv[2] = c.x;
-    xv[3] = c.y;
-  }
-  for (int j = warp; j < r; j += kEncOneThreads / 32) {  // warp-uniform trip count
-    const float4 v = reinterpret_cast<const float4*>(bas + (size_t)j * kHeadDim)[lane];
-    const float vv[4] = {v.x, v.y, v.z, v.w};
-    float S = 0.f, E = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float pp, pe, s2, se;
-      two_prod(xv[i], vv[i], pp, pe);
-      two_sum(S, pp, s2, se);
-      S = s2;
-      E = __fadd_rn(E, __fadd_rn(se, pe));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
-      const float E2 = __shfl_xor_sync(0xffffffffu, E, o);
-      float s3, err;
-      two_sum(S, S2, s3, err);
-      S = s3;
-      E = __fadd_rn(__fadd_rn(E, E2), err);
-    }
-    if (lane == 0) {
-      const float2 m = cv.mv[(size_t)grp * r + j];
-      float a, ae;
-      two_sum(S, -m.x, a, ae);
-      lat[pos][j] = __fadd_rn(a, __fadd_rn(__fsub_rn(E, m.y), ae));
-    }
-  }
+  append_one_token(cv, x + ((long long)b * Hkv + h) * kHeadDim, p0, h, b, Hkv, sm);
   __syncthreads();
-
-  if (!cv.quantize) {
-    uint8_t* gdst = cv.blocks + (sidx * cv.n_blk_cap + blk) * cv.rec_bytes;
-    for (int j = tid; j < r; j += blockDim.x)
-      *reinterpret_cast<__half*>(gdst + latent_off(pos, j)) = __float2half_rn(lat[pos][j]);
-  } else {
-    float* tail = cv.tail + sidx * kBlock * r;
-    if (pos < kBlock - 1) {
-      for (int j = tid; j < r; j += blockDim.x) tail[pos * r + j] = lat[pos][j];
-    } else {
-      for (int i = tid; i < (kBlock - 1) * r; i += blockDim.x) lat[i / r][i % r] = tail[i];
-      for (int i = tid; i < cv.rec_bytes / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(rec)[i] = 0u;
-      __syncthreads();
-      for (int j = tid; j < r; j += blockDim.x) {
-        float mn = lat[0][j], mx = lat[0][j];
-        for (int t = 1; t < kBlock; ++t) {
-          mn = fminf(mn, lat[t][j]);
-          mx = fmaxf(mx, lat[t][j]);
-        }
-        const float qmax = j < cv.n_hi ? 15.f : 3.f;
-        const __half sh = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), qmax));
-        const __half zh = __float2half_rn(mn);
-        const float s32 = __half2float(sh), z32 = __half2float(zh);
-        sz[j] = __halves2half2(sh, zh);
-        atomicMax(&cv.hdr->max_scale, __float_as_uint(s32));
-        for (int t = 0; t < kBlock; ++t) {
-          float q = 0.f;
-          if (s32 != 0.f) q = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(lat[t][j], z32), s32)), 0.f), qmax);
-          codes[t * r + j] = (uint8_t)q;
-        }
-      }
-      __syncthreads();
-      for (int i = tid; i < kBlock * r; i += blockDim.x) {
-        const int t = i / r, j = i % r;
-        int byte, shift;
-        code_pos(cv.role, cv.n_hi, cv.n_hi_oct, cv.n_lo_oct, t, j, byte, shift);
-        atomicOr(reinterpret_cast<unsigned int*>(rec + (byte & ~3)), (unsigned int)codes[i] << (8 * (byte & 3) + shift));
-      }
-      const int n_pad = 8 * cv.n_oct;
-      const int szb = 128 * cv.n_hi_oct + 64 * cv.n_lo_oct;
-      __half* r16 = reinterpret_cast<__half*>(rec + szb);
-      for (int pch = tid; pch < n_pad; pch += blockDim.x) {
-        const int j = padded_to_channel(pch, r, cv.n_hi, cv.n_hi_oct, 1);
-        const __half2 v = j >= 0 ? sz[j] : __halves2half2(__float2half(0.f), __float2half(0.f));
-        if (cv.role == PALU_ROLE_KEY) {
-          r16[pch] = __low2half(v);
-          r16[n_pad + pch] = __high2half(v);
-        } else {
-          r16[2 * pch] = __low2half(v);
-          r16[2 * pch + 1] = __high2half(v);
-        }
-      }
-      __syncthreads();
-      uint8_t* gdst = cv.blocks + (sidx * cv.n_blk_cap + blk) * cv.rec_bytes;
-      for (int i = tid; i < cv.rec_bytes / 16; i += blockDim.x)
-        reinterpret_cast<uint4*>(gdst)[i] = reinterpret_cast<const uint4*>(rec)[i];
-    }
-  }
-  // the last CTA to finish publishes the new length
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const unsigned int t = atomicAdd(&cv.hdr->ticket, 1u);
-    if (t == n_cta - 1) {
-      cv.hdr->length = p0 + 1;
-      cv.hdr->ticket = 0u;
-      __threadfence();
-    }
-  }
+  if (tid == 0) publish_length(cv, p0, gridDim.x * gridDim.y);
 }
 
 // Sets the device length (the host has checked that no quantized block is reopened).
@@ -623,7 +455,7 @@ extern "C" palu_status palu_encode_append(palu_cache* cache, const void* x, int6
   const int64_t nblk = (tokens + kBlock - 1) / kBlock + 1;  // blocks touched from any start offset
   if (nblk > 2147483647LL) return fail(PALU_ERR_UNSUPPORTED, "too many tokens in one append");
   if (tokens == 1) {
-    const int smem1 = cache->rank * 512;
+    const int smem1 = (int)append_smem_bytes(cache->rank, cache->record_bytes);
     int per_sm1 = 0;
     st = kernel_occupancy(reinterpret_cast<const void*>(encode_one_kernel), kEncOneThreads, smem1, &per_sm1);
     if (st != PALU_OK) return st;

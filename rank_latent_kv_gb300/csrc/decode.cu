@@ -7,6 +7,7 @@
 #include <map>
 #include <mutex>
 
+#include "append_one.cuh"
 #include "decode_kernel.cuh"
 
 namespace palu {
@@ -17,15 +18,37 @@ namespace palu {
 // per-lane fp16 hi/lo factors prescaled by 2^e with
 // |q~| 2^e max(1, largest stored scale) < 2^14, so that every fp16 operand and
 // product of the score MMAs stays finite.
-__global__ void __launch_bounds__(256) latent_qprep_kernel(const DecodeParams p) {
-  __shared__ __align__(16) float q_s[8][kHeadDim];
-  __shared__ __align__(16) float mu_s[kHeadDim];
-  __shared__ float B_s[32 * 129];
-  __shared__ __align__(16) float qt_s[8][kHeadDim];
-  __shared__ float red_s[8], cq_s[8];
-  grid_dep_launch();
+// Scratch of one stream's q-prep (16-byte aligned base).
+struct QprepSmem {
+  float (*q_s)[kHeadDim];
+  float* mu_s;
+  float* B_s;  // [32][129] basis rows, padded rows: conflict-free column reads
+  float (*qt_s)[kHeadDim];
+  float *red_s, *cq_s;
+};
+constexpr size_t kQprepSmemBytes = sizeof(float) * (8 * kHeadDim + kHeadDim + 32 * 129 + 8 * kHeadDim + 16);
+__device__ __forceinline__ QprepSmem qprep_smem(uint8_t* base) {
+  QprepSmem s;
+  float* f = reinterpret_cast<float*>(base);
+  s.q_s = reinterpret_cast<float(*)[kHeadDim]>(f);
+  s.mu_s = f + 8 * kHeadDim;
+  s.qt_s = reinterpret_cast<float(*)[kHeadDim]>(f + 9 * kHeadDim);
+  s.B_s = f + 17 * kHeadDim;
+  s.red_s = s.B_s + 32 * 129;
+  s.cq_s = s.red_s + 8;
+  return s;
+}
+
+// Stream X's q-prep by a 256-thread CTA.  max_s_floor: a scale the stream's
+// blocks may hold that the header need not show yet (one this CTA just stored).
+__device__ void qprep_stream(const DecodeParams& p, long long X, float max_s_floor, const QprepSmem& sm) {
+  float (*q_s)[kHeadDim] = sm.q_s;
+  float* mu_s = sm.mu_s;
+  float* B_s = sm.B_s;
+  float (*qt_s)[kHeadDim] = sm.qt_s;
+  float* red_s = sm.red_s;
+  float* cq_s = sm.cq_s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const long long X = blockIdx.x;
   const int b = (int)(X / p.Hkv), kh = (int)(X % p.Hkv), Gq = p.Gq;
   const int gk = kh / p.k.heads_per_group;
   const int npch = 8 * p.k.n_oct;
@@ -105,7 +128,7 @@ __global__ void __launch_bounds__(256) latent_qprep_kernel(const DecodeParams p)
     amax = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) amax = fmaxf(amax, red_s[w]);
-    const float max_s = __uint_as_float(__ldcg(&p.k.hdr->max_scale));
+    const float max_s = fmaxf(__uint_as_float(__ldcg(&p.k.hdr->max_scale)), max_s_floor);
     const float xm = amax * fmaxf(1.f, max_s);
     int e = 0;
     if (xm > 0.f) {
@@ -127,6 +150,53 @@ __global__ void __launch_bounds__(256) latent_qprep_kernel(const DecodeParams p)
     qp[2 * ko + 1] = __float_as_uint(cq_s[2 * c + 1] * two_e);
     qp[2 * ko + 2] = __float_as_uint(two_e);
     qp[2 * ko + 3] = __float_as_uint(inv2e);
+  }
+}
+
+__global__ void __launch_bounds__(256) latent_qprep_kernel(const DecodeParams p) {
+  __shared__ __align__(16) uint8_t scratch[kQprepSmemBytes];
+  grid_dep_launch();
+  qprep_stream(p, blockIdx.x, 0.f, qprep_smem(scratch));
+}
+
+// ------------------------------------------------------------------ step prologue
+// One decode step's work before attention (SURVEY "next" row: fused per-step
+// pipeline), in one launch: grid (streams, 2).  CTA (X, 0) appends stream
+// X's new key token and then prepares stream X's query factors (the prescale
+// sees a block this append completed without waiting on other CTAs: only
+// stream X's scales meet stream X's factors); CTA (X, 1) appends the new
+// value token.  Each cache's last appending CTA publishes its new length.
+__global__ void __launch_bounds__(256) latent_step_prologue_kernel(const DecodeParams p, const __half* k_new,
+                                                                   const __half* v_new) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ uint64_t bar;
+  const int tid = threadIdx.x;
+  const long long X = blockIdx.x;
+  const bool key = blockIdx.y == 0;
+  const CacheView& cv = key ? p.k : p.v;
+  const int h = (int)(X % p.Hkv), b = (int)(X / p.Hkv);
+  const AppendSmem sm = append_smem(dsm, cv.r, cv.rec_bytes);
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar, (uint32_t)cv.r * 512u);
+    bulk_g2s(sm.bas, cv.basisT + (size_t)(h / cv.heads_per_group) * cv.r * kHeadDim, (uint32_t)cv.r * 512u, &bar);
+  }
+  const long long p0 = __ldcg(&cv.hdr->length);
+  __syncthreads();
+  const bool got = mbar_wait_bounded(&bar, 0);
+  if (!got && tid == 0) set_dev_error(cv.hdr, PALU_DEVERR_TIMEOUT);
+  float s_new = 0.f;
+  if (p0 + 1 > cv.capacity) {
+    if (X == 0 && tid == 0) set_dev_error(cv.hdr, PALU_DEVERR_CAPACITY);
+  } else {
+    s_new = append_one_token(cv, (key ? k_new : v_new) + X * kHeadDim, p0, h, b, p.Hkv, sm);
+    __syncthreads();
+    if (tid == 0) publish_length(cv, p0, (unsigned int)p.streams);
+  }
+  if (key) {
+    __syncthreads();  // the append's scratch is free
+    qprep_stream(p, X, s_new, qprep_smem(dsm));
   }
 }
 
@@ -404,29 +474,11 @@ static palu_status plan_decode(const palu_cache* k, const palu_cache* v, int32_t
 
 using namespace palu;
 
-extern "C" palu_status palu_decode_workspace_size(const palu_cache* k, const palu_cache* v, int32_t q_heads,
-                                                  size_t* bytes) {
-  DecodePlan pl;
-  palu_status st = plan_decode(k, v, q_heads, &pl);
-  if (st != PALU_OK) return st;
-  if (!bytes) return fail(PALU_ERR_INVALID_ARG, "bytes is NULL");
-  *bytes = pl.ws_bytes;
-  return PALU_OK;
-}
-
-extern "C" palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v, const void* q, int32_t q_heads,
-                                        float softmax_scale, void* out, int32_t out_fp32, void* workspace,
-                                        size_t workspace_bytes, void* stream) {
-  DecodePlan pl;
-  palu_status st = plan_decode(k, v, q_heads, &pl);
-  if (st != PALU_OK) return st;
-  if (!q || !out || !workspace) return fail(PALU_ERR_INVALID_ARG, "q, out and workspace must be non-NULL");
-  if (((uintptr_t)q & 15) || ((uintptr_t)out & 15) || ((uintptr_t)workspace & 15))
-    return fail(PALU_ERR_INVALID_ARG, "q, out and workspace must be 16-byte aligned");
-  if (workspace_bytes < pl.ws_bytes)
-    return fail(PALU_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(pl.ws_bytes) + " bytes");
-  if (k->length != v->length) return fail(PALU_ERR_INVALID_ARG, "key and value caches differ in length");
-  if (k->length < 1) return fail(PALU_ERR_INVALID_ARG, "the caches are empty");
+namespace palu {
+// Fills the launch parameters shared by palu_decode_attn and palu_decode_step.
+static DecodeParams decode_params(const DecodePlan& pl, const palu_cache* k, const palu_cache* v, const void* q,
+                                  int32_t q_heads, float softmax_scale, void* out, int32_t out_fp32,
+                                  void* workspace) {
   DecodeParams p;
   p.k = make_view(k);
   p.v = make_view(v);
@@ -451,15 +503,19 @@ extern "C" palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v
   p.qp_stride = pl.qp_stride;
   p.dec_grid = pl.grid;
   p.streams = (long long)k->batch * k->kv_heads;
+  p.after_append = 0;
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)kHeadDim);
   p.scale_log2 = scale * 1.4426950408889634f;
-  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  return p;
+}
+
+// The decode kernel and the combine, each started while its predecessor
+// finishes (programmatic dependent launch; each waits in-kernel).
+static palu_status launch_decode_combine(const DecodePlan& pl, const DecodeParams& p, cudaStream_t strm) {
   const unsigned int n_streams = (unsigned int)p.streams;
-  latent_qprep_kernel<<<n_streams, 256, 0, strm>>>(p);
-  st = cuda_check(cudaGetLastError(), "latent_qprep_kernel launch");
-  if (st != PALU_OK) return st;
   int per_sm = 0;
-  st = kernel_occupancy(reinterpret_cast<const void*>(latent_combine_kernel), 256, (int)pl.comb_smem, &per_sm);
+  palu_status st =
+      kernel_occupancy(reinterpret_cast<const void*>(latent_combine_kernel), 256, (int)pl.comb_smem, &per_sm);
   if (st != PALU_OK) return st;
   // decode and combine each start while their predecessor finishes
   // (programmatic dependent launch; each waits in-kernel for the results)
@@ -479,6 +535,71 @@ extern "C" palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = pl.comb_smem;
   return cuda_check(cudaLaunchKernelEx(&cfg, latent_combine_kernel, p), "latent_combine_kernel launch");
+}
+}  // namespace palu
+
+extern "C" palu_status palu_decode_workspace_size(const palu_cache* k, const palu_cache* v, int32_t q_heads,
+                                                  size_t* bytes) {
+  DecodePlan pl;
+  palu_status st = plan_decode(k, v, q_heads, &pl);
+  if (st != PALU_OK) return st;
+  if (!bytes) return fail(PALU_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = pl.ws_bytes;
+  return PALU_OK;
+}
+
+extern "C" palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v, const void* q, int32_t q_heads,
+                                        float softmax_scale, void* out, int32_t out_fp32, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  DecodePlan pl;
+  palu_status st = plan_decode(k, v, q_heads, &pl);
+  if (st != PALU_OK) return st;
+  if (!q || !out || !workspace) return fail(PALU_ERR_INVALID_ARG, "q, out and workspace must be non-NULL");
+  if (((uintptr_t)q & 15) || ((uintptr_t)out & 15) || ((uintptr_t)workspace & 15))
+    return fail(PALU_ERR_INVALID_ARG, "q, out and workspace must be 16-byte aligned");
+  if (workspace_bytes < pl.ws_bytes)
+    return fail(PALU_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(pl.ws_bytes) + " bytes");
+  if (k->length != v->length) return fail(PALU_ERR_INVALID_ARG, "key and value caches differ in length");
+  if (k->length < 1) return fail(PALU_ERR_INVALID_ARG, "the caches are empty");
+  DecodeParams p = decode_params(pl, k, v, q, q_heads, softmax_scale, out, out_fp32, workspace);
+  p.after_append = 0;
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  latent_qprep_kernel<<<(unsigned int)p.streams, 256, 0, strm>>>(p);
+  st = cuda_check(cudaGetLastError(), "latent_qprep_kernel launch");
+  if (st != PALU_OK) return st;
+  return launch_decode_combine(pl, p, strm);
+}
+
+extern "C" palu_status palu_decode_step(palu_cache* k, palu_cache* v, const void* k_new, const void* v_new,
+                                        const void* q, int32_t q_heads, float softmax_scale, void* out,
+                                        int32_t out_fp32, void* workspace, size_t workspace_bytes, void* stream) {
+  DecodePlan pl;
+  palu_status st = plan_decode(k, v, q_heads, &pl);
+  if (st != PALU_OK) return st;
+  if (!k_new || !v_new || !q || !out || !workspace)
+    return fail(PALU_ERR_INVALID_ARG, "k_new, v_new, q, out and workspace must be non-NULL");
+  if ((((uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)q | (uintptr_t)out | (uintptr_t)workspace) & 15))
+    return fail(PALU_ERR_INVALID_ARG, "k_new, v_new, q, out and workspace must be 16-byte aligned");
+  if (workspace_bytes < pl.ws_bytes)
+    return fail(PALU_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(pl.ws_bytes) + " bytes");
+  if (k->length != v->length) return fail(PALU_ERR_INVALID_ARG, "key and value caches differ in length");
+  if (k->length + 1 > k->capacity)
+    return fail(PALU_ERR_CAPACITY, "the caches are full (capacity " + std::to_string(k->capacity) + " tokens)");
+  DecodeParams p = decode_params(pl, k, v, q, q_heads, softmax_scale, out, out_fp32, workspace);
+  p.after_append = 1;
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  const size_t smem = std::max({append_smem_bytes(k->rank, k->record_bytes),
+                                append_smem_bytes(v->rank, v->record_bytes), kQprepSmemBytes});
+  int per_sm = 0;
+  st = kernel_occupancy(reinterpret_cast<const void*>(latent_step_prologue_kernel), 256, (int)smem, &per_sm);
+  if (st != PALU_OK) return st;
+  latent_step_prologue_kernel<<<dim3((unsigned int)p.streams, 2), 256, smem, strm>>>(p, static_cast<const __half*>(k_new),
+                                                                                 static_cast<const __half*>(v_new));
+  st = cuda_check(cudaGetLastError(), "latent_step_prologue_kernel launch");
+  if (st != PALU_OK) return st;
+  k->length += 1;
+  v->length += 1;
+  return launch_decode_combine(pl, p, strm);
 }
 
 // ------------------------------------------------------------------ allocation-free decode

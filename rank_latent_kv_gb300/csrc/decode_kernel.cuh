@@ -75,6 +75,7 @@ struct DecodeParams {
   int qp_ko;          // key octets held per lane in qpack
   int qp_stride;      // words per lane in qpack
   int dec_grid;       // CTAs of the decode launch
+  int after_append;   // the preceding launch appended tokens: read nothing before it completes
   long long streams;  // batch * kv_heads
   float scale_log2;   // softmax scale * log2(e)
 };
@@ -352,6 +353,11 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
   uint8_t* ring = smem + p.ring_off;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+  if (p.after_append) {
+    // the preceding launch wrote the length and maybe a new block: wait for
+    // it, and only then let the combine (which prefetches both) be scheduled
+    grid_dep_wait();
+  }
   grid_dep_launch();
   const long long len = __ldcg(&p.k.hdr->length);
   const long long nf = len / kBlock;

@@ -68,6 +68,8 @@ _SIGNATURES = {
                                    c_void_p, c_size_t, c_void_p]),
     "palu_decode_attn_noalloc": (c_int32, [_P(palu_cache), _P(palu_cache), c_void_p, c_int32, c_float, c_void_p,
                                            c_int32, c_void_p]),
+    "palu_decode_step": (c_int32, [_P(palu_cache), _P(palu_cache), c_void_p, c_void_p, c_void_p, c_int32, c_float,
+                                   c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
     "palu_cache_stats": (c_int32, [_P(palu_cache), _P(palu_stats)]),
     "palu_cache_truncate": (c_int32, [_P(palu_cache), c_int64, c_void_p]),
     "palu_cache_sync": (c_int32, [_P(palu_cache), _P(c_uint32), c_void_p]),
@@ -180,6 +182,13 @@ def palu_decode_workspace_size(k: palu_cache, v: palu_cache, q_heads: int) -> in
 def palu_decode_attn(k, v, q, out, workspace, softmax_scale=0.0, stream=None):
     _check(lib().palu_decode_attn(ctypes.byref(k), ctypes.byref(v), _ptr(q), q.shape[1], softmax_scale, _ptr(out),
                                   1 if out.dtype == torch.float32 else 0, _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def palu_decode_step(k, v, k_new, v_new, q, out, workspace, softmax_scale=0.0, stream=None):
+    """Append one token of k and v per stream, then decode attention (k_new, v_new: [B, Hkv, D] or [B, Hkv, 1, D])."""
+    _check(lib().palu_decode_step(ctypes.byref(k), ctypes.byref(v), _ptr(k_new), _ptr(v_new), _ptr(q), q.shape[1],
+                                  softmax_scale, _ptr(out), 1 if out.dtype == torch.float32 else 0, _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
@@ -299,4 +308,15 @@ def decode(kc: LatentCache, vc: LatentCache, q, out_dtype=torch.float32, softmax
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     palu_decode_attn(kc.c, vc.c, q, out, workspace, softmax_scale, stream)
+    return out
+
+
+def decode_step(kc: LatentCache, vc: LatentCache, k_new, v_new, q, out_dtype=torch.float32, softmax_scale=0.0,
+                stream=None, workspace=None, out=None):
+    """One decode step: append k_new, v_new ([B, Hkv, 1, D] fp16), then decode attention; returns out."""
+    if workspace is None:
+        workspace = _dev_bytes(palu_decode_workspace_size(kc.c, vc.c, q.shape[1]), q.device)
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    palu_decode_step(kc.c, vc.c, k_new, v_new, q, out, workspace, softmax_scale, stream)
     return out

@@ -215,6 +215,39 @@ def test_decode_multi_block_warps(P, B, Hkv, S):
     run_decode_case(P, B=B, Hkv=Hkv, Gq=3, S=S, rk=30, rv=53, n_groups=2, seed=S, steps=1)
 
 
+# the fused decode step (append k, append v, attend) against the separate calls
+# on identical caches, and against the oracle; steps cross block boundaries
+@pytest.mark.parametrize("S,rk,rv,quantize_v", [(29, 16, 24, True), (250, 30, 53, True), (95, 32, 32, False),
+                                                (3000, 74, 74, True)])
+def test_decode_step_matches_separate_calls(P, S, rk, rv, quantize_v):
+    rng = np.random.default_rng(S + rk)
+    B, Hkv, Gq, steps = 2, 4, 3, 6
+    xk = rand_lowrank(rng, B, Hkv, S + steps, n_groups=2)
+    xv = rand_lowrank(rng, B, Hkv, S + steps, n_groups=2)
+    cfg_k = P.palu_config_default(n_head_groups=2, rank=rk)
+    cfg_v = P.palu_config_default(n_head_groups=2, rank=rv, quantize=1 if quantize_v else 0)
+    ka, va = make_caches(P, cfg_k, cfg_v, xk[:, :, :S], xv[:, :, :S], S + steps + 8)
+    kb, vb = make_caches(P, cfg_k, cfg_v, xk[:, :, :S], xv[:, :, :S], S + steps + 8)
+    for t in range(S, S + steps):
+        q = torch.from_numpy(rng.standard_normal((B, Hkv * Gq, 128)).astype(np.float16)).to(DEV)
+        k1 = torch.from_numpy(xk[:, :, t:t + 1].copy()).to(DEV)
+        v1 = torch.from_numpy(xv[:, :, t:t + 1].copy()).to(DEV)
+        ka.append(k1)
+        va.append(v1)
+        out_a = P.decode(ka, va, q)
+        out_b = P.decode_step(kb, vb, k1, v1, q)
+        torch.cuda.synchronize()
+        assert torch.equal(out_a, out_b), f"step {t}"
+    assert kb.sync() == 0 and vb.sync() == 0
+    assert kb.length == S + steps and vb.length == S + steps
+    nb = (S + steps) // 32
+    assert np.array_equal(kb.record_array()[:, :, :nb], ka.record_array()[:, :, :nb])
+    assert np.array_equal(vb.record_array()[:, :, :nb], va.record_array()[:, :, :nb])
+    ref = O.attend(q.cpu().numpy(), oracle_view(kb, O.ROLE_KEY), oracle_view(vb, O.ROLE_VALUE))
+    err = O.relative_error(out_b.cpu().numpy(), ref)
+    assert err.max() <= ATTN_TOL, f"max rel err {err.max():.3e}"
+
+
 @pytest.mark.parametrize("S", [1, 5, 31, 32, 33, 64, 95, 1000, 4099])
 def test_decode_lengths(P, S):
     run_decode_case(P, B=1, Hkv=2, Gq=3, S=S, rk=16, rv=24, n_groups=1, seed=S, steps=1)
