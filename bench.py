@@ -320,16 +320,15 @@ def run_palu(args, w, world, rank, local):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     outs = [torch.empty(w.batch, w.hq, 128, dtype=torch.float16, device=dev) for _ in range(L)]
 
-    def step_calls(slot, ev=None):
+    def step_calls(slot):
         for l in range(L):
             kc, vc = caches[l]
-            kc.append(ks[l][slot], stream=s)
-            vc.append(vs[l][slot], stream=s)
-            if ev is not None:
-                ev[l][0].record(s)
-            P.palu_decode_attn(kc.c, vc.c, qs[l][slot], outs[l], ws, stream=s)
-            if ev is not None:
-                ev[l][1].record(s)
+            if args.unfused:
+                kc.append(ks[l][slot], stream=s)
+                vc.append(vs[l][slot], stream=s)
+                P.palu_decode_attn(kc.c, vc.c, qs[l][slot], outs[l], ws, stream=s)
+            else:
+                P.palu_decode_step(kc.c, vc.c, ks[l][slot], vs[l][slot], qs[l][slot], outs[l], ws, stream=s)
 
     def reset_calls():
         for kc, vc in caches:
@@ -345,16 +344,11 @@ def run_palu(args, w, world, rank, local):
         kc.sync(s)
         vc.sync(s)
 
-    try:
-        events = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] for _ in range(L)]
-                  for _ in range(NP)]
-    except TypeError:
-        events = None
     graphs = []
     for slot in range(NP):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
-            step_calls(slot, events[slot] if events else None)
+            step_calls(slot)
         graphs.append(g)
     g_reset = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_reset, stream=s):
@@ -365,7 +359,7 @@ def run_palu(args, w, world, rank, local):
         vc.sync(s)
 
     def run_steps(n, first):
-        """Replay n steps starting at global step index `first`; returns (lengths, launches)."""
+        """Replay n steps starting at global step index `first`; returns the context lengths."""
         lengths = []
         for i in range(first, first + n):
             pos = i % EPISODE
@@ -395,25 +389,38 @@ def run_palu(args, w, world, rank, local):
     kv_tokens_per_step = w.batch * s_ctx * L
     value = whole_job_rate(world * kv_tokens_per_step, ms_max / 1e3)
 
-    # per-launch decode duration from the in-graph events of the last replays
-    # (each layer has its own ranks, hence its own algorithmic bytes)
+    # each layer has its own ranks, hence its own algorithmic bytes
     def layer_bytes(l, ctx):
         rk, nk, rv, nv = layer_ranks[l]
         return decode_bytes(w, rk, nk, rv, nv, ctx, w.quantize_values, out_bytes=2)
 
-    launches = []     # (layer, ms, context)
-    if events:
-        for slot in range(NP):
-            ctx_slot = [c for i, c in enumerate(lengths) if (W + i) % NP == slot][-1]   # its last replay
-            for l in range(L):
-                launches.append((l, events[slot][l][0].elapsed_time(events[slot][l][1]), ctx_slot))
-    else:
-        launches = eager_launch_times(P, caches, qs, outs, ws, s, L)
-    tot_ms = sum(ms for _, ms, _ in launches)
-    avg_launch = tot_ms / len(launches)
-    bytes_launch = sum(layer_bytes(l, ctx) for l, _, ctx in launches) / len(launches)
+    # decode attention alone (palu_decode_attn over every layer's caches as
+    # they stand after the timed steps), timed over whole-graph replays with
+    # events on the launching stream: the average launch duration inside a
+    # back-to-back sequence of layers, as in the step
+    ctx_now = lengths[-1]
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=s):
+        for l in range(L):
+            kc, vc = caches[l]
+            P.palu_decode_attn(kc.c, vc.c, qs[l][0], outs[l], ws, stream=s)
+    R2 = 10
+    a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            g2.replay()
+        a2.record(s)
+        for _ in range(R2):
+            g2.replay()
+        b2.record(s)
+    torch.cuda.synchronize()
+    tot_ms = a2.elapsed_time(b2)
+    n_launch = R2 * L
+    avg_launch = tot_ms / n_launch
+    layer_sum = sum(layer_bytes(l, ctx_now) for l in range(L))
+    bytes_launch = layer_sum / L
     peak, peak_kind = peaks()
-    achieved = sum(layer_bytes(l, ctx) for l, _, ctx in launches) / (tot_ms / 1e3) / 1e9
+    achieved = R2 * layer_sum / (tot_ms / 1e3) / 1e9
     for kc, vc in caches:
         kc.sync(s)
         vc.sync(s)
@@ -421,7 +428,7 @@ def run_palu(args, w, world, rank, local):
     # ---- end-to-end: pinned host inputs copied in, outputs copied out, every step
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(P, w, caches, s, L, S, outs, ws, W, K, world, dev)
+        e2e = run_e2e(P, w, caches, s, L, S, outs, ws, W, K, world, dev, args.unfused)
 
     # ---- fp16 comparator on identical shapes
     comp = None
@@ -443,14 +450,16 @@ def run_palu(args, w, world, rank, local):
                    "l2": "inputs larger than L2: %.2f GB of caches read per step" % (
                        L * bytes_launch / 1e9),
                    "episode_resets_in_timed_region": n_resets},
-        # per layer and step: two one-token appends, q-prep, decode, combine;
+        # per layer and step: palu_decode_step = step prologue (both appends
+        # and q-prep), then decode (unfused: two appends, q-prep, decode);
         # per episode reset: two truncates per layer
-        "gpu_launches": K * L * 5 + n_resets * L * 2,
-        "roofline": {"bound": "hbm", "kernel": "palu_decode_attn (q-prep + split decode + combine)",
+        "gpu_launches": K * L * (4 if args.unfused else 2) + n_resets * L * 2,
+        "roofline": {"bound": "hbm",
+                     "kernel": "palu_decode_attn (q-prep + split decode with in-kernel merge), graph of all layers",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "traffic": traffic_record(),
                      "algorithmic_bytes_per_launch": bytes_launch, "avg_launch_us": avg_launch * 1e3,
-                     "launches_timed": len(launches)},
+                     "launches_timed": n_launch},
         "clocks": clk.summary(),
         "prefill": {"fit_ms_layer0_kv": fit_ms, "encode_ms_layer0_kv": enc_ms,
                     "prefill_tokens_per_layer": w.batch * S},
@@ -465,23 +474,7 @@ def run_palu(args, w, world, rank, local):
     return result
 
 
-def eager_launch_times(P, caches, qs, outs, ws, s, L, reps=3):
-    """Per-launch decode times with the queue kept full by a leading sleep kernel."""
-    ev = []
-    with torch.cuda.stream(s):
-        torch.cuda._sleep(int(2e8))
-        for _ in range(reps):
-            for l in range(L):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(s)
-                P.palu_decode_attn(caches[l][0].c, caches[l][1].c, qs[l][0], outs[l], ws, stream=s)
-                b.record(s)
-                ev.append((l, a, b, caches[l][0].c.length))
-    torch.cuda.synchronize()
-    return [(l, a.elapsed_time(b), ctx) for l, a, b, ctx in ev]
-
-
-def run_e2e(P, w, caches, s, L, S, outs, ws, W, K, world, dev):
+def run_e2e(P, w, caches, s, L, S, outs, ws, W, K, world, dev, unfused=False):
     """Same metric through the same calls, with each step's q/k/v copied from
     pinned host memory and the step's outputs copied back, inside the timing."""
     from rank_latent_kv_gb300 import synth
@@ -501,9 +494,12 @@ def run_e2e(P, w, caches, s, L, S, outs, ws, W, K, world, dev):
     def calls():
         for l in range(L):
             kc, vc = caches[l]
-            kc.append(k_dev[l], stream=s)
-            vc.append(v_dev[l], stream=s)
-            P.palu_decode_attn(kc.c, vc.c, q_dev[l], out_dev[l], ws, stream=s)
+            if unfused:
+                kc.append(k_dev[l], stream=s)
+                vc.append(v_dev[l], stream=s)
+                P.palu_decode_attn(kc.c, vc.c, q_dev[l], out_dev[l], ws, stream=s)
+            else:
+                P.palu_decode_step(kc.c, vc.c, k_dev[l], v_dev[l], q_dev[l], out_dev[l], ws, stream=s)
 
     def reset():
         for kc, vc in caches:
@@ -620,6 +616,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="qwen7b")
     ap.add_argument("--layers", type=int, default=0, help="layers to build and time (default: the workload's)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="separate append/append/decode calls instead of palu_decode_step")
     ap.add_argument("--no-comparator", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for the CPU baseline")

@@ -186,12 +186,12 @@ palu_status palu_decode_workspace_size(const palu_cache* k, const palu_cache* v,
  *   out  device [batch, q_heads, D], fp32 if out_fp32 else fp16.
  *   softmax_scale 0 selects 1/sqrt(D).
  *   workspace  device scratch of palu_decode_workspace_size bytes (packed
- *        query factors and per-stream partial results); no initial contents
- *        are needed.
- * k and v must have the same batch, kv_heads and length.  Three kernel
- * launches on `stream` (query factors, the split attention over the code
- * blocks, the per-stream combine); calls that share a workspace must not
- * overlap on the GPU. */
+ *        query factors, per-stream tickets and partial results); no initial
+ *        contents are needed.
+ * k and v must have the same batch, kv_heads and length.  Two kernel
+ * launches on `stream` (the query factors, then the split attention over
+ * the code blocks, whose last CTA per stream merges that stream's partials);
+ * calls that share a workspace must not overlap on the GPU. */
 palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v, const void* q,
                              int32_t q_heads, float softmax_scale, void* out, int32_t out_fp32,
                              void* workspace, size_t workspace_bytes, void* stream);
@@ -201,7 +201,7 @@ palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v, const voi
  * cached token including the new one (decode step 3); the same results as
  * palu_encode_append(k, k_new, 1), palu_encode_append(v, v_new, 1) and
  * palu_decode_attn(k, v, q, ...) in that order.  The "fused per-step
- * pipeline" of this library: three kernel launches instead of five (the two
+ * pipeline" of this library: two kernel launches instead of four (the two
  * appends and the query factors share one launch).
  *   k_new, v_new  device fp16 [batch, kv_heads, D] (one token per stream).
  *   q, out, softmax_scale, out_fp32, workspace  as for palu_decode_attn

@@ -121,9 +121,10 @@ __device__ void qprep_stream(const DecodeParams& p, long long X, float max_s_flo
     }
   }
   __syncthreads();
-  // scaled q~ and c for the combine's tail tokens
+  // scaled q~ and c for the tail tokens; the stream's ticket starts at zero
   for (int i = tid; i < 8 * kHeadDim; i += 256) p.qt[(size_t)X * 8 * kHeadDim + i] = qt_s[i >> 7][i & (kHeadDim - 1)];
   if (tid < 8) p.cq[(size_t)X * 8 + tid] = cq_s[tid];
+  if (tid == 0) p.tickets[X] = 0u;
   if (warp == 0) {
     amax = 0.f;
 #pragma unroll
@@ -200,182 +201,11 @@ __global__ void __launch_bounds__(256) latent_step_prologue_kernel(const DecodeP
   }
 }
 
-// ------------------------------------------------------------------ combine
-// One CTA per stream, after the decode kernel: merge the stream's partials
-// (log-sum-exp), fold in the fp32 tail tokens, apply V^V^T and + mu^V.
-// Dynamic shared memory: V basis [rv][128], tails, partials, tail weights,
-// merged latents, denominators.
-__global__ void __launch_bounds__(256) latent_combine_kernel(const DecodeParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ uint64_t mbar, mbar_p;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const long long X = blockIdx.x;
-  const int b = (int)(X / p.Hkv), kh = (int)(X % p.Hkv), Gq = p.Gq;
-  const int rk = p.k.r, rv = p.v.r, ms = kPartHead + p.rvp;
-  const int gv = kh / p.v.heads_per_group;
-  const int rec_v = p.v.rec_bytes;
-  const int tv_bytes = p.v.quantize ? kBlock * rv * 4 : rec_v;
-  float* BV_s = reinterpret_cast<float*>(smem);                 // [rv][128]
-  float* TK_s = BV_s + (size_t)rv * kHeadDim;                    // [32][rk]
-  float* TV_s = TK_s + (size_t)kBlock * rk;                      // [32][rv] (or one fp16 record)
-  float* P_s = TV_s + (tv_bytes + 15) / 16 * 4;                  // [nseg][Gq][ms] partials
-  float* ST_s = P_s + (size_t)p.seg_max * Gq * ms;               // [8][32] tail scores, then weights
-  float* O_s = ST_s + 8 * kBlock;                                // [8][128] merged latents
-  float* L_s = O_s + 8 * kHeadDim;                               // [8]
-
-  // everything but the partials and q~ was written before the q-prep launch:
-  // fetch it while the decode kernel is still running
-  const long long len = __ldcg(&p.k.hdr->length);
-  const long long nf = len / kBlock;
-  const int n_tail = (int)(len % kBlock);
-  const long long T = p.streams * nf;
-  int nseg = 0;
-  if (T > 0) {
-    // the decode launch's warps that take part; one partial per CTA
-    const long long W = min((long long)p.dec_grid * kDecWarps, T);
-    nseg = (int)(block_owner(X * nf + nf - 1, T, W) / kDecWarps - block_owner(X * nf, T, W) / kDecWarps + 1);
-  }
-  const float mu_v = __ldg(p.v.mu + (size_t)gv * kHeadDim + (tid & 127));
-  if (tid == 0) {
-    mbar_init(&mbar, 1);
-    mbar_init(&mbar_p, 1);
-    fence_mbar_init();
-    const uint32_t bytes = (uint32_t)rv * 512u + (n_tail > 0 ? (uint32_t)(kBlock * rk * 4 + tv_bytes) : 0u);
-    mbar_arrive_expect_tx(&mbar, bytes);
-    bulk_g2s(BV_s, p.v.basisT + (size_t)gv * rv * kHeadDim, (uint32_t)rv * 512u, &mbar);
-    if (n_tail > 0) {
-      bulk_g2s(TK_s, p.k.tail + (size_t)X * kBlock * rk, (uint32_t)(kBlock * rk * 4), &mbar);
-      const void* tv = p.v.quantize ? static_cast<const void*>(p.v.tail + (size_t)X * kBlock * rv)
-                                    : static_cast<const void*>(p.v.blocks + ((size_t)X * p.v.n_blk_cap + nf) * rec_v);
-      bulk_g2s(TV_s, tv, (uint32_t)tv_bytes, &mbar);
-    }
-  }
-  grid_dep_wait();  // the decode kernel's partials (and, through it, q~ and c)
-  if (tid == 0) {
-    // the stream's partials are contiguous: one bulk copy
-    const uint32_t pbytes = (uint32_t)nseg * Gq * ms * 4u;
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    mbar_arrive_expect_tx(&mbar_p, pbytes);
-    if (pbytes > 0) bulk_g2s(P_s, p.ws + (size_t)X * p.seg_max * Gq * ms, pbytes, &mbar_p);
-  }
-  __syncthreads();  // barriers initialised
-  const bool got = mbar_wait_bounded(&mbar, 0) && mbar_wait_bounded(&mbar_p, 0);
-  if (!got && tid == 0) set_dev_error(p.k.hdr, PALU_DEVERR_TIMEOUT);
-  // tail scores (log2 units)
-  const float* qt = p.qt + (size_t)X * 8 * kHeadDim;
-  for (int i = tid; i < n_tail * 8; i += 256) {
-    const int t = i >> 3, h = i & 7;
-    float sc_t = -INFINITY;
-    if (h < Gq) {
-      sc_t = __ldcg(p.cq + (size_t)X * 8 + h);
-      for (int j2 = 0; j2 < rk; ++j2) {
-        const int pch = j2 < p.k.n_hi ? j2 : 8 * p.k.n_hi_oct + (j2 - p.k.n_hi);
-        sc_t = fmaf(__ldcg(qt + h * kHeadDim + pch), TK_s[t * rk + j2], sc_t);
-      }
-    }
-    ST_s[h * kBlock + t] = sc_t;
-  }
-  __syncthreads();
-  // warp h: max, weights (over the partials' m), denominator
-  if (warp < Gq) {
-    const int h = warp;
-    float M = -INFINITY;
-    for (int sg = lane; sg < nseg; sg += 32) M = fmaxf(M, P_s[(sg * Gq + h) * ms]);
-    const float st = lane < n_tail ? ST_s[h * kBlock + lane] : -INFINITY;
-    M = fmaxf(M, st);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.f;
-    for (int sg = lane; sg < nseg; sg += 32) {
-      const float m = P_s[(sg * Gq + h) * ms];
-      const float w = m == -INFINITY ? 0.f : ex2(m - M);
-      L = fmaf(w, P_s[(sg * Gq + h) * ms + 1], L);
-      P_s[(sg * Gq + h) * ms] = w;
-    }
-    const float pt = lane < n_tail ? ex2(st - M) : 0.f;
-    L += pt;
-    __syncwarp();
-    ST_s[h * kBlock + lane] = pt;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    if (lane == 0) L_s[h] = L;
-  }
-  __syncthreads();
-  // merged latent per (head, real value channel)
-  for (int i = tid; i < Gq * p.rvp; i += 256) {
-    const int h = i / p.rvp, pch = i - h * p.rvp;
-    const int j2 = padded_to_channel(pch, rv, p.v.n_hi, p.v.n_hi_oct, p.v.quantize);
-    if (j2 < 0) continue;
-    float a4[4] = {0.f, 0.f, 0.f, 0.f};
-    int sg = 0;
-    for (; sg + 4 <= nseg; sg += 4) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float* pr = P_s + ((size_t)(sg + u) * Gq + h) * ms;
-        a4[u] = fmaf(pr[0], pr[kPartHead + pch], a4[u]);
-      }
-    }
-    for (; sg < nseg; ++sg) {
-      const float* pr = P_s + ((size_t)sg * Gq + h) * ms;
-      a4[0] = fmaf(pr[0], pr[kPartHead + pch], a4[0]);
-    }
-    float a = (a4[0] + a4[1]) + (a4[2] + a4[3]);
-    for (int t = 0; t < n_tail; ++t) {
-      float lv;
-      if (p.v.quantize) {
-        lv = TV_s[t * rv + j2];
-      } else {
-        const int kk = 2 * (t >> 4) + ((t & 15) >> 3);
-        const int ln = 4 * (j2 & 7) + ((t & 7) >> 1);
-        lv = __half2float(*reinterpret_cast<const __half*>(reinterpret_cast<const uint8_t*>(TV_s) + 512 * (j2 >> 3) +
-                                                           16 * ln + 4 * kk + 2 * (t & 1)));
-      }
-      a = fmaf(ST_s[h * kBlock + t], lv, a);
-    }
-    O_s[h * kHeadDim + j2] = a;
-  }
-  __syncthreads();
-  // out[h][d] = (sum_j o_hj V[d, j]) / L_h + mu[d]
-  {
-    const int d = tid & 127, h0 = (tid >> 7) * 4;
-    float o4[4] = {0.f, 0.f, 0.f, 0.f};
-    int j2 = 0;
-    for (; j2 + 4 <= rv; j2 += 4) {
-      const float b0 = BV_s[j2 * kHeadDim + d], b1 = BV_s[(j2 + 1) * kHeadDim + d];
-      const float b2 = BV_s[(j2 + 2) * kHeadDim + d], b3 = BV_s[(j2 + 3) * kHeadDim + d];
-#pragma unroll
-      for (int hh = 0; hh < 4; ++hh) {
-        const float4 o = *reinterpret_cast<const float4*>(O_s + (h0 + hh) * kHeadDim + j2);
-        o4[hh] = fmaf(o.x, b0, fmaf(o.y, b1, fmaf(o.z, b2, fmaf(o.w, b3, o4[hh]))));
-      }
-    }
-    for (; j2 < rv; ++j2) {
-      const float bv = BV_s[j2 * kHeadDim + d];
-#pragma unroll
-      for (int hh = 0; hh < 4; ++hh) o4[hh] = fmaf(O_s[(h0 + hh) * kHeadDim + j2], bv, o4[hh]);
-    }
-    const float mu = mu_v;
-#pragma unroll
-    for (int hh = 0; hh < 4; ++hh) {
-      const int h = h0 + hh;
-      if (h < Gq) {
-        const float v = fmaf(o4[hh], 1.f / L_s[h], mu);
-        const long long oi = ((long long)b * p.Hq + (long long)kh * Gq + h) * kHeadDim + d;
-        if (p.out_fp32)
-          static_cast<float*>(p.out)[oi] = v;
-        else
-          static_cast<__half*>(p.out)[oi] = __float2half_rn(v);
-      }
-    }
-  }
-}
-
 struct DecodePlan {
   int KC, VC;
   bool VQ;
-  int ns, stage_bytes, ring_off, wp_off, smem, grid, seg_max, rvp, qp_ko, qp_stride;
-  size_t comb_smem;
-  size_t qpack_off, qt_off, cq_off, part_off, ws_bytes;
+  int nw, ns, stage_bytes, ring_off, wp_off, end_off, end_off2, smem, grid, seg_max, rvp, qp_ko, qp_stride;
+  size_t qpack_off, qt_off, cq_off, tick_off, part_off, ws_bytes;
   DecodeKernel kern;
 };
 
@@ -427,46 +257,45 @@ static palu_status plan_decode(const palu_cache* k, const palu_cache* v, int32_t
   pl->stage_bytes = 2 * (rec_k + rec_v);
   pl->ns = pl->stage_bytes <= 2048 ? 4 : pl->stage_bytes <= 6144 ? 3 : 2;
   pl->rvp = 8 * v->n_oct;
-  pl->ring_off = (int)align_up(kDecBarOff + 8 * kDecWarps * pl->ns, 128);
   const int64_t streams = (int64_t)k->batch * k->kv_heads;
   const int sms = device_sm_count();
-  const size_t rings = (size_t)kDecWarps * pl->ns * pl->stage_bytes;
-  pl->wp_off = (int)align_up(pl->ring_off + rings, 16);
-  pl->smem = (int)(pl->wp_off + (size_t)kDecWarps * 2 * Gq * (kPartHead + pl->rvp) * 4);
+  // the end phase reuses the rings when they are large enough
+  const EndLayout el = end_layout(k->rank, v->rank, v->quantize, rec_v);
+  // 16 warps in one CTA per SM when the rings fit (every warp of an SM then
+  // has the same scheduling age, and their ranges end together), else 8
+  const bool exact = k->n_oct <= 8 && v->n_oct <= 8;
+  for (int nw = exact ? kMaxDecWarps : kMaxDecWarps / 2; nw >= 8; nw /= 2) {
+    pl->nw = nw;
+    pl->ring_off = (int)align_up(kDecBarOff + 8 * (nw * pl->ns + 2), 128);
+    const size_t rings = (size_t)nw * pl->ns * pl->stage_bytes;
+    pl->wp_off = (int)align_up(pl->ring_off + rings, 16);
+    const size_t wp_end = pl->wp_off + (size_t)nw * 2 * Gq * (kPartHead + pl->rvp) * 4;
+    pl->end_off = (size_t)el.bytes <= rings ? pl->ring_off : (int)align_up(wp_end, 16);
+    pl->smem = (int)std::max(wp_end, (size_t)pl->end_off + el.bytes);
+    // a second end area inside the rings, for a CTA that finishes two streams at once
+    const size_t el16 = align_up(el.bytes, 16);
+    pl->end_off2 = (nw == kMaxDecWarps && 2 * el16 <= rings) ? (int)(pl->ring_off + el16) : -1;
+    if (pl->smem <= 227 * 1024) break;
+  }
   if (pl->smem > 227 * 1024) return fail(PALU_ERR_UNSUPPORTED, "decode shared-memory plan exceeds 227 KB");
   int per_sm = 0;
-  palu_status st = kernel_occupancy(reinterpret_cast<const void*>(pl->kern), kDecThreads, pl->smem, &per_sm);
+  palu_status st = kernel_occupancy(reinterpret_cast<const void*>(pl->kern), 32 * pl->nw, pl->smem, &per_sm);
   if (st != PALU_OK) return st;
   int64_t grid = (int64_t)sms * std::min(per_sm, 4);
   grid = std::min<int64_t>(grid, std::max<int64_t>(1, streams * k->n_blk_cap));
   // at least one warp per stream, so that no warp's range spans more than two
   // streams (extra CTAs, if any, simply run in a second wave)
-  grid = std::max<int64_t>(grid, (streams + kDecWarps - 1) / kDecWarps);
+  grid = std::max<int64_t>(grid, (streams + pl->nw - 1) / pl->nw);
   pl->grid = (int)std::max<int64_t>(1, grid);
-  // the combine stages one stream's partials on chip (one per CTA that
-  // touches the stream: at most ceil(CTAs / streams) + 1); with few streams,
-  // use fewer CTAs so that they fit
-  const int tv_bytes = v->quantize ? kBlock * v->rank * 4 : rec_v;
-  const size_t comb_fixed = (size_t)v->rank * 512 + (size_t)128 * k->rank + align_up(tv_bytes, 16) +
-                            8 * kBlock * 4 + 8 * kHeadDim * 4 + 32;
-  const size_t per_seg = (size_t)Gq * (kPartHead + pl->rvp) * 4;
-  const size_t comb_budget = 200 * 1024;
+  // CTAs that touch one stream: at most ceil(CTAs / streams) + 1
   pl->seg_max = (int)((pl->grid + streams - 1) / streams + 1);
-  if (comb_fixed + pl->seg_max * per_seg > comb_budget) {
-    const int64_t seg_fit = (int64_t)((comb_budget - comb_fixed) / per_seg);
-    if (seg_fit < 2) return fail(PALU_ERR_UNSUPPORTED, "decode merge does not fit in shared memory");
-    pl->grid = (int)std::max<int64_t>(1, std::min<int64_t>(pl->grid, streams * (seg_fit - 1)));
-    pl->grid = (int)std::max<int64_t>(pl->grid, (streams + kDecWarps - 1) / kDecWarps);
-    pl->seg_max = (int)((pl->grid + streams - 1) / streams + 1);
-  }
-  pl->comb_smem = comb_fixed + pl->seg_max * per_seg;
-  if (pl->comb_smem > 227 * 1024) return fail(PALU_ERR_UNSUPPORTED, "decode merge does not fit in shared memory");
-  // workspace: packed query factors, q~ and c per stream, partials
+  // workspace: packed query factors, q~ and c per stream, tickets, partials
   pl->qpack_off = 0;
   pl->qt_off = align_up(pl->qpack_off + sizeof(uint32_t) * (size_t)streams * 32 * pl->qp_stride, 256);
   pl->cq_off = align_up(pl->qt_off + sizeof(float) * (size_t)streams * 8 * kHeadDim, 256);
-  pl->part_off = align_up(pl->cq_off + sizeof(float) * (size_t)streams * 8, 256);
-  pl->ws_bytes = align_up(pl->part_off + sizeof(float) * (size_t)streams * pl->seg_max * Gq * (kPartHead + pl->rvp), 256);
+  pl->tick_off = align_up(pl->cq_off + sizeof(float) * (size_t)streams * 8, 256);
+  pl->part_off = align_up(pl->tick_off + sizeof(uint32_t) * (size_t)streams, 256);
+  pl->ws_bytes = align_up(pl->part_off + sizeof(float) * (size_t)streams * pl->seg_max * Gq * kOutPart, 256);
   return PALU_OK;
 }
 
@@ -489,6 +318,7 @@ static DecodeParams decode_params(const DecodePlan& pl, const palu_cache* k, con
   p.qt = reinterpret_cast<float*>(ws + pl.qt_off);
   p.cq = reinterpret_cast<float*>(ws + pl.cq_off);
   p.ws = reinterpret_cast<float*>(ws + pl.part_off);
+  p.tickets = reinterpret_cast<uint32_t*>(ws + pl.tick_off);
   p.out_fp32 = out_fp32;
   p.Hq = q_heads;
   p.Hkv = k->kv_heads;
@@ -498,6 +328,8 @@ static DecodeParams decode_params(const DecodePlan& pl, const palu_cache* k, con
   p.stage_bytes = pl.stage_bytes;
   p.ring_off = pl.ring_off;
   p.wp_off = pl.wp_off;
+  p.end_off = pl.end_off;
+  p.end_off2 = pl.end_off2;
   p.seg_max = pl.seg_max;
   p.qp_ko = pl.qp_ko;
   p.qp_stride = pl.qp_stride;
@@ -509,32 +341,20 @@ static DecodeParams decode_params(const DecodePlan& pl, const palu_cache* k, con
   return p;
 }
 
-// The decode kernel and the combine, each started while its predecessor
-// finishes (programmatic dependent launch; each waits in-kernel).
-static palu_status launch_decode_combine(const DecodePlan& pl, const DecodeParams& p, cudaStream_t strm) {
-  const unsigned int n_streams = (unsigned int)p.streams;
-  int per_sm = 0;
-  palu_status st =
-      kernel_occupancy(reinterpret_cast<const void*>(latent_combine_kernel), 256, (int)pl.comb_smem, &per_sm);
-  if (st != PALU_OK) return st;
-  // decode and combine each start while their predecessor finishes
-  // (programmatic dependent launch; each waits in-kernel for the results)
+// The decode kernel, started while its predecessor finishes (programmatic
+// dependent launch; it waits in-kernel for the query factors).
+static palu_status launch_decode(const DecodePlan& pl, const DecodeParams& p, cudaStream_t strm) {
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr.val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.grid);
-  cfg.blockDim = dim3(kDecThreads);
+  cfg.blockDim = dim3(32 * pl.nw);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = strm;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  st = cuda_check(cudaLaunchKernelEx(&cfg, pl.kern, p), "latent_decode_kernel launch");
-  if (st != PALU_OK) return st;
-  cfg.gridDim = dim3(n_streams);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = pl.comb_smem;
-  return cuda_check(cudaLaunchKernelEx(&cfg, latent_combine_kernel, p), "latent_combine_kernel launch");
+  return cuda_check(cudaLaunchKernelEx(&cfg, pl.kern, p), "latent_decode_kernel launch");
 }
 }  // namespace palu
 
@@ -567,7 +387,7 @@ extern "C" palu_status palu_decode_attn(const palu_cache* k, const palu_cache* v
   latent_qprep_kernel<<<(unsigned int)p.streams, 256, 0, strm>>>(p);
   st = cuda_check(cudaGetLastError(), "latent_qprep_kernel launch");
   if (st != PALU_OK) return st;
-  return launch_decode_combine(pl, p, strm);
+  return launch_decode(pl, p, strm);
 }
 
 extern "C" palu_status palu_decode_step(palu_cache* k, palu_cache* v, const void* k_new, const void* v_new,
@@ -599,7 +419,7 @@ extern "C" palu_status palu_decode_step(palu_cache* k, palu_cache* v, const void
   if (st != PALU_OK) return st;
   k->length += 1;
   v->length += 1;
-  return launch_decode_combine(pl, p, strm);
+  return launch_decode(pl, p, strm);
 }
 
 // ------------------------------------------------------------------ allocation-free decode

@@ -34,10 +34,12 @@
 //    come out of the tensor cores too (an all-ones A operand).
 //  * Weighted sum on tensor cores: values dequantized once to fp16
 //    (HFMA2 code*s+z) as A (channels x tokens), the probabilities as B.
-//  * Each CTA merges its warps (log-sum-exp) into one partial per segment; a
-//    per-stream ticket in the key cache's state picks the last contributor,
-//    which merges the stream's partials, folds in the fp32 tail tokens and
-//    applies V^V^T and + mu^V once per query head.
+//  * Each CTA merges its warps (log-sum-exp) per stream, the CTA holding a
+//    stream's last full block folds in the fp32 tail tokens, and every CTA
+//    applies V^V^T to its merged latent (the projection is linear, so it
+//    commutes with the final merge).  A CTA that covers a whole stream writes
+//    the output; otherwise a per-stream ticket in the workspace picks the
+//    stream's last CTA, which merges the projected partials and adds mu^V.
 #pragma once
 
 #include <math.h>
@@ -46,15 +48,20 @@
 
 namespace palu {
 
-constexpr int kDecWarps = 8;
-constexpr int kDecThreads = 32 * kDecWarps;
+constexpr int kMaxDecWarps = 16;  // warps per decode CTA: 16 (one CTA per SM) or 8; the class
+                                  // kernels (large ranks, many registers) always run 8
+constexpr int kMaxDecThreads = 32 * kMaxDecWarps;
 constexpr float kLazyTau = 8.f;   // log2 headroom before the running max is raised
-constexpr int kDecFlagOff = 0;    // decode CTA shared memory: flags int [4]
-constexpr int kDecBarOff = 64;    // then mbarriers [warps][ns]; the rings follow
+constexpr int kDecFlagOff = 0;                  // decode CTA shared memory: flags int [2 * warps]
+constexpr int kDecBarOff = 8 * kMaxDecWarps;    // then mbarriers [warps][ns] + 2; the rings follow
 // A partial (per segment and query head): m, l, two pad words, then the
 // latent accumulator per padded value channel; 16-byte multiple, so one
 // stream's partials move as a single bulk copy.
 constexpr int kPartHead = 4;
+// A projected partial (per CTA, stream and query head): m, l, two pad words,
+// then sum_t p_t v_t over the head dimension.
+constexpr int kOutHead = 4;
+constexpr int kOutPart = kOutHead + kHeadDim;
 
 struct DecodeParams {
   CacheView k, v;
@@ -63,7 +70,8 @@ struct DecodeParams {
   uint32_t* qpack;    // per stream and lane: Qh[ko], Ql[ko], CQ0, CQ1, 2^e, 2^-e  (qp_stride words)
   float* qt;          // per stream: scaled q~ [8][128] per padded key channel
   float* cq;          // per stream: scaled q . mu^K [8]
-  float* ws;          // partials [streams][seg_max][Gq][kPartHead + rvp]
+  float* ws;          // projected partials [streams][seg_max][Gq][kOutPart]
+  uint32_t* tickets;  // per stream: CTAs done with the stream (zeroed by the q-prep)
   int out_fp32;
   int Hq, Hkv, Gq;
   int rvp;            // padded value channels = 8 * v.n_oct
@@ -71,6 +79,8 @@ struct DecodeParams {
   int stage_bytes;    // 2 * (k.rec_bytes + v.rec_bytes)
   int ring_off;       // shared-memory offset of the rings
   int wp_off;         // shared-memory offset of the warps' partials [warps][2][Gq][kPartHead + rvp]
+  int end_off;        // shared-memory offset of the end phase's area (EndSmem)
+  int end_off2;       // a second end area (two streams in parallel), or -1
   int seg_max;        // partial slots per stream
   int qp_ko;          // key octets held per lane in qpack
   int qp_stride;      // words per lane in qpack
@@ -118,6 +128,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // let the next launch be scheduled.  Both are no-ops without the attribute.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Named barrier over n threads (id 0 with the whole CTA is __syncthreads).
+__device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+// Bulk prefetch of global bytes into L2 (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ uint32_t ld32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 __device__ __forceinline__ uint32_t ld16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
 
@@ -331,6 +347,59 @@ __device__ __forceinline__ void value_block(const uint8_t* vr, const GV& gv, int
   }
 }
 
+// Shared-memory area of the decode kernel's end phase (one stream at a time;
+// it reuses the rings when they are large enough).  Byte offsets from its
+// 16-byte aligned base, shared by the launch plan and the kernel.
+struct EndLayout {
+  int bv, qt, cq, tk, tv, st, ol, sw, wk, hm, hl, wo, flag, bytes;
+};
+__host__ __device__ inline EndLayout end_layout(int rk, int rv, int v_quantize, int rec_v) {
+  EndLayout e;
+  e.bv = 0;                                   // V basis rows [rv][128]
+  e.qt = e.bv + rv * kHeadDim * 4;            // scaled q~ [8][128]
+  e.cq = e.qt + 8 * kHeadDim * 4;             // scaled q . mu^K [8]
+  e.tk = e.cq + 32;                           // key tail latents [32][rk | 1]
+  e.tv = e.tk + kBlock * (rk | 1) * 4;        // value tail [32][rv] (or the fp16 record)
+  e.st = e.tv + (v_quantize ? kBlock * rv * 4 : rec_v);
+  e.ol = e.st + 8 * kBlock * 4;               // tail scores, then weights [8][32]
+  e.sw = e.ol + 8 * kHeadDim * 4;             // merged latents [8][128]
+  e.wk = e.sw + 32 * 8 * 4;                   // weights of the warp segments [32][8]
+  e.hm = e.wk + 8 * 32 * 4;                   // final merge: partial weights [8][32]
+  e.hl = e.hm + 32;                           // running max, sum, tail rescale [8]
+  e.wo = e.hl + 32;
+  e.flag = e.wo + 32;
+  e.bytes = e.flag + 16;
+  return e;
+}
+struct EndSmem {
+  float *bv, *qt, *cq, *tk, *tv, *st, *ol, *sw, *wk, *hm, *hl, *wo;
+  int* flag;
+};
+__device__ __forceinline__ EndSmem end_smem(uint8_t* base, const DecodeParams& p) {
+  const EndLayout e = end_layout(p.k.r, p.v.r, p.v.quantize, p.v.rec_bytes);
+  EndSmem s;
+  s.bv = reinterpret_cast<float*>(base + e.bv);
+  s.qt = reinterpret_cast<float*>(base + e.qt);
+  s.cq = reinterpret_cast<float*>(base + e.cq);
+  s.tk = reinterpret_cast<float*>(base + e.tk);
+  s.tv = reinterpret_cast<float*>(base + e.tv);
+  s.st = reinterpret_cast<float*>(base + e.st);
+  s.ol = reinterpret_cast<float*>(base + e.ol);
+  s.sw = reinterpret_cast<float*>(base + e.sw);
+  s.wk = reinterpret_cast<float*>(base + e.wk);
+  s.hm = reinterpret_cast<float*>(base + e.hm);
+  s.hl = reinterpret_cast<float*>(base + e.hl);
+  s.wo = reinterpret_cast<float*>(base + e.wo);
+  s.flag = reinterpret_cast<int*>(base + e.flag);
+  return s;
+}
+__device__ __forceinline__ void store_out(const DecodeParams& p, long long i, float v) {
+  if (p.out_fp32)
+    static_cast<float*>(p.out)[i] = v;
+  else
+    static_cast<__half*>(p.out)[i] = __float2half_rn(v);
+}
+
 // Owner CTA of flat block i when T blocks are split evenly over G CTAs
 // (CTA c covers [floor(cT/G), floor((c+1)T/G))).
 __device__ __forceinline__ long long block_owner(long long i, long long T, long long G) {
@@ -341,21 +410,22 @@ __device__ __forceinline__ long long block_owner(long long i, long long T, long 
 // KC, VC: key / value record classes; KE, VE: exact octet counts, or 0 when
 // the kernel serves every count of its class.  Launched after the q-prep
 // kernel (programmatic dependent launch: the first copies are in flight
-// before the packed query factors are read) and before the combine kernel.
+// before the packed query factors are read).
 template <int KC, int VC, bool VQ, int KE, int VE>
-__global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 1)
+    latent_decode_kernel(const DecodeParams p) {
   using GK = Geom<KC, KE, true>;
   using GV = Geom<VC, VE, VQ>;
   constexpr int KO = GK::kMaxOct, VT = (GV::kMaxOct + 1) / 2;
   extern __shared__ __align__(128) uint8_t smem[];
-  int* flag_s = reinterpret_cast<int*>(smem + kDecFlagOff);  // [0..15] stream of each warp's segments
+  int* flag_s = reinterpret_cast<int*>(smem + kDecFlagOff);  // stream of each warp's two segments
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecBarOff);  // [warps][ns]
   uint8_t* ring = smem + p.ring_off;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+  const int nw = blockDim.x >> 5, nt = blockDim.x;  // 16 or 8 warps
   if (p.after_append) {
-    // the preceding launch wrote the length and maybe a new block: wait for
-    // it, and only then let the combine (which prefetches both) be scheduled
+    // the preceding launch wrote the length and maybe a new block
     grid_dep_wait();
   }
   grid_dep_launch();
@@ -367,8 +437,8 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
   // every warp works on its own: the flat range of full blocks is split over
   // at most T warps, so each warp that takes part owns >= 1 block and the
   // warps covering a stream are consecutive
-  const long long W = min((long long)gridDim.x * kDecWarps, T);
-  const long long gw = (long long)blockIdx.x * kDecWarps + warp;
+  const long long W = min((long long)gridDim.x * nw, T);
+  const long long gw = (long long)blockIdx.x * nw + warp;
   const long long R0 = gw < W ? gw * T / W : 0, R1 = gw < W ? (gw + 1) * T / W : 0;
   const int ns = p.ns, Gq = p.Gq;
   GK geo_k;
@@ -376,16 +446,47 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
   geo_k.init(p.k);
   geo_v.init(p.v);
   const int rec_k = geo_k.rec(), rec_v = geo_v.rec();
+  if (tid == 32) {
+    // warm L2 with what the end phase will copy: the V basis rows of the
+    // CTA's first and last stream, and the tails of a stream ending here
+    long long x0 = 0, x1 = -1, b_end = -1;
+    if (nf > 0) {
+      const long long c0 = min((long long)blockIdx.x * nw, W), c1 = min(c0 + nw, W);
+      if (c0 < c1) {
+        b_end = c1 * T / W;
+        x0 = (c0 * T / W) / nf;
+        x1 = (b_end - 1) / nf;
+      }
+    } else {
+      x0 = (long long)blockIdx.x * nw;
+      x1 = min(x0 + nw, p.streams) - 1;
+    }
+    if (x0 <= x1) {
+      const int g0 = (int)(x0 % p.Hkv) / p.v.heads_per_group, g1 = (int)(x1 % p.Hkv) / p.v.heads_per_group;
+      prefetch_l2(p.v.basisT + (size_t)g0 * p.v.r * kHeadDim, (uint32_t)p.v.r * 512u);
+      if (g1 != g0) prefetch_l2(p.v.basisT + (size_t)g1 * p.v.r * kHeadDim, (uint32_t)p.v.r * 512u);
+      if (len % kBlock != 0 && b_end == (x1 + 1) * nf) {
+        prefetch_l2(p.k.tail + (size_t)x1 * kBlock * p.k.r, (uint32_t)(kBlock * p.k.r * 4));
+        if (p.v.quantize)
+          prefetch_l2(p.v.tail + (size_t)x1 * kBlock * p.v.r, (uint32_t)(kBlock * p.v.r * 4));
+        else
+          prefetch_l2(p.v.blocks + ((size_t)x1 * p.v.n_blk_cap + nf) * p.v.rec_bytes, (uint32_t)p.v.rec_bytes);
+      }
+    }
+  }
 
   // ---- one-time setup: barriers
   if (tid == 0) {
-    for (int i = 0; i < kDecWarps * ns; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < nw * ns + 2; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
   }
   __syncthreads();
   const int ms = kPartHead + p.rvp;
   float* wp = reinterpret_cast<float*>(smem + p.wp_off) + (size_t)warp * 2 * Gq * ms;
   if (lane < 2) flag_s[2 * warp + lane] = -1;
+  // the warp partial slots start at zero: the end phase weighs every slot,
+  // with weight 0 for the slots of other streams or of no segment
+  for (int i = lane; i < 2 * Gq * ms; i += 32) wp[i] = 0.f;
 
   uint8_t* wring = ring + (size_t)warp * ns * p.stage_bytes;
   uint64_t* wbar = bars + warp * ns;
@@ -608,41 +709,295 @@ __global__ void __launch_bounds__(kDecThreads, (KC + VC >= 7) ? 1 : 2) latent_de
     }
   }
 
-  // ---- merge the CTA's warps per stream (log-sum-exp) into one partial per
-  // (stream, CTA); the CTAs covering a stream are consecutive
-  __syncthreads();
-  int xlo = 0x7fffffff, xhi = -1;
+  // ---- end phase, per stream this CTA touches: merge the warps (log-sum-exp),
+  // fold in the fp32 tail tokens (the CTA holding the stream's last full
+  // block; with no full block, CTA x / nw serves stream x), apply V^V^T, and
+  // either finish the stream or leave a projected partial for the stream's
+  // last CTA to merge.  A 16-warp CTA that covers two streams runs the two in
+  // parallel, 8 warps and one end area each.
+  __syncthreads();  // every warp is done with its ring and its partials
+  grid_dep_wait();  // q~, c and the tickets come from the preceding launch
+  // the CTA's streams, from the warps' segment flags (one per lane)
+  const int fl = lane < 2 * nw ? flag_s[lane] : -1;
+  int xlo, xhi;
+  if (nf > 0) {
+    int lo = fl >= 0 ? fl : 0x7fffffff, hi = fl;
 #pragma unroll
-  for (int i = 0; i < 2 * kDecWarps; ++i) {
-    const int x = flag_s[i];
-    if (x >= 0) {
-      xlo = min(xlo, x);
-      xhi = max(xhi, x);
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
     }
+    xlo = lo;
+    xhi = hi;
+  } else {
+    xlo = blockIdx.x * nw;
+    xhi = (int)min((long long)xlo + nw, p.streams) - 1;
   }
+  const int n_tail = (int)(len % kBlock);
+  const int rk = p.k.r, rv = p.v.r, tks = rk | 1, rvp = p.rvp;
   const float* wpa = reinterpret_cast<const float*>(smem + p.wp_off);
-  for (int x = xlo; x <= xhi; ++x) {
-    const long long cslot = (long long)blockIdx.x - block_owner((long long)x * nf, T, W) / kDecWarps;
-    float* out = p.ws + ((size_t)x * p.seg_max + cslot) * (size_t)Gq * ms;
-    for (int i = tid; i < Gq * ms; i += kDecThreads) {
-      const int h = i / ms, e2 = i - h * ms;
-      float M = -INFINITY;
+
+  // One stream x by the group of lnt threads (ltid = rank in the group) that
+  // synchronises on named barrier bar_id, with end area es and barrier ebar.
+  auto end_stream = [&](int x, const EndSmem& es, uint64_t* ebar, uint32_t& epar, int& bv_group, int ltid, int lnt,
+                        int bar_id) {
+    const int lw = ltid >> 5, lnw = lnt >> 5;
+    const int hpt = 8 * kHeadDim / lnt;  // query heads per thread in the projection: 4 or 2
+    const int d = ltid & (kHeadDim - 1), h0 = (ltid >> 7) * hpt;
+    const unsigned int wmask = __ballot_sync(0xffffffffu, fl == x);  // the warp segments of stream x
+    long long c_first = x / nw, c_last = c_first;
+    if (nf > 0) {
+      c_first = block_owner((long long)x * nf, T, W) / nw;
+      c_last = block_owner((long long)x * nf + nf - 1, T, W) / nw;
+    }
+    const int cslot = (int)(blockIdx.x - c_first), nseg = (int)(c_last - c_first + 1);
+    const bool tail_here = n_tail > 0 && blockIdx.x == c_last;
+    const int kh = (int)(x % p.Hkv), bb = (int)(x / p.Hkv);
+    const int gv = kh / p.v.heads_per_group;
+    const bool new_basis = gv != bv_group;
+    const bool copies = new_basis || tail_here;
+    if (ltid == 0 && copies) {
+      // the V basis rows (unless this group's are in place), and for the
+      // tail: q~, c and the value tail (the area was last read through the
+      // generic proxy: order those reads first)
+      fence_proxy_async_smem();
+      const uint32_t bv = new_basis ? (uint32_t)rv * 512u : 0u;
+      const uint32_t tv = p.v.quantize ? (uint32_t)(kBlock * rv * 4) : (uint32_t)p.v.rec_bytes;
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      mbar_arrive_expect_tx(ebar, bv + (tail_here ? 4096u + 32u + tv : 0u));
+      if (new_basis) bulk_g2s(es.bv, p.v.basisT + (size_t)gv * rv * kHeadDim, bv, ebar);
+      if (tail_here) {
+        bulk_g2s(es.qt, p.qt + (size_t)x * 8 * kHeadDim, 4096u, ebar);
+        bulk_g2s(es.cq, p.cq + (size_t)x * 8, 32u, ebar);
+        const void* src = p.v.quantize ? static_cast<const void*>(p.v.tail + (size_t)x * kBlock * rv)
+                                       : static_cast<const void*>(p.v.blocks + ((size_t)x * p.v.n_blk_cap + nf) * p.v.rec_bytes);
+        bulk_g2s(es.tv, src, tv, ebar);
+      }
+    }
+    bv_group = gv;
+    // the key tail [32][rk] (at most 16 words per thread), loaded now, stored
+    // below at an odd row stride
+    float tkv[16];
+    if (tail_here) {
+      const float* src = p.k.tail + (size_t)x * kBlock * rk;
 #pragma unroll
-      for (int k = 0; k < 2 * kDecWarps; ++k)
-        if (flag_s[k] == x) M = fmaxf(M, wpa[((size_t)k * Gq + h) * ms]);
+      for (int u = 0; u < 16; ++u) {
+        const int i = ltid + lnt * u;
+        tkv[u] = i < kBlock * rk ? __ldcg(src + i) : 0.f;
+      }
+    }
+    // per head: the maximum over the stream's warp segments, their weights
+    // (zero for every other slot) and the sum; lane = slot
+    for (int h = lw; h < Gq; h += lnw) {
+      const bool in = (wmask >> lane) & 1u;
+      const float mk = in ? wpa[((size_t)lane * Gq + h) * ms] : -INFINITY;
+      const float lk = in ? wpa[((size_t)lane * Gq + h) * ms + 1] : 0.f;
+      float M = mk;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float wk = mk == -INFINITY ? 0.f : ex2(mk - M);
+      float L = wk * lk;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      es.sw[lane * 8 + h] = wk;
+      if (lane == 0) {
+        es.hm[h] = M;
+        es.hl[h] = L;
+      }
+    }
+    bar_sync(bar_id, lnt);
+    // merged latent per (head, real value channel): every slot, weight 0 for
+    // the ones that are not the stream's
+    for (int i = ltid; i < Gq * rvp; i += lnt) {
+      const int h = i / rvp, pch = i - h * rvp;
+      const int j2 = padded_to_channel(pch, rv, p.v.n_hi, p.v.n_hi_oct, p.v.quantize);
+      if (j2 < 0) continue;
       float v = 0.f;
-      if (e2 == 0) {
-        v = M;
-      } else if (e2 == 1 || e2 >= kPartHead) {
+#pragma unroll 8
+      for (int k = 0; k < 2 * nw; ++k) v = fmaf(es.sw[k * 8 + h], wpa[((size_t)k * Gq + h) * ms + kPartHead + pch], v);
+      es.ol[h * kHeadDim + j2] = v;
+    }
+    if (tail_here) {
 #pragma unroll
-        for (int k = 0; k < 2 * kDecWarps; ++k) {
-          if (flag_s[k] != x) continue;
-          const float mk = wpa[((size_t)k * Gq + h) * ms];
-          if (mk != -INFINITY) v = fmaf(wpa[((size_t)k * Gq + h) * ms + e2], ex2(mk - M), v);
+      for (int u = 0; u < 16; ++u) {
+        const int i = ltid + lnt * u;
+        if (i < kBlock * rk) es.tk[(i / rk) * tks + i % rk] = tkv[u];
+      }
+    }
+    bool got = true;
+    if (copies) {
+      got = mbar_wait_bounded(ebar, epar);
+      epar ^= 1u;
+      if (!got && ltid == 0) set_dev_error(p.k.hdr, PALU_DEVERR_TIMEOUT);
+    }
+    bar_sync(bar_id, lnt);
+    if (tail_here) {
+      // tail scores in log2 units (q~ and c carry the softmax scale): warp
+      // per head, lane t
+      for (int h = lw; h < Gq; h += lnw) {
+        if (lane < n_tail) {
+          const int t = lane;
+          float sc_t = es.cq[h];
+          const float* tkr = es.tk + t * tks;
+          const float* qh = es.qt + h * kHeadDim;
+          for (int j2 = 0; j2 < p.k.n_hi; ++j2) sc_t = fmaf(qh[j2], tkr[j2], sc_t);
+          const float* ql = qh + 8 * p.k.n_hi_oct - p.k.n_hi;
+          for (int j2 = p.k.n_hi; j2 < rk; ++j2) sc_t = fmaf(ql[j2], tkr[j2], sc_t);
+          es.st[h * kBlock + t] = got ? sc_t : -INFINITY;
+        }
+        __syncwarp();
+        const float m_old = es.hm[h];
+        const float st = lane < n_tail ? es.st[h * kBlock + lane] : -INFINITY;
+        float M = fmaxf(m_old, st);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float w_old = m_old == -INFINITY ? 0.f : ex2(m_old - M);
+        const float pt = st == -INFINITY ? 0.f : ex2(st - M);
+        float L = pt;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        __syncwarp();
+        es.st[h * kBlock + lane] = pt;
+        if (lane == 0) {
+          es.hm[h] = M;
+          es.hl[h] = fmaf(w_old, es.hl[h], L);
+          es.wo[h] = w_old;
         }
       }
-      out[i] = v;
+      bar_sync(bar_id, lnt);
+      for (int i = ltid; i < Gq * rv; i += lnt) {
+        const int h = i / rv, j2 = i - h * rv;
+        float a = es.wo[h] * es.ol[h * kHeadDim + j2];
+        for (int t = 0; t < n_tail; ++t) {
+          float lv;
+          if (p.v.quantize) {
+            lv = es.tv[t * rv + j2];
+          } else {
+            // the partial block's fp16 record (fragment order)
+            const int kk = 2 * (t >> 4) + ((t & 15) >> 3);
+            const int ln = 4 * (j2 & 7) + ((t & 7) >> 1);
+            lv = __half2float(*reinterpret_cast<const __half*>(reinterpret_cast<const uint8_t*>(es.tv) +
+                                                               512 * (j2 >> 3) + 16 * ln + 4 * kk + 2 * (t & 1)));
+          }
+          a = fmaf(es.st[h * kBlock + t], lv, a);
+        }
+        es.ol[h * kHeadDim + j2] = a;
+      }
+      bar_sync(bar_id, lnt);
     }
+    // o[h][d] = sum_j latent[h][j] V[d][j]: thread (d, hpt heads)
+    float o4[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      int j2 = 0;
+      for (; j2 + 4 <= rv; j2 += 4) {
+        const float b0 = es.bv[j2 * kHeadDim + d], b1 = es.bv[(j2 + 1) * kHeadDim + d];
+        const float b2 = es.bv[(j2 + 2) * kHeadDim + d], b3 = es.bv[(j2 + 3) * kHeadDim + d];
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+          if (hh < hpt) {
+            const float4 o = *reinterpret_cast<const float4*>(es.ol + (h0 + hh) * kHeadDim + j2);
+            o4[hh] = fmaf(o.x, b0, fmaf(o.y, b1, fmaf(o.z, b2, fmaf(o.w, b3, o4[hh]))));
+          }
+        }
+      }
+      for (; j2 < rv; ++j2) {
+        const float bvj = es.bv[j2 * kHeadDim + d];
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh)
+          if (hh < hpt) o4[hh] = fmaf(es.ol[(h0 + hh) * kHeadDim + j2], bvj, o4[hh]);
+      }
+    }
+    const float mu = __ldg(p.v.mu + (size_t)gv * kHeadDim + d);
+    const long long out0 = ((long long)bb * p.Hq + (long long)kh * Gq) * kHeadDim + d;
+    if (nseg == 1) {
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) {
+        const int h = h0 + hh;
+        if (hh < hpt && h < Gq) store_out(p, out0 + (long long)h * kHeadDim, fmaf(o4[hh], 1.f / es.hl[h], mu));
+      }
+    } else if (cslot < p.seg_max && nseg <= p.seg_max) {
+      float* part = p.ws + ((size_t)x * p.seg_max + cslot) * (size_t)Gq * kOutPart;
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) {
+        const int h = h0 + hh;
+        if (hh < hpt && h < Gq) {
+          part[(size_t)h * kOutPart + kOutHead + d] = o4[hh];
+          if (d == 0) {
+            part[(size_t)h * kOutPart] = es.hm[h];
+            part[(size_t)h * kOutPart + 1] = es.hl[h];
+          }
+        }
+      }
+      bar_sync(bar_id, lnt);  // the group's partial is written
+      if (ltid == 0) {
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");  // release the partial
+        const unsigned int prev = atomicAdd(p.tickets + x, 1u);
+        es.flag[0] = prev + 1 == (unsigned int)nseg ? 1 : 0;
+      }
+      bar_sync(bar_id, lnt);
+      if (es.flag[0]) {
+        // the stream's last CTA: merge the nseg projected partials, online
+        // (running max per head), four partials' loads in flight at a time
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");  // acquire the others' partials
+        const float* pbase = p.ws + (size_t)x * p.seg_max * Gq * kOutPart;
+        float Mh[4], Lh[4], Oh[4];
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+          Mh[hh] = -INFINITY;
+          Lh[hh] = 0.f;
+          Oh[hh] = 0.f;
+        }
+        for (int k0 = 0; k0 < nseg; k0 += 4) {
+          float mv[4][4], lv[4][4], ov[4][4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) {
+              const int h = h0 + hh;
+              const bool ok = k0 + u < nseg && hh < hpt && h < Gq;
+              const float* pk = pbase + ((size_t)(k0 + u) * Gq + h) * kOutPart;
+              mv[u][hh] = ok ? __ldcg(pk) : -INFINITY;
+              lv[u][hh] = ok ? __ldcg(pk + 1) : 0.f;
+              ov[u][hh] = ok ? __ldcg(pk + kOutHead + d) : 0.f;
+            }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) {
+              if (mv[u][hh] == -INFINITY) continue;
+              const float Mn = fmaxf(Mh[hh], mv[u][hh]);
+              const float a = ex2(Mh[hh] - Mn), w = ex2(mv[u][hh] - Mn);
+              Lh[hh] = fmaf(Lh[hh], a, lv[u][hh] * w);
+              Oh[hh] = fmaf(Oh[hh], a, ov[u][hh] * w);
+              Mh[hh] = Mn;
+            }
+        }
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+          const int h = h0 + hh;
+          if (hh < hpt && h < Gq) store_out(p, out0 + (long long)h * kHeadDim, fmaf(Oh[hh], 1.f / Lh[hh], mu));
+        }
+        if (ltid == 0) p.tickets[x] = 0u;
+      }
+    } else if (ltid == 0) {
+      set_dev_error(p.k.hdr, PALU_DEVERR_CAPACITY);
+    }
+    bar_sync(bar_id, lnt);  // the end area is reused by the next stream
+  };
+
+  uint64_t* ebar = bars + nw * ns;  // the end phase's copies (two, for two groups)
+  if (xhi == xlo + 1 && nw == kMaxDecWarps && p.end_off2 >= 0) {
+    // two streams, two groups of 8 warps, two end areas
+    const int half = warp >= nw / 2 ? 1 : 0;
+    const EndSmem es = end_smem(smem + (half ? p.end_off2 : p.end_off), p);
+    uint32_t epar = 0;
+    int bv_group = -1;
+    end_stream(xlo + half, es, ebar + half, epar, bv_group, tid - half * (nt / 2), nt / 2, 1 + half);
+  } else {
+    const EndSmem es = end_smem(smem + p.end_off, p);
+    uint32_t epar = 0;
+    int bv_group = -1;
+    for (int x = xlo; x <= xhi; ++x) end_stream(x, es, ebar, epar, bv_group, tid, nt, 0);
   }
 }
 

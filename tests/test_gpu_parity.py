@@ -215,6 +215,14 @@ def test_decode_multi_block_warps(P, B, Hkv, S):
     run_decode_case(P, B=B, Hkv=Hkv, Gq=3, S=S, rk=30, rv=53, n_groups=2, seed=S, steps=1)
 
 
+# more streams than the decode grid has warps to spare: CTAs that cover whole
+# streams (finished in place), streams split over two CTAs (a ticket picks the
+# one that merges), and contexts with no full block (tails only, several CTAs)
+@pytest.mark.parametrize("B,Hkv,S", [(48, 8, 100), (16, 8, 20), (64, 8, 700)])
+def test_decode_many_streams(P, B, Hkv, S):
+    run_decode_case(P, B=B, Hkv=Hkv, Gq=2, S=S, rk=16, rv=24, n_groups=2, seed=B + S, steps=1)
+
+
 # the fused decode step (append k, append v, attend) against the separate calls
 # on identical caches, and against the oracle; steps cross block boundaries
 @pytest.mark.parametrize("S,rk,rv,quantize_v", [(29, 16, 24, True), (250, 30, 53, True), (95, 32, 32, False),
