@@ -53,7 +53,8 @@ constexpr int kMaxDecWarps = 16;  // warps per decode CTA: 16 (one CTA per SM) o
 constexpr int kMaxDecThreads = 32 * kMaxDecWarps;
 constexpr float kLazyTau = 8.f;   // log2 headroom before the running max is raised
 constexpr int kDecFlagOff = 0;                  // decode CTA shared memory: flags int [2 * warps]
-constexpr int kDecBarOff = 8 * kMaxDecWarps;    // then mbarriers [warps][ns] + 2; the rings follow
+constexpr int kDecInfoOff = 8 * kMaxDecWarps;   // then the first CTA's streams' CTA ranges int [8]
+constexpr int kDecBarOff = kDecInfoOff + 32;    // then mbarriers [warps][ns] + 2; the rings follow
 // A partial (per segment and query head): m, l, two pad words, then the
 // latent accumulator per padded value channel; 16-byte multiple, so one
 // stream's partials move as a single bulk copy.
@@ -351,7 +352,7 @@ __device__ __forceinline__ void value_block(const uint8_t* vr, const GV& gv, int
 // it reuses the rings when they are large enough).  Byte offsets from its
 // 16-byte aligned base, shared by the launch plan and the kernel.
 struct EndLayout {
-  int bv, qt, cq, tk, tv, st, ol, sw, wk, hm, hl, wo, flag, bytes;
+  int bv, qt, cq, tk, tv, st, ol, sw, hm, hl, wo, flag, bytes;
 };
 __host__ __device__ inline EndLayout end_layout(int rk, int rv, int v_quantize, int rec_v) {
   EndLayout e;
@@ -363,8 +364,7 @@ __host__ __device__ inline EndLayout end_layout(int rk, int rv, int v_quantize, 
   e.st = e.tv + (v_quantize ? kBlock * rv * 4 : rec_v);
   e.ol = e.st + 8 * kBlock * 4;               // tail scores, then weights [8][32]
   e.sw = e.ol + 8 * kHeadDim * 4;             // merged latents [8][128]
-  e.wk = e.sw + 32 * 8 * 4;                   // weights of the warp segments [32][8]
-  e.hm = e.wk + 8 * 32 * 4;                   // final merge: partial weights [8][32]
+  e.hm = e.sw + 32 * 8 * 4;                   // weights of the warp segments [32][8]
   e.hl = e.hm + 32;                           // running max, sum, tail rescale [8]
   e.wo = e.hl + 32;
   e.flag = e.wo + 32;
@@ -372,7 +372,7 @@ __host__ __device__ inline EndLayout end_layout(int rk, int rv, int v_quantize, 
   return e;
 }
 struct EndSmem {
-  float *bv, *qt, *cq, *tk, *tv, *st, *ol, *sw, *wk, *hm, *hl, *wo;
+  float *bv, *qt, *cq, *tk, *tv, *st, *ol, *sw, *hm, *hl, *wo;
   int* flag;
 };
 __device__ __forceinline__ EndSmem end_smem(uint8_t* base, const DecodeParams& p) {
@@ -386,7 +386,6 @@ __device__ __forceinline__ EndSmem end_smem(uint8_t* base, const DecodeParams& p
   s.st = reinterpret_cast<float*>(base + e.st);
   s.ol = reinterpret_cast<float*>(base + e.ol);
   s.sw = reinterpret_cast<float*>(base + e.sw);
-  s.wk = reinterpret_cast<float*>(base + e.wk);
   s.hm = reinterpret_cast<float*>(base + e.hm);
   s.hl = reinterpret_cast<float*>(base + e.hl);
   s.wo = reinterpret_cast<float*>(base + e.wo);
@@ -446,9 +445,11 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
   geo_k.init(p.k);
   geo_v.init(p.v);
   const int rec_k = geo_k.rec(), rec_v = geo_v.rec();
+  int* info_s = reinterpret_cast<int*>(smem + kDecInfoOff);  // x0, then (first, last CTA) of x0 and x0 + 1
   if (tid == 32) {
     // warm L2 with what the end phase will copy: the V basis rows of the
-    // CTA's first and last stream, and the tails of a stream ending here
+    // CTA's first and last stream, and the tails of a stream ending here;
+    // and the CTA ranges of the CTA's first two streams, for the end phase
     long long x0 = 0, x1 = -1, b_end = -1;
     if (nf > 0) {
       const long long c0 = min((long long)blockIdx.x * nw, W), c1 = min(c0 + nw, W);
@@ -460,6 +461,17 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
     } else {
       x0 = (long long)blockIdx.x * nw;
       x1 = min(x0 + nw, p.streams) - 1;
+    }
+    info_s[0] = (int)x0;
+    for (int i = 0; i < 2; ++i) {
+      const long long x = x0 + i;
+      long long cf = x / nw, cl = cf;
+      if (nf > 0) {
+        cf = block_owner(x * nf, T, W) / nw;
+        cl = block_owner(x * nf + nf - 1, T, W) / nw;
+      }
+      info_s[1 + 2 * i] = (int)cf;
+      info_s[2 + 2 * i] = (int)cl;
     }
     if (x0 <= x1) {
       const int g0 = (int)(x0 % p.Hkv) / p.v.heads_per_group, g1 = (int)(x1 % p.Hkv) / p.v.heads_per_group;
@@ -475,18 +487,18 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
     }
   }
 
-  // ---- one-time setup: barriers
+  // ---- one-time setup: barriers; the warps' partial slots (two segments
+  // each) start at zero, so that the end phase can weigh every slot, with
+  // weight 0 for the slots of other streams or of no segment
   if (tid == 0) {
     for (int i = 0; i < nw * ns + 2; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
   }
-  __syncthreads();
   const int ms = kPartHead + p.rvp;
   float* wp = reinterpret_cast<float*>(smem + p.wp_off) + (size_t)warp * 2 * Gq * ms;
   if (lane < 2) flag_s[2 * warp + lane] = -1;
-  // the warp partial slots start at zero: the end phase weighs every slot,
-  // with weight 0 for the slots of other streams or of no segment
   for (int i = lane; i < 2 * Gq * ms; i += 32) wp[i] = 0.f;
+  __syncthreads();
 
   uint8_t* wring = ring + (size_t)warp * ns * p.stage_bytes;
   uint64_t* wbar = bars + warp * ns;
@@ -744,11 +756,17 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
     const int lw = ltid >> 5, lnw = lnt >> 5;
     const int hpt = 8 * kHeadDim / lnt;  // query heads per thread in the projection: 4 or 2
     const int d = ltid & (kHeadDim - 1), h0 = (ltid >> 7) * hpt;
-    const unsigned int wmask = __ballot_sync(0xffffffffu, fl == x);  // the warp segments of stream x
-    long long c_first = x / nw, c_last = c_first;
-    if (nf > 0) {
-      c_first = block_owner((long long)x * nf, T, W) / nw;
-      c_last = block_owner((long long)x * nf + nf - 1, T, W) / nw;
+    long long c_first, c_last;
+    const int xi = x - info_s[0];
+    if (xi >= 0 && xi < 2) {
+      c_first = info_s[1 + 2 * xi];
+      c_last = info_s[2 + 2 * xi];
+    } else {
+      c_first = c_last = x / nw;
+      if (nf > 0) {
+        c_first = block_owner((long long)x * nf, T, W) / nw;
+        c_last = block_owner((long long)x * nf + nf - 1, T, W) / nw;
+      }
     }
     const int cslot = (int)(blockIdx.x - c_first), nseg = (int)(c_last - c_first + 1);
     const bool tail_here = n_tail > 0 && blockIdx.x == c_last;
@@ -775,19 +793,22 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
       }
     }
     bv_group = gv;
-    // the key tail [32][rk] (at most 16 words per thread), loaded now, stored
-    // below at an odd row stride
-    float tkv[16];
+    // the key tail [32][rk]: rows lw + lnw v, channels lane + 32 u; loaded
+    // now, stored below at an odd row stride
+    float tkv[4][4];
     if (tail_here) {
       const float* src = p.k.tail + (size_t)x * kBlock * rk;
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int i = ltid + lnt * u;
-        tkv[u] = i < kBlock * rk ? __ldcg(src + i) : 0.f;
-      }
+      for (int v = 0; v < 4; ++v)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int t = lw + lnw * v, j = lane + 32 * u;
+          tkv[v][u] = (t < kBlock && j < rk) ? __ldcg(src + t * rk + j) : 0.f;
+        }
     }
     // per head: the maximum over the stream's warp segments, their weights
     // (zero for every other slot) and the sum; lane = slot
+    const unsigned int wmask = __ballot_sync(0xffffffffu, fl == x);  // the warp segments of stream x
     for (int h = lw; h < Gq; h += lnw) {
       const bool in = (wmask >> lane) & 1u;
       const float mk = in ? wpa[((size_t)lane * Gq + h) * ms] : -INFINITY;
@@ -806,23 +827,28 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
       }
     }
     bar_sync(bar_id, lnt);
-    // merged latent per (head, real value channel): every slot, weight 0 for
-    // the ones that are not the stream's
-    for (int i = ltid; i < Gq * rvp; i += lnt) {
-      const int h = i / rvp, pch = i - h * rvp;
-      const int j2 = padded_to_channel(pch, rv, p.v.n_hi, p.v.n_hi_oct, p.v.quantize);
-      if (j2 < 0) continue;
-      float v = 0.f;
-#pragma unroll 8
-      for (int k = 0; k < 2 * nw; ++k) v = fmaf(es.sw[k * 8 + h], wpa[((size_t)k * Gq + h) * ms + kPartHead + pch], v);
-      es.ol[h * kHeadDim + j2] = v;
+    // merged latent per (head, real value channel), over the covering slots
+    // in slot order (the slots of one stream are those of a run of warps)
+    {
+      const int k_lo = wmask ? __ffs(wmask) - 1 : 0, k_hi = wmask ? 32 - __clz(wmask) : 0;
+      for (int i = ltid; i < Gq * rvp; i += lnt) {
+        const int h = i / rvp, pch = i - h * rvp;
+        const int j2 = padded_to_channel(pch, rv, p.v.n_hi, p.v.n_hi_oct, p.v.quantize);
+        if (j2 < 0) continue;
+        float v = 0.f;
+#pragma unroll 4
+        for (int k = k_lo; k < k_hi; ++k) v = fmaf(es.sw[k * 8 + h], wpa[((size_t)k * Gq + h) * ms + kPartHead + pch], v);
+        es.ol[h * kHeadDim + j2] = v;
+      }
     }
     if (tail_here) {
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int i = ltid + lnt * u;
-        if (i < kBlock * rk) es.tk[(i / rk) * tks + i % rk] = tkv[u];
-      }
+      for (int v = 0; v < 4; ++v)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int t = lw + lnw * v, j = lane + 32 * u;
+          if (t < kBlock && j < rk) es.tk[t * tks + j] = tkv[v][u];
+        }
     }
     bool got = true;
     if (copies) {
@@ -937,7 +963,7 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
       bar_sync(bar_id, lnt);
       if (es.flag[0]) {
         // the stream's last CTA: merge the nseg projected partials, online
-        // (running max per head), four partials' loads in flight at a time
+        // (running max per head), two partials' loads in flight at a time
         asm volatile("fence.acq_rel.gpu;" ::: "memory");  // acquire the others' partials
         const float* pbase = p.ws + (size_t)x * p.seg_max * Gq * kOutPart;
         float Mh[4], Lh[4], Oh[4];
@@ -947,10 +973,11 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
           Lh[hh] = 0.f;
           Oh[hh] = 0.f;
         }
-        for (int k0 = 0; k0 < nseg; k0 += 4) {
-          float mv[4][4], lv[4][4], ov[4][4];
+#pragma unroll 1
+        for (int k0 = 0; k0 < nseg; k0 += 2) {
+          float mv[2][4], lv[2][4], ov[2][4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
+          for (int u = 0; u < 2; ++u)
 #pragma unroll
             for (int hh = 0; hh < 4; ++hh) {
               const int h = h0 + hh;
@@ -961,7 +988,7 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
               ov[u][hh] = ok ? __ldcg(pk + kOutHead + d) : 0.f;
             }
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
+          for (int u = 0; u < 2; ++u)
 #pragma unroll
             for (int hh = 0; hh < 4; ++hh) {
               if (mv[u][hh] == -INFINITY) continue;
@@ -986,19 +1013,15 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
   };
 
   uint64_t* ebar = bars + nw * ns;  // the end phase's copies (two, for two groups)
-  if (xhi == xlo + 1 && nw == kMaxDecWarps && p.end_off2 >= 0) {
-    // two streams, two groups of 8 warps, two end areas
-    const int half = warp >= nw / 2 ? 1 : 0;
-    const EndSmem es = end_smem(smem + (half ? p.end_off2 : p.end_off), p);
-    uint32_t epar = 0;
-    int bv_group = -1;
-    end_stream(xlo + half, es, ebar + half, epar, bv_group, tid - half * (nt / 2), nt / 2, 1 + half);
-  } else {
-    const EndSmem es = end_smem(smem + p.end_off, p);
-    uint32_t epar = 0;
-    int bv_group = -1;
-    for (int x = xlo; x <= xhi; ++x) end_stream(x, es, ebar, epar, bv_group, tid, nt, 0);
-  }
+  // two streams: two groups of 8 warps, each with its own end area and barrier
+  const bool split = xhi == xlo + 1 && nw == kMaxDecWarps && p.end_off2 >= 0;
+  const int half = (split && warp >= nw / 2) ? 1 : 0;
+  const EndSmem es = end_smem(smem + (half ? p.end_off2 : p.end_off), p);
+  uint32_t epar = 0;
+  int bv_group = -1;
+  const int x_first = split ? xlo + half : xlo, x_last = split ? xlo + half : xhi;
+  for (int x = x_first; x <= x_last; ++x)
+    end_stream(x, es, ebar + half, epar, bv_group, tid - half * (nt / 2), split ? nt / 2 : nt, split ? 1 + half : 0);
 }
 
 typedef void (*DecodeKernel)(const DecodeParams);
