@@ -93,50 +93,55 @@ __device__ __forceinline__ AppendSmem append_smem(uint8_t* base, int r, int rec_
   return s;
 }
 
-// Appends one token (x: this stream's D fp16 values) at position p0 of stream
-// (b, h).  Every thread of the CTA calls it; sm.bas must hold the group's
-// basis rows.  Each warp computes whole latent channels: lane l holds
-// x[4l..4l+3] and the matching entries of the basis row, forms exact products
-// and float-pair partial sums, and a butterfly of error-free sums combines
-// the 32 partials; then mu_g . V_g[:, j] (a float pair) is subtracted and the
-// result rounded once to fp32.  Returns, in every thread, the largest fp16
-// scale of the block this token completed (0 if none).
-__device__ __forceinline__ float append_one_token(const CacheView& cv, const __half* __restrict__ x, long long p0, int h, int b,
-                                  int Hkv, const AppendSmem& sm) {
+// Projects one token (x: this stream's D fp16 values) onto the basis rows in
+// sm.bas and stores its fp32 latent in row pos of sm.lat (stride r + 1).
+// Every thread of the CTA calls it.  Eight lanes compute one latent channel:
+// each holds 16 entries of x and of the basis row, forms exact products and
+// float-pair partial sums, and a butterfly of error-free sums combines the 8
+// partials; then mu_g . V_g[:, j] (a float pair) is subtracted and the result
+// rounded once to fp32.
+__device__ __forceinline__ void project_token(const CacheView& cv, const __half* __restrict__ x, int pos, int grp,
+                                              const AppendSmem& sm) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
   const int r = cv.r, ld = r + 1;
-  const int pos = (int)(p0 % kBlock);
-  const long long blk = p0 / kBlock;
-  const int grp = h / cv.heads_per_group;
-  const long long sidx = (long long)b * Hkv + h;
   float* lat = sm.lat;
-  __shared__ float smax;
-  if (tid == 0) smax = 0.f;
-
-  float xv[4];
-  {
-    const uint2 w = *reinterpret_cast<const uint2*>(x + 4 * lane);
+  (void)tid;
+  // 8 lanes per channel, 4 channels per warp and pass: lane (q, i) = (lane / 8,
+  // lane % 8) holds x[d] for d = 32u + 4i + (0..3), u < 4 (conflict-free
+  // 128-bit basis reads: one 8-lane phase covers all 32 banks)
+  const int lq = lane >> 3, li = lane & 7;
+  float xv[16];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const uint2 w = *reinterpret_cast<const uint2*>(x + 32 * u + 4 * li);
     const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
     const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
-    xv[0] = a.x;
-    xv[1] = a.y;
-    xv[2] = c.x;
-    xv[3] = c.y;
+    xv[4 * u] = a.x;
+    xv[4 * u + 1] = a.y;
+    xv[4 * u + 2] = c.x;
+    xv[4 * u + 3] = c.y;
   }
-  for (int j = warp; j < r; j += nwarps) {  // warp-uniform trip count
-    const float4 v = reinterpret_cast<const float4*>(sm.bas + (size_t)j * kHeadDim)[lane];
-    const float vv[4] = {v.x, v.y, v.z, v.w};
+  for (int j0 = 4 * warp; j0 < r; j0 += 4 * nwarps) {  // warp-uniform trip count
+    const int j = j0 + lq;
     float S = 0.f, E = 0.f;
+    if (j < r) {
+      const float* row = sm.bas + (size_t)j * kHeadDim + 4 * li;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float pp, pe, s2, se;
-      two_prod(xv[i], vv[i], pp, pe);
-      two_sum(S, pp, s2, se);
-      S = s2;
-      E = __fadd_rn(E, __fadd_rn(se, pe));
+      for (int u = 0; u < 4; ++u) {
+        const float4 v = *reinterpret_cast<const float4*>(row + 32 * u);
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float pp, pe, s2, se;
+          two_prod(xv[4 * u + e], vv[e], pp, pe);
+          two_sum(S, pp, s2, se);
+          S = s2;
+          E = __fadd_rn(E, __fadd_rn(se, pe));
+        }
+      }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
+    for (int o = 4; o > 0; o >>= 1) {
       const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
       const float E2 = __shfl_xor_sync(0xffffffffu, E, o);
       float s3, err;
@@ -144,13 +149,59 @@ __device__ __forceinline__ float append_one_token(const CacheView& cv, const __h
       S = s3;
       E = __fadd_rn(__fadd_rn(E, E2), err);
     }
-    if (lane == 0) {
+    if (li == 0 && j < r) {
       const float2 m = cv.mv[(size_t)grp * r + j];
       float a, ae;
       two_sum(S, -m.x, a, ae);
       lat[pos * ld + j] = __fadd_rn(a, __fadd_rn(__fsub_rn(E, m.y), ae));
     }
   }
+}
+
+// Largest fp16 scale of the block that token x completes at position
+// kBlock - 1 of stream (b, h), computed exactly as the append will store it
+// (same projection, same quantizer arithmetic), without writing anything to
+// the cache.  sm.bas must hold the group's basis rows.  Every thread calls it
+// and gets the result.
+__device__ __forceinline__ float completed_block_max_scale(const CacheView& cv, const __half* __restrict__ x, int h,
+                                                           int b, int Hkv, const AppendSmem& sm) {
+  const int tid = threadIdx.x, r = cv.r, ld = r + 1;
+  const long long sidx = (long long)b * Hkv + h;
+  __shared__ float smax2;
+  if (tid == 0) smax2 = 0.f;
+  project_token(cv, x, kBlock - 1, h / cv.heads_per_group, sm);
+  const float* tail = cv.tail + sidx * kBlock * r;
+  for (int i = tid; i < (kBlock - 1) * r; i += blockDim.x) sm.lat[(i / r) * ld + (i % r)] = __ldcg(tail + i);
+  __syncthreads();
+  for (int j = tid; j < r; j += blockDim.x) {
+    float mn = sm.lat[j], mx = sm.lat[j];
+    for (int t = 1; t < kBlock; ++t) {
+      mn = fminf(mn, sm.lat[t * ld + j]);
+      mx = fmaxf(mx, sm.lat[t * ld + j]);
+    }
+    const float qmax = j < cv.n_hi ? 15.f : 3.f;
+    const float s32 = __half2float(__float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), qmax)));
+    atomicMax(reinterpret_cast<unsigned int*>(&smax2), __float_as_uint(s32));
+  }
+  __syncthreads();
+  return smax2;
+}
+
+// Appends one token (x: this stream's D fp16 values) at position p0 of stream
+// (b, h).  Every thread of the CTA calls it; sm.bas must hold the group's
+// basis rows.  Returns, in every thread, the largest fp16 scale of the block
+// this token completed (0 if none).
+__device__ __forceinline__ float append_one_token(const CacheView& cv, const __half* __restrict__ x, long long p0, int h, int b,
+                                  int Hkv, const AppendSmem& sm) {
+  const int tid = threadIdx.x;
+  const int r = cv.r, ld = r + 1;
+  const int pos = (int)(p0 % kBlock);
+  const long long blk = p0 / kBlock;
+  const long long sidx = (long long)b * Hkv + h;
+  float* lat = sm.lat;
+  __shared__ float smax;
+  if (tid == 0) smax = 0.f;
+  project_token(cv, x, pos, h / cv.heads_per_group, sm);
   __syncthreads();
 
   if (!cv.quantize) {

@@ -40,8 +40,12 @@ __device__ __forceinline__ QprepSmem qprep_smem(uint8_t* base) {
 }
 
 // Stream X's q-prep by a 256-thread CTA.  max_s_floor: a scale the stream's
-// blocks may hold that the header need not show yet (one this CTA just stored).
-__device__ void qprep_stream(const DecodeParams& p, long long X, float max_s_floor, const QprepSmem& sm) {
+// blocks may hold that the header need not show yet (the largest of a block
+// this step completes).
+// bas_s: the group's key basis rows [r][128] in shared memory, if the caller
+// holds them (else they are read from global memory).
+__device__ void qprep_stream(const DecodeParams& p, long long X, float max_s_floor, const QprepSmem& sm,
+                             const float* bas_s = nullptr) {
   float (*q_s)[kHeadDim] = sm.q_s;
   float* mu_s = sm.mu_s;
   float* B_s = sm.B_s;
@@ -76,8 +80,9 @@ __device__ void qprep_stream(const DecodeParams& p, long long X, float max_s_flo
     for (int u = 0; u < 4; ++u) {
       const int i = tid + 256 * u, r = i >> 5, c4 = i & 31, pch = ch + r;
       const int j = pch < npch ? padded_to_channel(pch, p.k.r, p.k.n_hi, p.k.n_hi_oct, 1) : -1;
-      v[u] = j >= 0 ? __ldg(reinterpret_cast<const float4*>(basis_g + (size_t)j * kHeadDim) + c4)
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[u] = j < 0    ? make_float4(0.f, 0.f, 0.f, 0.f)
+             : bas_s ? reinterpret_cast<const float4*>(bas_s + (size_t)j * kHeadDim)[c4]
+                     : __ldg(reinterpret_cast<const float4*>(basis_g + (size_t)j * kHeadDim) + c4);
     }
     if (ch > 0) __syncthreads();  // the previous chunk's readers are done
 #pragma unroll
@@ -125,6 +130,7 @@ __device__ void qprep_stream(const DecodeParams& p, long long X, float max_s_flo
   for (int i = tid; i < 8 * kHeadDim; i += 256) p.qt[(size_t)X * 8 * kHeadDim + i] = qt_s[i >> 7][i & (kHeadDim - 1)];
   if (tid < 8) p.cq[(size_t)X * 8 + tid] = cq_s[tid];
   if (tid == 0) p.tickets[X] = 0u;
+  if (tid == 0 && X == 0) p.tickets[p.streams] = 0u;
   if (warp == 0) {
     amax = 0.f;
 #pragma unroll
@@ -162,19 +168,23 @@ __global__ void __launch_bounds__(256) latent_qprep_kernel(const DecodeParams p)
 
 // ------------------------------------------------------------------ step prologue
 // One decode step's work before attention (SURVEY "next" row: fused per-step
-// pipeline), in one launch: grid (streams, 2).  CTA (X, 0) appends stream
-// X's new key token and then prepares stream X's query factors (the prescale
-// sees a block this append completed without waiting on other CTAs: only
-// stream X's scales meet stream X's factors); CTA (X, 1) appends the new
-// value token.  Each cache's last appending CTA publishes its new length.
+// pipeline), in one launch: grid (streams, 3).  CTA (X, 0) appends stream
+// X's new key token, CTA (X, 1) the new value token, CTA (X, 2) prepares
+// stream X's query factors; the three run side by side.  The stored lengths
+// stay as they were: the decode launch that follows advances them.
+// Launched as a programmatic dependent: the basis rows, which no launch
+// writes, are fetched before waiting for the preceding launch.  The q-prep
+// recomputes the largest scale of a block this step completes (exactly as
+// the key append stores it) instead of waiting for the append, so the
+// result is the same as that of the separate calls.
 __global__ void __launch_bounds__(256) latent_step_prologue_kernel(const DecodeParams p, const __half* k_new,
                                                                    const __half* v_new) {
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ uint64_t bar;
   const int tid = threadIdx.x;
   const long long X = blockIdx.x;
-  const bool key = blockIdx.y == 0;
-  const CacheView& cv = key ? p.k : p.v;
+  const int role = blockIdx.y;  // 0 key append, 1 value append, 2 q-prep
+  const CacheView& cv = role == 1 ? p.v : p.k;
   const int h = (int)(X % p.Hkv), b = (int)(X / p.Hkv);
   const AppendSmem sm = append_smem(dsm, cv.r, cv.rec_bytes);
   if (tid == 0) {
@@ -183,21 +193,26 @@ __global__ void __launch_bounds__(256) latent_step_prologue_kernel(const DecodeP
     mbar_arrive_expect_tx(&bar, (uint32_t)cv.r * 512u);
     bulk_g2s(sm.bas, cv.basisT + (size_t)(h / cv.heads_per_group) * cv.r * kHeadDim, (uint32_t)cv.r * 512u, &bar);
   }
+  grid_dep_wait();
+  grid_dep_launch();
   const long long p0 = __ldcg(&cv.hdr->length);
   __syncthreads();
   const bool got = mbar_wait_bounded(&bar, 0);
   if (!got && tid == 0) set_dev_error(cv.hdr, PALU_DEVERR_TIMEOUT);
-  float s_new = 0.f;
+  if (role == 2) {
+    // a block this step completes holds scales the header may not show yet:
+    // the q-prep takes them from the same arithmetic the key append runs
+    float s_floor = 0.f;
+    if (p0 + 1 <= cv.capacity && p0 % kBlock == kBlock - 1)
+      s_floor = completed_block_max_scale(cv, k_new + X * kHeadDim, h, b, p.Hkv, sm);
+    __syncthreads();
+    qprep_stream(p, X, s_floor, qprep_smem(dsm + append_smem_bytes(cv.r, cv.rec_bytes)), sm.bas);
+    return;
+  }
   if (p0 + 1 > cv.capacity) {
     if (X == 0 && tid == 0) set_dev_error(cv.hdr, PALU_DEVERR_CAPACITY);
   } else {
-    s_new = append_one_token(cv, (key ? k_new : v_new) + X * kHeadDim, p0, h, b, p.Hkv, sm);
-    __syncthreads();
-    if (tid == 0) publish_length(cv, p0, (unsigned int)p.streams);
-  }
-  if (key) {
-    __syncthreads();  // the append's scratch is free
-    qprep_stream(p, X, s_new, qprep_smem(dsm));
+    append_one_token(cv, (role == 0 ? k_new : v_new) + X * kHeadDim, p0, h, b, p.Hkv, sm);
   }
 }
 
@@ -294,7 +309,7 @@ static palu_status plan_decode(const palu_cache* k, const palu_cache* v, int32_t
   pl->qt_off = align_up(pl->qpack_off + sizeof(uint32_t) * (size_t)streams * 32 * pl->qp_stride, 256);
   pl->cq_off = align_up(pl->qt_off + sizeof(float) * (size_t)streams * 8 * kHeadDim, 256);
   pl->tick_off = align_up(pl->cq_off + sizeof(float) * (size_t)streams * 8, 256);
-  pl->part_off = align_up(pl->tick_off + sizeof(uint32_t) * (size_t)streams, 256);
+  pl->part_off = align_up(pl->tick_off + sizeof(uint32_t) * (size_t)(streams + 1), 256);
   pl->ws_bytes = align_up(pl->part_off + sizeof(float) * (size_t)streams * pl->seg_max * Gq * kOutPart, 256);
   return PALU_OK;
 }
@@ -408,14 +423,26 @@ extern "C" palu_status palu_decode_step(palu_cache* k, palu_cache* v, const void
   DecodeParams p = decode_params(pl, k, v, q, q_heads, softmax_scale, out, out_fp32, workspace);
   p.after_append = 1;
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
-  const size_t smem = std::max({append_smem_bytes(k->rank, k->record_bytes),
-                                append_smem_bytes(v->rank, v->record_bytes), kQprepSmemBytes});
+  const size_t smem = std::max(append_smem_bytes(v->rank, v->record_bytes),
+                               append_smem_bytes(k->rank, k->record_bytes) + kQprepSmemBytes);
   int per_sm = 0;
   st = kernel_occupancy(reinterpret_cast<const void*>(latent_step_prologue_kernel), 256, (int)smem, &per_sm);
   if (st != PALU_OK) return st;
-  latent_step_prologue_kernel<<<dim3((unsigned int)p.streams, 2), 256, smem, strm>>>(p, static_cast<const __half*>(k_new),
-                                                                                 static_cast<const __half*>(v_new));
-  st = cuda_check(cudaGetLastError(), "latent_step_prologue_kernel launch");
+  {
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned int)p.streams, 3);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = strm;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    st = cuda_check(cudaLaunchKernelEx(&cfg, latent_step_prologue_kernel, p, static_cast<const __half*>(k_new),
+                                       static_cast<const __half*>(v_new)),
+                    "latent_step_prologue_kernel launch");
+  }
   if (st != PALU_OK) return st;
   k->length += 1;
   v->length += 1;

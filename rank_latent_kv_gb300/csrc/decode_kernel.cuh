@@ -72,7 +72,7 @@ struct DecodeParams {
   float* qt;          // per stream: scaled q~ [8][128] per padded key channel
   float* cq;          // per stream: scaled q . mu^K [8]
   float* ws;          // projected partials [streams][seg_max][Gq][kOutPart]
-  uint32_t* tickets;  // per stream: CTAs done with the stream (zeroed by the q-prep)
+  uint32_t* tickets;  // per stream: CTAs done with the stream, then CTAs done with the launch (zeroed by the q-prep)
   int out_fp32;
   int Hq, Hkv, Gq;
   int rvp;            // padded value channels = 8 * v.n_oct
@@ -423,15 +423,20 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
   const int nw = blockDim.x >> 5, nt = blockDim.x;  // 16 or 8 warps
-  if (p.after_append) {
-    // the preceding launch wrote the length and maybe a new block
-    grid_dep_wait();
-  }
+  // After a step prologue (one token appended per stream), this launch owns
+  // the length update: the prologue leaves the stored length alone, every
+  // CTA reads it as it was before the step, and the last CTA to finish
+  // stores the new one.  Copies of blocks the prologue did not write may
+  // start before its results are awaited; a block the appended token
+  // completed may not.
+  const long long len0 = __ldcg(&p.k.hdr->length);
+  const bool grows = p.after_append && len0 < p.k.capacity;
+  const long long len = len0 + (grows ? 1 : 0);
+  if (grows && len % kBlock == 0) grid_dep_wait();
   grid_dep_launch();
-  const long long len = __ldcg(&p.k.hdr->length);
   const long long nf = len / kBlock;
   const long long T = p.streams * nf;
-  if (tid == 0 && blockIdx.x == 0 && __ldcg(&p.v.hdr->length) != len)
+  if (tid == 0 && blockIdx.x == 0 && __ldcg(&p.v.hdr->length) != len0)
     set_dev_error(p.k.hdr, PALU_DEVERR_LENGTH_MISMATCH);
   // every warp works on its own: the flat range of full blocks is split over
   // at most T warps, so each warp that takes part owns >= 1 block and the
@@ -1022,6 +1027,22 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
   const int x_first = split ? xlo + half : xlo, x_last = split ? xlo + half : xhi;
   for (int x = x_first; x <= x_last; ++x)
     end_stream(x, es, ebar + half, epar, bv_group, tid - half * (nt / 2), split ? nt / 2 : nt, split ? 1 + half : 0);
+  if (grows) {
+    // the last CTA stores the new length of both caches (every CTA read the
+    // old one at its start, before it counted itself here)
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      const unsigned int prev = atomicAdd(p.tickets + p.streams, 1u);
+      if (prev + 1 == gridDim.x) {
+        __threadfence();
+        p.k.hdr->length = len;
+        p.v.hdr->length = len;
+        p.tickets[p.streams] = 0u;
+        __threadfence();
+      }
+    }
+  }
 }
 
 typedef void (*DecodeKernel)(const DecodeParams);

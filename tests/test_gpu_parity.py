@@ -256,6 +256,36 @@ def test_decode_step_matches_separate_calls(P, S, rk, rv, quantize_v):
     assert err.max() <= ATTN_TOL, f"max rel err {err.max():.3e}"
 
 
+# the step whose key token completes a block whose scales dwarf every scale
+# stored before (small prefill, one very large token): the query prescale of
+# the fused step must already cover that block (no fp16 overflow), with the
+# same result as the separate calls
+def test_decode_step_completing_block_with_large_scales(P):
+    rng = np.random.default_rng(77)
+    B, Hkv, Gq, S = 2, 4, 3, 63
+    xk = (rand_lowrank(rng, B, Hkv, S + 1, n_groups=2).astype(np.float32) * 0.01)
+    xv = (rand_lowrank(rng, B, Hkv, S + 1, n_groups=2).astype(np.float32) * 0.01)
+    xk[:, :, S] = rng.standard_normal((B, Hkv, 128)) * 400.0
+    xk, xv = xk.astype(np.float16), xv.astype(np.float16)
+    cfg = P.palu_config_default(n_head_groups=2, rank=24)
+    ka, va = make_caches(P, cfg, cfg, xk[:, :, :S], xv[:, :, :S], S + 8)
+    kb, vb = make_caches(P, cfg, cfg, xk[:, :, :S], xv[:, :, :S], S + 8)
+    q = torch.from_numpy(rng.standard_normal((B, Hkv * Gq, 128)).astype(np.float16)).to(DEV)
+    k1 = torch.from_numpy(xk[:, :, S:S + 1].copy()).to(DEV)
+    v1 = torch.from_numpy(xv[:, :, S:S + 1].copy()).to(DEV)
+    ka.append(k1)
+    va.append(v1)
+    out_a = P.decode(ka, va, q)
+    out_b = P.decode_step(kb, vb, k1, v1, q)
+    torch.cuda.synchronize()
+    assert kb.sync() == 0 and vb.sync() == 0
+    assert torch.isfinite(out_b).all()
+    assert torch.equal(out_a, out_b)
+    ref = O.attend(q.cpu().numpy(), oracle_view(kb, O.ROLE_KEY), oracle_view(vb, O.ROLE_VALUE))
+    err = O.relative_error(out_b.cpu().numpy(), ref)
+    assert err.max() <= ATTN_TOL, f"max rel err {err.max():.3e}"
+
+
 @pytest.mark.parametrize("S", [1, 5, 31, 32, 33, 64, 95, 1000, 4099])
 def test_decode_lengths(P, S):
     run_decode_case(P, B=1, Hkv=2, Gq=3, S=S, rk=16, rv=24, n_groups=1, seed=S, steps=1)
