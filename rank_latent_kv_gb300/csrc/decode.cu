@@ -22,33 +22,32 @@ namespace palu {
 struct QprepSmem {
   float (*q_s)[kHeadDim];
   float* mu_s;
-  float* B_s;  // [32][129] basis rows, padded rows: conflict-free column reads
   float (*qt_s)[kHeadDim];
   float *red_s, *cq_s;
 };
-constexpr size_t kQprepSmemBytes = sizeof(float) * (8 * kHeadDim + kHeadDim + 32 * 129 + 8 * kHeadDim + 16);
+constexpr size_t kQprepSmemBytes = sizeof(float) * (8 * kHeadDim + kHeadDim + 8 * kHeadDim + 16);
 __device__ __forceinline__ QprepSmem qprep_smem(uint8_t* base) {
   QprepSmem s;
   float* f = reinterpret_cast<float*>(base);
   s.q_s = reinterpret_cast<float(*)[kHeadDim]>(f);
   s.mu_s = f + 8 * kHeadDim;
   s.qt_s = reinterpret_cast<float(*)[kHeadDim]>(f + 9 * kHeadDim);
-  s.B_s = f + 17 * kHeadDim;
-  s.red_s = s.B_s + 32 * 129;
+  s.red_s = f + 17 * kHeadDim;
   s.cq_s = s.red_s + 8;
   return s;
 }
 
 // Stream X's q-prep by a 256-thread CTA.  max_s_floor: a scale the stream's
 // blocks may hold that the header need not show yet (the largest of a block
-// this step completes).
-// bas_s: the group's key basis rows [r][128] in shared memory, if the caller
-// holds them (else they are read from global memory).
+// this step completes).  bas_s: the group's key basis rows [r][128] in shared
+// memory, if the caller holds them (else they are read from global memory).
+// q~ is one pass per 32 padded key channels: 8 lanes per channel, each with
+// 16 entries of the basis row (d = 4i + 32u, conflict-free 128-bit reads)
+// and of every query head, a 3-level butterfly for the 8 heads' sums.
 __device__ void qprep_stream(const DecodeParams& p, long long X, float max_s_floor, const QprepSmem& sm,
                              const float* bas_s = nullptr) {
   float (*q_s)[kHeadDim] = sm.q_s;
   float* mu_s = sm.mu_s;
-  float* B_s = sm.B_s;
   float (*qt_s)[kHeadDim] = sm.qt_s;
   float* red_s = sm.red_s;
   float* cq_s = sm.cq_s;
@@ -57,6 +56,7 @@ __device__ void qprep_stream(const DecodeParams& p, long long X, float max_s_flo
   const int gk = kh / p.k.heads_per_group;
   const int npch = 8 * p.k.n_oct;
   const float* basis_g = p.k.basisT + (size_t)gk * p.k.r * kHeadDim;
+  const float max_s = fmaxf(__uint_as_float(__ldcg(&p.k.hdr->max_scale)), max_s_floor);
   {
     const int h = tid >> 5, d4 = tid & 31;
     float4 qv = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -73,40 +73,40 @@ __device__ void qprep_stream(const DecodeParams& p, long long X, float max_s_flo
     for (int i = tid; i < 8 * kHeadDim; i += 256)
       if ((i & (kHeadDim - 1)) >= npch) qt_s[i >> 7][i & (kHeadDim - 1)] = 0.f;
   }
+  __syncthreads();
   float amax = 0.f;
+  const int jq = tid >> 3, li = tid & 7;
   for (int ch = 0; ch < npch; ch += 32) {
-    float4 v[4];
+    const int pch = ch + jq;
+    const int j = pch < npch ? padded_to_channel(pch, p.k.r, p.k.n_hi, p.k.n_hi_oct, 1) : -1;
+    float acc[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = tid + 256 * u, r = i >> 5, c4 = i & 31, pch = ch + r;
-      const int j = pch < npch ? padded_to_channel(pch, p.k.r, p.k.n_hi, p.k.n_hi_oct, 1) : -1;
-      v[u] = j < 0    ? make_float4(0.f, 0.f, 0.f, 0.f)
-             : bas_s ? reinterpret_cast<const float4*>(bas_s + (size_t)j * kHeadDim)[c4]
-                     : __ldg(reinterpret_cast<const float4*>(basis_g + (size_t)j * kHeadDim) + c4);
-    }
-    if (ch > 0) __syncthreads();  // the previous chunk's readers are done
+    for (int h = 0; h < 8; ++h) acc[h] = 0.f;
+    if (j >= 0) {
+      const float* row = (bas_s ? bas_s : basis_g) + (size_t)j * kHeadDim + 4 * li;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = tid + 256 * u, r = i >> 5, c4 = i & 31;
-      float* dst = B_s + r * 129 + 4 * c4;
-      dst[0] = v[u].x;
-      dst[1] = v[u].y;
-      dst[2] = v[u].z;
-      dst[3] = v[u].w;
+      for (int u = 0; u < 4; ++u) {
+        const float4 v = bas_s ? *reinterpret_cast<const float4*>(row + 32 * u)
+                               : __ldg(reinterpret_cast<const float4*>(row + 32 * u));
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          const float4 q4 = *reinterpret_cast<const float4*>(&q_s[h][4 * li + 32 * u]);
+          acc[h] = fmaf(q4.x, v.x, fmaf(q4.y, v.y, fmaf(q4.z, v.z, fmaf(q4.w, v.w, acc[h]))));
+        }
+      }
     }
-    __syncthreads();
-    const float* br = B_s + lane * 129;
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll 8
-    for (int d4 = 0; d4 < kHeadDim / 4; ++d4) {
-      const float4 q4 = *reinterpret_cast<const float4*>(&q_s[warp][4 * d4]);
-      a0 = fmaf(q4.x, br[4 * d4], fmaf(q4.y, br[4 * d4 + 1], a0));
-      a1 = fmaf(q4.z, br[4 * d4 + 2], fmaf(q4.w, br[4 * d4 + 3], a1));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1)
+#pragma unroll
+      for (int h = 0; h < 8; ++h) acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], o);
+    if (li == 0 && pch < npch) {
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const float qt = h < Gq ? acc[h] * p.scale_log2 : 0.f;
+        qt_s[h][pch] = qt;
+        amax = fmaxf(amax, fabsf(qt));
+      }
     }
-    const int pch = ch + lane;
-    const float qt = (warp < Gq && pch < npch) ? (a0 + a1) * p.scale_log2 : 0.f;
-    if (pch < kHeadDim) qt_s[warp][pch] = qt;
-    amax = fmaxf(amax, fabsf(qt));
   }
   {
     float s = 0.f;
@@ -131,28 +131,29 @@ __device__ void qprep_stream(const DecodeParams& p, long long X, float max_s_flo
   if (tid < 8) p.cq[(size_t)X * 8 + tid] = cq_s[tid];
   if (tid == 0) p.tickets[X] = 0u;
   if (tid == 0 && X == 0) p.tickets[p.streams] = 0u;
-  if (warp == 0) {
-    amax = 0.f;
+  // prescale 2^e with |q~| 2^e max(1, largest stored scale) < 2^14, and the
+  // per-lane fp16 hi/lo factors: thread (lane l, octet o)
+  amax = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) amax = fmaxf(amax, red_s[w]);
-    const float max_s = fmaxf(__uint_as_float(__ldcg(&p.k.hdr->max_scale)), max_s_floor);
-    const float xm = amax * fmaxf(1.f, max_s);
-    int e = 0;
-    if (xm > 0.f) {
-      const int ex = (int)((__float_as_uint(xm) >> 23) & 0xFF) - 126;  // xm < 2^ex
-      e = min(max(14 - ex, -120), 120);
-    }
-    const float two_e = pow2i(e), inv2e = pow2i(-e);
-    const int g = lane >> 2, c = lane & 3, ko = p.qp_ko;
-    uint32_t* qp = p.qpack + ((size_t)X * 32 + lane) * p.qp_stride;
-    for (int o = 0; o < ko; ++o) {
-      const float x0 = 8 * o + 2 * c < kHeadDim ? qt_s[g][8 * o + 2 * c] * two_e : 0.f;
-      const float x1 = 8 * o + 2 * c + 1 < kHeadDim ? qt_s[g][8 * o + 2 * c + 1] * two_e : 0.f;
-      const uint32_t hi = pack_f16x2(x0, x1);
-      const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-      qp[o] = hi;
-      qp[ko + o] = pack_f16x2(x0 - hf.x, x1 - hf.y);
-    }
+  for (int w = 0; w < 8; ++w) amax = fmaxf(amax, red_s[w]);
+  const float xm = amax * fmaxf(1.f, max_s);
+  int e = 0;
+  if (xm > 0.f) {
+    const int ex = (int)((__float_as_uint(xm) >> 23) & 0xFF) - 126;  // xm < 2^ex
+    e = min(max(14 - ex, -120), 120);
+  }
+  const float two_e = pow2i(e), inv2e = pow2i(-e);
+  const int g = lane >> 2, c = lane & 3, ko = p.qp_ko;
+  uint32_t* qp = p.qpack + ((size_t)X * 32 + lane) * p.qp_stride;
+  for (int o = warp; o < ko; o += 8) {
+    const float x0 = 8 * o + 2 * c < kHeadDim ? qt_s[g][8 * o + 2 * c] * two_e : 0.f;
+    const float x1 = 8 * o + 2 * c + 1 < kHeadDim ? qt_s[g][8 * o + 2 * c + 1] * two_e : 0.f;
+    const uint32_t hi = pack_f16x2(x0, x1);
+    const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+    qp[o] = hi;
+    qp[ko + o] = pack_f16x2(x0 - hf.x, x1 - hf.y);
+  }
+  if (warp == 0) {
     qp[2 * ko] = __float_as_uint(cq_s[2 * c] * two_e);
     qp[2 * ko + 1] = __float_as_uint(cq_s[2 * c + 1] * two_e);
     qp[2 * ko + 2] = __float_as_uint(two_e);
