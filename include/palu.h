@@ -220,6 +220,28 @@ palu_status palu_decode_step(palu_cache* k, palu_cache* v, const void* k_new, co
  * captured in a graph together with appends. */
 palu_status palu_cache_truncate(palu_cache* cache, int64_t length, void* stream);
 
+/* Cache save and restore (page 4, "prompt cache": the cache of a prompt
+ * prefix saved and reused by a later request; SURVEY "next" row).  An image
+ * holds a fixed 128-byte header, the cache's state (basis, mean, largest
+ * stored scale), the records of every stream's stored blocks, and the fp32
+ * tail: host memory, plain bytes.
+ * palu_cache_save_size: bytes of the image of `cache` at cache->length (the
+ *   host count; after graph replays call palu_cache_sync first).
+ * palu_cache_save: copies the image into `host` (>= that many bytes),
+ *   asynchronously on `stream` (the header is written at once; the device
+ *   bytes are there when the stream has passed the call; pinned host memory
+ *   makes the copies asynchronous).
+ * palu_cache_restore: copies an image into `cache`, which must have been
+ *   initialised with the same role, rank, head grouping, quantization, batch
+ *   and kv_heads (its basis and mean are replaced by the image's) and a
+ *   capacity of at least the image's length (else PALU_ERR_CAPACITY);
+ *   another kind of image is refused with PALU_ERR_INVALID_ARG.  Sets
+ *   cache->length and the device length, clears the device error word.
+ *   The caller owns both buffers. */
+palu_status palu_cache_save_size(const palu_cache* cache, size_t* bytes);
+palu_status palu_cache_save(const palu_cache* cache, void* host, size_t bytes, void* stream);
+palu_status palu_cache_restore(palu_cache* cache, const void* host, size_t bytes, void* stream);
+
 /* palu_decode_attn without a caller workspace, for callers that cannot
  * allocate device memory while decoding (a plugin whose host application owns
  * every allocation, a serving loop that forbids allocation between steps, a

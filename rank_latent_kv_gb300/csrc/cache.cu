@@ -67,8 +67,13 @@ __host__ __device__ inline EncodeSmem encode_smem(int r, int rec_bytes) {
 }
 
 // grid (blocks touched, kv_heads, batch), 128 threads.
+// Two launches per append (phase 1, then phase 2 on the same stream): phase 1
+// fills every block the tokens reach except a last, partial one; phase 2
+// writes that partial block (the tail) and publishes the new length.  A
+// single launch would race: the CTA completing the old partial block reads
+// the tail rows the CTA of the new partial block overwrites.
 __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const __half* __restrict__ x,
-                                                            long long T, int Hkv) {
+                                                            long long T, int Hkv, int phase) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int r = cv.r;
   const EncodeSmem L = encode_smem(r, cv.rec_bytes);
@@ -90,9 +95,11 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
     return;  // nothing written, length unchanged (no CTA takes a ticket)
   }
 
-  const long long blk = p0 / kBlock + blockIdx.x;
+  // phase 1: block p0 / 32 + blockIdx.x; phase 2: the block holding token p1
+  const long long blk = phase == 2 ? p1 / kBlock : p0 / kBlock + blockIdx.x;
   const long long lo = blk * kBlock;
-  if (lo < p1) {
+  const bool last_partial = blk == p1 / kBlock && p1 % kBlock != 0;
+  if (lo < p1 && last_partial == (phase == 2)) {
     const long long new_lo = lo > p0 ? lo : p0;
     const long long hi = (lo + kBlock < p1) ? lo + kBlock : p1;
     const int off_new = (int)(new_lo - lo);
@@ -262,7 +269,8 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
     }
   }
 
-  // the last CTA to finish publishes the new length
+  // the last CTA of phase 2 to finish publishes the new length
+  if (phase != 2) return;
   __syncthreads();
   if (tid == 0) {
     __threadfence();
@@ -471,11 +479,13 @@ extern "C" palu_status palu_encode_append(palu_cache* cache, const void* x, int6
   st = kernel_occupancy(reinterpret_cast<const void*>(encode_append_kernel), 128, smem, &per_sm);
   if (st != PALU_OK) return st;
   const CacheView cv = make_view(cache);
-  encode_append_kernel<<<dim3((unsigned)nblk, cache->kv_heads, cache->batch), 128, smem,
-                         static_cast<cudaStream_t>(stream)>>>(cv, static_cast<const __half*>(x), tokens,
-                                                              cache->kv_heads);
-  st = cuda_check(cudaGetLastError(), "encode_append_kernel launch");
-  if (st != PALU_OK) return st;
+  for (int phase = 1; phase <= 2; ++phase) {
+    encode_append_kernel<<<dim3(phase == 1 ? (unsigned)nblk : 1u, cache->kv_heads, cache->batch), 128, smem,
+                           static_cast<cudaStream_t>(stream)>>>(cv, static_cast<const __half*>(x), tokens,
+                                                                cache->kv_heads, phase);
+    st = cuda_check(cudaGetLastError(), "encode_append_kernel launch");
+    if (st != PALU_OK) return st;
+  }
   cache->length += tokens;
   return PALU_OK;
 }
@@ -494,6 +504,145 @@ extern "C" palu_status palu_cache_truncate(palu_cache* cache, int64_t length, vo
   st = cuda_check(cudaGetLastError(), "cache_truncate_kernel launch");
   if (st != PALU_OK) return st;
   cache->length = length;
+  return PALU_OK;
+}
+
+// ------------------------------------------------------------------ save / restore
+// A cache image ("prompt cache", page 4: a saved prompt prefix reused by a
+// later request): a fixed header, then the state (basis, mean, header with the
+// largest stored scale), the records of the stream's stored blocks, and the
+// fp32 tail.  Plain bytes in host memory; little-endian as the host.
+namespace palu {
+constexpr uint64_t kImageMagic = 0x50414C55494D4731ull;  // "PALUIMG1"
+struct ImageHeader {
+  uint64_t magic;
+  int32_t role, head_dim, rank, n_hi, n_groups, heads_per_group, quantize, batch, kv_heads, record_bytes;
+  int64_t length, n_blocks, state_bytes, block_bytes, tail_bytes;
+  int32_t pad[10];
+};
+static_assert(sizeof(ImageHeader) == 128, "image header is 128 bytes");
+
+// Records per stream that hold data at `length` tokens: the full blocks, and
+// for unquantized caches the partial block too.
+static int64_t stored_blocks(const palu_cache* c, int64_t length) {
+  return c->quantize ? length / kBlock : (length + kBlock - 1) / kBlock;
+}
+
+static ImageHeader image_header(const palu_cache* c) {
+  ImageHeader h;
+  std::memset(&h, 0, sizeof(h));
+  h.magic = kImageMagic;
+  h.role = c->role;
+  h.head_dim = c->head_dim;
+  h.rank = c->rank;
+  h.n_hi = c->n_hi;
+  h.n_groups = c->n_groups;
+  h.heads_per_group = c->heads_per_group;
+  h.quantize = c->quantize;
+  h.batch = c->batch;
+  h.kv_heads = c->kv_heads;
+  h.record_bytes = c->record_bytes;
+  h.length = c->length;
+  h.n_blocks = stored_blocks(c, c->length);
+  h.state_bytes = (int64_t)state_layout(c->n_groups, c->rank).total;
+  h.block_bytes = (int64_t)c->batch * c->kv_heads * h.n_blocks * c->record_bytes;
+  h.tail_bytes = c->quantize ? (int64_t)sizeof(float) * c->batch * c->kv_heads * kBlock * c->rank : 0;
+  return h;
+}
+
+// After a restore: the image's length, a clear error word and ticket (the
+// largest stored scale comes with the image's state).
+__global__ void cache_restore_header_kernel(StateHeader* hdr, long long length) {
+  hdr->length = length;
+  hdr->err = 0u;
+  hdr->ticket = 0u;
+}
+}  // namespace palu
+
+extern "C" palu_status palu_cache_save_size(const palu_cache* cache, size_t* bytes) {
+  palu_status st = check_cache(cache, "cache");
+  if (st != PALU_OK) return st;
+  if (!bytes) return fail(PALU_ERR_INVALID_ARG, "bytes is NULL");
+  const ImageHeader h = image_header(cache);
+  *bytes = sizeof(ImageHeader) + (size_t)(h.state_bytes + h.block_bytes + h.tail_bytes);
+  return PALU_OK;
+}
+
+extern "C" palu_status palu_cache_save(const palu_cache* cache, void* host, size_t bytes, void* stream) {
+  palu_status st = check_cache(cache, "cache");
+  if (st != PALU_OK) return st;
+  if (!host) return fail(PALU_ERR_INVALID_ARG, "host buffer is NULL");
+  const ImageHeader h = image_header(cache);
+  const size_t need = sizeof(ImageHeader) + (size_t)(h.state_bytes + h.block_bytes + h.tail_bytes);
+  if (bytes < need) return fail(PALU_ERR_INVALID_ARG, "host buffer too small: need " + std::to_string(need) + " bytes");
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  uint8_t* dst = static_cast<uint8_t*>(host);
+  std::memcpy(dst, &h, sizeof(h));
+  dst += sizeof(h);
+  st = cuda_check(cudaMemcpyAsync(dst, cache->state, (size_t)h.state_bytes, cudaMemcpyDeviceToHost, strm),
+                  "cudaMemcpyAsync(state)");
+  if (st != PALU_OK) return st;
+  dst += h.state_bytes;
+  if (h.block_bytes > 0) {
+    // the stored prefix of every stream's records, gathered densely
+    const size_t width = (size_t)h.n_blocks * cache->record_bytes;
+    st = cuda_check(cudaMemcpy2DAsync(dst, width, cache->blocks, (size_t)cache->n_blk_cap * cache->record_bytes, width,
+                                      (size_t)cache->batch * cache->kv_heads, cudaMemcpyDeviceToHost, strm),
+                    "cudaMemcpy2DAsync(blocks)");
+    if (st != PALU_OK) return st;
+    dst += h.block_bytes;
+  }
+  if (h.tail_bytes > 0)
+    st = cuda_check(cudaMemcpyAsync(dst, cache->tail, (size_t)h.tail_bytes, cudaMemcpyDeviceToHost, strm),
+                    "cudaMemcpyAsync(tail)");
+  return st;
+}
+
+extern "C" palu_status palu_cache_restore(palu_cache* cache, const void* host, size_t bytes, void* stream) {
+  palu_status st = check_cache(cache, "cache");
+  if (st != PALU_OK) return st;
+  if (!host || bytes < sizeof(ImageHeader)) return fail(PALU_ERR_INVALID_ARG, "host image is NULL or too short");
+  ImageHeader h;
+  std::memcpy(&h, host, sizeof(h));
+  if (h.magic != kImageMagic) return fail(PALU_ERR_INVALID_ARG, "not a cache image (bad magic)");
+  const ImageHeader mine = image_header(cache);
+  if (h.role != mine.role || h.head_dim != mine.head_dim || h.rank != mine.rank || h.n_hi != mine.n_hi ||
+      h.n_groups != mine.n_groups || h.heads_per_group != mine.heads_per_group || h.quantize != mine.quantize ||
+      h.batch != mine.batch || h.kv_heads != mine.kv_heads || h.record_bytes != mine.record_bytes)
+    return fail(PALU_ERR_INVALID_ARG,
+                "the image was saved from a cache of another role, rank, head grouping, quantization, batch or kv_heads");
+  if (h.length < 0 || h.length > cache->capacity)
+    return fail(PALU_ERR_CAPACITY, "the image holds " + std::to_string(h.length) + " tokens, the cache's capacity is " +
+                                       std::to_string(cache->capacity));
+  if (h.n_blocks != stored_blocks(cache, h.length) || h.state_bytes != mine.state_bytes ||
+      h.block_bytes != (int64_t)cache->batch * cache->kv_heads * h.n_blocks * cache->record_bytes ||
+      h.tail_bytes != mine.tail_bytes)
+    return fail(PALU_ERR_INVALID_ARG, "inconsistent cache image header");
+  const size_t need = sizeof(ImageHeader) + (size_t)(h.state_bytes + h.block_bytes + h.tail_bytes);
+  if (bytes < need) return fail(PALU_ERR_INVALID_ARG, "host image too short: need " + std::to_string(need) + " bytes");
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  const uint8_t* src = static_cast<const uint8_t*>(host) + sizeof(h);
+  st = cuda_check(cudaMemcpyAsync(cache->state, src, (size_t)h.state_bytes, cudaMemcpyHostToDevice, strm),
+                  "cudaMemcpyAsync(state)");
+  if (st != PALU_OK) return st;
+  src += h.state_bytes;
+  if (h.block_bytes > 0) {
+    const size_t width = (size_t)h.n_blocks * cache->record_bytes;
+    st = cuda_check(cudaMemcpy2DAsync(cache->blocks, (size_t)cache->n_blk_cap * cache->record_bytes, src, width, width,
+                                      (size_t)cache->batch * cache->kv_heads, cudaMemcpyHostToDevice, strm),
+                    "cudaMemcpy2DAsync(blocks)");
+    if (st != PALU_OK) return st;
+    src += h.block_bytes;
+  }
+  if (h.tail_bytes > 0) {
+    st = cuda_check(cudaMemcpyAsync(cache->tail, src, (size_t)h.tail_bytes, cudaMemcpyHostToDevice, strm),
+                    "cudaMemcpyAsync(tail)");
+    if (st != PALU_OK) return st;
+  }
+  cache_restore_header_kernel<<<1, 1, 0, strm>>>(reinterpret_cast<StateHeader*>(cache->state), h.length);
+  st = cuda_check(cudaGetLastError(), "cache_restore_header_kernel launch");
+  if (st != PALU_OK) return st;
+  cache->length = h.length;
   return PALU_OK;
 }
 

@@ -72,6 +72,9 @@ _SIGNATURES = {
                                    c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
     "palu_cache_stats": (c_int32, [_P(palu_cache), _P(palu_stats)]),
     "palu_cache_truncate": (c_int32, [_P(palu_cache), c_int64, c_void_p]),
+    "palu_cache_save_size": (c_int32, [_P(palu_cache), _P(c_size_t)]),
+    "palu_cache_save": (c_int32, [_P(palu_cache), c_void_p, c_size_t, c_void_p]),
+    "palu_cache_restore": (c_int32, [_P(palu_cache), c_void_p, c_size_t, c_void_p]),
     "palu_cache_sync": (c_int32, [_P(palu_cache), _P(c_uint32), c_void_p]),
     "palu_fp16_decode_workspace_size": (c_int32, [c_int64, c_int32, c_int64, c_int32, _P(c_size_t)]),
     "palu_fp16_decode_attn": (c_int32, [c_void_p, c_void_p, c_int64, c_int32, c_int64, c_int64, c_void_p, c_int32,
@@ -208,6 +211,22 @@ def palu_cache_truncate(cache, length, stream=None):
     _check(lib().palu_cache_truncate(ctypes.byref(cache), length, _stream(stream)))
 
 
+def palu_cache_save_size(cache) -> int:
+    n = c_size_t()
+    _check(lib().palu_cache_save_size(ctypes.byref(cache), ctypes.byref(n)))
+    return n.value
+
+
+def palu_cache_save(cache, host, stream=None):
+    """Copy the cache image into `host` (a CPU uint8 tensor of >= palu_cache_save_size bytes)."""
+    _check(lib().palu_cache_save(ctypes.byref(cache), c_void_p(host.data_ptr()), host.numel(), _stream(stream)))
+
+
+def palu_cache_restore(cache, host, stream=None):
+    """Copy a cache image (a CPU uint8 tensor) into `cache`."""
+    _check(lib().palu_cache_restore(ctypes.byref(cache), c_void_p(host.data_ptr()), host.numel(), _stream(stream)))
+
+
 def palu_cache_sync(cache, stream=None) -> int:
     """Synchronise and refresh cache.length; raises PaluError if the device error word was set."""
     e = c_uint32()
@@ -262,6 +281,15 @@ class LatentCache:
 
     def truncate(self, length, stream=None):
         palu_cache_truncate(self.c, length, stream)
+
+    def save(self, stream=None):
+        """The cache image in pinned host memory (complete once `stream` has passed the call)."""
+        host = torch.empty(palu_cache_save_size(self.c), dtype=torch.uint8, pin_memory=torch.cuda.is_available())
+        palu_cache_save(self.c, host, stream)
+        return host
+
+    def restore(self, image, stream=None):
+        palu_cache_restore(self.c, image, stream)
 
     def record_array(self):
         """Block records as a host uint8 array [B, Hkv, n_blk_cap, record_bytes]."""

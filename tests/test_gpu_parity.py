@@ -136,6 +136,30 @@ def test_encode_prefill_and_appends_bit_exact(P, rank):
     check_encode(P, vc, O.ROLE_VALUE, chunks_v)
 
 
+# multi-token appends that complete the open partial block and open a new
+# one in the same call (the completing CTA reads the tail rows the new
+# block's tail overwrites: the two must be ordered), over many streams
+def test_encode_appends_crossing_open_blocks(P):
+    rng = np.random.default_rng(123)
+    B, H, S = 8, 8, 20
+    sizes = [5, 40, 27, 70, 3, 33, 61]
+    total = S + sum(sizes)
+    xk = rand_lowrank(rng, B, H, total, n_groups=2)
+    xv = rand_lowrank(rng, B, H, total, n_groups=2)
+    cfg = P.palu_config_default(n_head_groups=2, rank=30)
+    kc, vc = make_caches(P, cfg, cfg, xk[:, :, :S], xv[:, :, :S], total + 8)
+    chunks_k, chunks_v = [xk[:, :, :S]], [xv[:, :, :S]]
+    t = S
+    for n in sizes:
+        kc.append(torch.from_numpy(xk[:, :, t:t + n].copy()).to(DEV))
+        vc.append(torch.from_numpy(xv[:, :, t:t + n].copy()).to(DEV))
+        chunks_k.append(xk[:, :, t:t + n])
+        chunks_v.append(xv[:, :, t:t + n])
+        t += n
+    check_encode(P, kc, O.ROLE_KEY, chunks_k)
+    check_encode(P, vc, O.ROLE_VALUE, chunks_v)
+
+
 @pytest.mark.parametrize("rank", [5, 32, 100])
 def test_encode_fp16_value_latents(P, rank):
     rng = np.random.default_rng(100 + rank)
