@@ -232,6 +232,7 @@ __device__ __forceinline__ float append_one_token(const CacheView& cv, const __h
     const float s32 = __half2float(sh), z32 = __half2float(zh);
     sm.sz[j] = __halves2half2(sh, zh);
     atomicMax(&cv.hdr->max_scale, __float_as_uint(s32));
+    atomicMax(&cv.smax[sidx], __float_as_uint(s32));
     atomicMax(reinterpret_cast<unsigned int*>(&smax), __float_as_uint(s32));
     for (int t = 0; t < kBlock; ++t) {
       float q = 0.f;

@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
           const float s32 = __half2float(sh), z32 = __half2float(zh);
           sz[j] = __halves2half2(sh, zh);
           atomicMax(&cv.hdr->max_scale, __float_as_uint(s32));
+          atomicMax(&cv.smax[(long long)b * Hkv + h], __float_as_uint(s32));
           for (int t = 0; t < kBlock; ++t) {
             float q = 0.f;
             if (s32 != 0.f) {
@@ -392,7 +393,7 @@ extern "C" palu_status palu_cache_size(const palu_config* cfg, int32_t role, int
   const bool quant = cfg->quantize || role == PALU_ROLE_KEY;
   if (block_bytes) *block_bytes = align_up((size_t)batch * kv_heads * n_blk * g.rec_bytes, 256);
   if (tail_bytes) *tail_bytes = quant ? align_up(sizeof(float) * (size_t)batch * kv_heads * kBlock * rank, 256) : 0;
-  if (state_bytes) *state_bytes = state_layout(cfg->n_head_groups, rank).total;
+  if (state_bytes) *state_bytes = state_layout(cfg->n_head_groups, rank, batch * (int64_t)kv_heads).total;
   return PALU_OK;
 }
 
@@ -432,13 +433,16 @@ extern "C" palu_status palu_cache_init(palu_cache* cache, const palu_config* cfg
   c.tail = quant ? static_cast<float*>(tail) : nullptr;
   c.state = state;
   c.length = 0;
-  const StateLayout sl = state_layout(c.n_groups, rank);
+  const StateLayout sl = state_layout(c.n_groups, rank, batch * (int64_t)kv_heads);
   uint8_t* s = static_cast<uint8_t*>(state);
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
   cache_init_kernel<<<dim3(rank, c.n_groups), kHeadDim, 0, strm>>>(
       basis, basis_ld, mu, reinterpret_cast<float*>(s + sl.basis_off), reinterpret_cast<float*>(s + sl.mu_off),
       reinterpret_cast<float2*>(s + sl.mv_off), reinterpret_cast<StateHeader*>(s), rank);
   st = cuda_check(cudaGetLastError(), "cache_init_kernel launch");
+  if (st != PALU_OK) return st;
+  st = cuda_check(cudaMemsetAsync(s + sl.smax_off, 0, sizeof(unsigned int) * (size_t)batch * kv_heads, strm),
+                  "cudaMemsetAsync(largest scales)");
   if (st != PALU_OK) return st;
   *cache = c;
   return PALU_OK;
@@ -544,7 +548,7 @@ static ImageHeader image_header(const palu_cache* c) {
   h.record_bytes = c->record_bytes;
   h.length = c->length;
   h.n_blocks = stored_blocks(c, c->length);
-  h.state_bytes = (int64_t)state_layout(c->n_groups, c->rank).total;
+  h.state_bytes = (int64_t)state_layout(c->n_groups, c->rank, (int64_t)c->batch * c->kv_heads).total;
   h.block_bytes = (int64_t)c->batch * c->kv_heads * h.n_blocks * c->record_bytes;
   h.tail_bytes = c->quantize ? (int64_t)sizeof(float) * c->batch * c->kv_heads * kBlock * c->rank : 0;
   return h;

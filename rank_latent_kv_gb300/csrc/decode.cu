@@ -38,8 +38,8 @@ __device__ __forceinline__ QprepSmem qprep_smem(uint8_t* base) {
 }
 
 // Stream X's q-prep by a 256-thread CTA.  max_s_floor: a scale the stream's
-// blocks may hold that the header need not show yet (the largest of a block
-// this step completes).  bas_s: the group's key basis rows [r][128] in shared
+// blocks may hold that its largest-scale word need not show yet (the largest
+// of a block this step completes).  bas_s: the group's key basis rows [r][128] in shared
 // memory, if the caller holds them (else they are read from global memory).
 // q~ is one pass per 32 padded key channels: 8 lanes per channel, each with
 // 16 entries of the basis row (d = 4i + 32u, conflict-free 128-bit reads)
@@ -56,7 +56,8 @@ __device__ void qprep_stream(const DecodeParams& p, long long X, float max_s_flo
   const int gk = kh / p.k.heads_per_group;
   const int npch = 8 * p.k.n_oct;
   const float* basis_g = p.k.basisT + (size_t)gk * p.k.r * kHeadDim;
-  const float max_s = fmaxf(__uint_as_float(__ldcg(&p.k.hdr->max_scale)), max_s_floor);
+  // the stream's own largest stored scale: no other stream's append moves it
+  const float max_s = fmaxf(__uint_as_float(__ldcg(&p.k.smax[X])), max_s_floor);
   {
     const int h = tid >> 5, d4 = tid & 31;
     float4 qv = make_float4(0.f, 0.f, 0.f, 0.f);

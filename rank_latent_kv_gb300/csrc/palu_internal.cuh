@@ -35,23 +35,25 @@ struct StateHeader {
   long long length;
   unsigned int err;
   unsigned int ticket;
-  unsigned int max_scale;  // bits of the largest fp16 scale stored so far (a non-negative float)
+  unsigned int max_scale;  // bits of the largest fp16 scale stored so far in any stream (a non-negative float)
   unsigned int pad[11];
 };
 static_assert(sizeof(StateHeader) == 64, "state header size");
 
 struct StateLayout {
-  size_t basis_off, mu_off, mv_off, total;
+  size_t basis_off, mu_off, mv_off, smax_off, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline StateLayout state_layout(int n_groups, int rank) {
+// streams = batch * kv_heads: one largest-scale word per stream follows mv.
+inline StateLayout state_layout(int n_groups, int rank, long long streams) {
   StateLayout s;
   s.basis_off = 256;
   s.mu_off = align_up(s.basis_off + sizeof(float) * (size_t)n_groups * rank * kHeadDim, 256);
   s.mv_off = align_up(s.mu_off + sizeof(float) * (size_t)n_groups * kHeadDim, 256);
-  s.total = align_up(s.mv_off + sizeof(float) * 2 * (size_t)n_groups * rank, 256);
+  s.smax_off = align_up(s.mv_off + sizeof(float) * 2 * (size_t)n_groups * rank, 256);
+  s.total = align_up(s.smax_off + sizeof(unsigned int) * (size_t)streams, 256);
   return s;
 }
 
@@ -63,6 +65,7 @@ struct CacheView {
   const float* basisT;   // [n_g][r][D]
   const float* mu;       // [n_g][D]
   const float2* mv;      // [n_g][r]
+  unsigned int* smax;    // [batch * kv_heads] bits of each stream's largest stored fp16 scale
   int64_t n_blk_cap;
   int64_t capacity;
   int r, n_hi, n_hi_oct, n_lo_oct, n_oct, rec_bytes;
@@ -71,7 +74,7 @@ struct CacheView {
 
 inline CacheView make_view(const palu_cache* c) {
   CacheView v;
-  StateLayout s = state_layout(c->n_groups, c->rank);
+  StateLayout s = state_layout(c->n_groups, c->rank, (long long)c->batch * c->kv_heads);
   uint8_t* st = static_cast<uint8_t*>(c->state);
   v.blocks = static_cast<uint8_t*>(c->blocks);
   v.tail = c->tail;
@@ -79,6 +82,7 @@ inline CacheView make_view(const palu_cache* c) {
   v.basisT = reinterpret_cast<const float*>(st + s.basis_off);
   v.mu = reinterpret_cast<const float*>(st + s.mu_off);
   v.mv = reinterpret_cast<const float2*>(st + s.mv_off);
+  v.smax = reinterpret_cast<unsigned int*>(st + s.smax_off);
   v.n_blk_cap = c->n_blk_cap;
   v.capacity = c->capacity;
   v.r = c->rank;
