@@ -123,6 +123,16 @@ def test_fit_workspace_and_validation(palu):
         palu.palu_fit_workspace_size(cfg, 1, 6, 64)
 
 
+def test_cache_image_calls_reject_uninitialised_caches(palu):
+    c = palu.palu_cache()
+    n = ctypes.c_size_t()
+    assert palu.lib().palu_cache_save_size(ctypes.byref(c), ctypes.byref(n)) == 4
+    buf = (ctypes.c_uint8 * 256)()
+    assert palu.lib().palu_cache_save(ctypes.byref(c), buf, 256, None) == 4
+    assert palu.lib().palu_cache_restore(ctypes.byref(c), buf, 256, None) == 4
+    assert "not initialised" in palu.palu_last_error()
+
+
 def test_uninitialised_cache_is_rejected(palu):
     c = palu.palu_cache()
     st = palu.palu_stats()
