@@ -430,3 +430,50 @@ def test_projection_inverts_on_a_full_basis():
     assert np.all(np.abs(L - exact) <= np.abs(exact) * 2.0 ** -24 + 1e-30)
     back = L.astype(np.float64) @ V.astype(np.float64).T + mu
     assert np.max(np.abs(back - x.astype(np.float64))) < 1e-5
+
+
+# ------------------------------------------------------------ small helpers
+
+def test_canonical_sign_hand_cases():
+    """Each column's largest-|.| entry ends positive; among equal magnitudes
+    the lowest row index decides; a zero column is left as it is."""
+    V = np.array([[0.6, -0.5, 0.0],
+                  [-0.8, 0.5, 0.0],
+                  [0.0, -0.7071, 0.0]])
+    W = O.canonical_sign(V)
+    assert np.array_equal(W[:, 0], [-0.6, 0.8, 0.0])
+    assert np.array_equal(W[:, 1], [0.5, -0.5, 0.7071])
+    assert np.array_equal(W[:, 2], [0.0, 0.0, 0.0])
+    tie = np.array([[-0.5], [0.5], [0.1]])           # |-0.5| == |0.5|: row 0 decides
+    assert np.array_equal(O.canonical_sign(tie)[:, 0], [0.5, -0.5, -0.1])
+
+
+def test_subspace_residual_closed_form():
+    """Two lines in the plane at angle t: the residual is |sin t|; a set
+    against itself (any basis of it) is 0; orthogonal sets give sqrt(k)."""
+    for t in (0.0, 0.3, 1.0, math.pi / 2):
+        a = np.array([[1.0], [0.0]])
+        b = np.array([[math.cos(t)], [math.sin(t)]])
+        assert abs(O.subspace_residual(a, b) - abs(math.sin(t))) < 1e-14
+    rng = np.random.default_rng(2)
+    Q, _ = np.linalg.qr(rng.standard_normal((10, 10)))
+    R, _ = np.linalg.qr(rng.standard_normal((3, 3)))
+    assert O.subspace_residual(Q[:, :3], Q[:, :3] @ R) < 1e-13
+    assert abs(O.subspace_residual(Q[:, :3], Q[:, 3:7]) - 2.0) < 1e-13
+
+
+def test_relative_error_hand_case():
+    ref = np.array([[[3.0, 4.0]], [[0.0, 2.0]]])     # norms 5 and 2
+    out = np.array([[[3.5, 4.0]], [[0.0, 1.0]]])
+    assert np.allclose(O.relative_error(out, ref), [[0.1], [0.5]], rtol=0, atol=1e-15)
+
+
+def test_group_rows_brute_force():
+    """Rows of group g are all (batch, head in g, token) vectors, batch-major."""
+    B, H, S, D = 2, 6, 3, 4
+    x = np.arange(B * H * S * D, dtype=np.float64).reshape(B, H, S, D)
+    for n_groups in (1, 2, 3, 6):
+        hg = H // n_groups
+        for g in range(n_groups):
+            want = [x[b, h, s] for b in range(B) for h in range(g * hg, (g + 1) * hg) for s in range(S)]
+            assert np.array_equal(O.group_rows(x, n_groups, g), np.array(want))
