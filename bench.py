@@ -434,6 +434,7 @@ def run_palu(args, w, world, rank, local):
     comp = None
     if not args.no_comparator:
         comp = run_comparator(P, w, s, L, int(round(s_ctx)), dev, world)
+        comp_kivi = run_kivi_comparator(P, w, s, L, int(round(s_ctx)), dev, world)
 
     stats_k, stats_v = kc0.stats(), vc0.stats()
     result = {
@@ -471,6 +472,7 @@ def run_palu(args, w, world, rank, local):
         result["e2e"] = e2e
     if comp is not None:
         result["comparator"] = comp
+        result["comparator_kivi"] = comp_kivi
     return result
 
 
@@ -562,6 +564,28 @@ def run_e2e(P, w, caches, s, L, S, outs, ws, W, K, world, dev, unfused=False):
             "d2h_bytes_per_step": int(out_host.numel() * 2)}
 
 
+def _time_graph(calls, s, steps, world, dev):
+    """Capture calls() in a CUDA graph on stream s; ms per replay (max over ranks)."""
+    with torch.cuda.stream(s):
+        calls()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        calls()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        a.record(s)
+        for _ in range(steps):
+            g.replay()
+        b.record(s)
+    torch.cuda.synchronize()
+    return max_over_ranks(a.elapsed_time(b), world, device=dev) / steps
+
+
 def run_comparator(P, w, s, L, s_ctx, dev, world, steps=20):
     """Uncompressed fp16 split-K decode attention on the same shapes and context."""
     from rank_latent_kv_gb300 import synth
@@ -579,30 +603,47 @@ def run_comparator(P, w, s, L, s_ctx, dev, world, steps=20):
         for k, v in kvs:
             P.palu_fp16_decode_attn(k, v, s_ctx, q, out, ws, stream=s)
 
-    with torch.cuda.stream(s):
-        calls()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        calls()
-    with torch.cuda.stream(s):
-        g.replay()
-        g.replay()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(s):
-        a.record(s)
-        for _ in range(steps):
-            g.replay()
-        b.record(s)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(a.elapsed_time(b), world, device=dev) / steps
+    ms = _time_graph(calls, s, steps, world, dev)
     bytes_step = L * (w.batch * w.hkv * s_ctx * 128 * 2 * 2 + w.batch * w.hq * 128 * 4)
     del kvs
     torch.cuda.empty_cache()
     return {"what": "uncompressed fp16 K/V split-K decode attention, same shapes and context",
             "value": whole_job_rate(world * w.batch * s_ctx * L, ms / 1e3), "unit": UNIT, "ms_per_step": ms,
             "achieved_gbs": bytes_step / (ms / 1e3) / 1e9, "bytes_per_step": bytes_step}
+
+
+def run_kivi_comparator(P, w, s, L, s_ctx, dev, world, steps=20):
+    """KIVI-2bit decode attention (2-bit per-channel keys, per-token values,
+    fp16 window of the tokens after the last 32-token block) on the same
+    shapes and context."""
+    from rank_latent_kv_gb300 import synth
+    caches = []
+    for l in range(L):
+        c = P.KiviCache(w.batch, w.hkv, s_ctx, dev)
+        k = torch.randn(w.batch, w.hkv, s_ctx, 128, dtype=torch.float16, device=dev)
+        v = torch.randn(w.batch, w.hkv, s_ctx, 128, dtype=torch.float16, device=dev)
+        c.append(k, v)
+        del k, v
+        caches.append(c)
+    torch.cuda.synchronize()
+    q, _, _ = synth.decode_inputs(w, 0, 0, device=dev, n_steps=1)
+    q = q[0]
+    out = torch.empty(w.batch, w.hq, 128, dtype=torch.float16, device=dev)
+    ws = torch.empty(P.palu_kivi_decode_workspace_size(caches[0].c, w.hq), dtype=torch.uint8, device=dev)
+
+    def calls():
+        for c in caches:
+            P.palu_kivi_decode_attn(c.c, q, out, ws, stream=s)
+
+    ms = _time_graph(calls, s, steps, world, dev)
+    nblk, win = s_ctx // 32, s_ctx % 32
+    bytes_step = L * (w.batch * w.hkv * (nblk * 3072 + win * 2 * 256) + w.batch * w.hq * 128 * 4)
+    del caches
+    torch.cuda.empty_cache()
+    return {"what": "KIVI-2bit decode attention (codes dequantized in-kernel to fp16 tiles), same shapes and context",
+            "value": whole_job_rate(world * w.batch * s_ctx * L, ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+            "achieved_gbs": bytes_step / (ms / 1e3) / 1e9, "bytes_per_step": bytes_step,
+            "bits_per_element_with_meta": 3.0, "gpu_launches_per_step": 2 * L}
 
 
 # ------------------------------------------------------------------ main

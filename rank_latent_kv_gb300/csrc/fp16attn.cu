@@ -9,14 +9,14 @@
 
 #include <algorithm>
 
-#include "palu_internal.cuh"
+#include "splitk_attend.cuh"
 
 namespace palu {
 
-constexpr int kF16Warps = 4;
-constexpr int kF16Tile = 64;      // tokens per stage (16 per warp)
+constexpr int kF16Warps = kSplitWarps;
+constexpr int kF16Tile = kSplitTile;  // tokens per stage (16 per warp)
 constexpr int kF16Stages = 3;
-constexpr int kF16TileBytes = kF16Tile * kHeadDim * 2;  // 16 KB per tensor
+constexpr int kF16TileBytes = kSplitTileBytes;  // 16 KB per tensor
 
 struct F16Params {
   const __half *k, *v, *q;
@@ -26,27 +26,17 @@ struct F16Params {
   float scale_log2;
 };
 
-__device__ __forceinline__ float ex2f_(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int ch) {
-  return base + row * 256 + ((ch ^ (row & 7)) << 4);
-}
-
 __global__ void __launch_bounds__(32 * kF16Warps) fp16_decode_kernel(const F16Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float merge[kF16Warps][8][2 + kHeadDim];
+  __shared__ float merge[kF16Warps][8][kSplitPartStride];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
   const int chunk = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
-  const int Gq = p.Gq, mstride = 2 + kHeadDim;
+  const int Gq = p.Gq;
   const long long t0 = (long long)chunk * p.tiles_per_chunk * kF16Tile;
   const long long t1 = min(t0 + (long long)p.tiles_per_chunk * kF16Tile, p.seq);
-  float* part = p.ws + (((long long)b * p.Hkv + kh) * p.n_chunks + chunk) * (long long)Gq * mstride;
+  float* part = p.ws + (((long long)b * p.Hkv + kh) * p.n_chunks + chunk) * (long long)Gq * kSplitPartStride;
   if (t0 >= t1) {
-    for (int i = tid; i < Gq * mstride; i += blockDim.x) part[i] = (i % mstride) == 0 ? -INFINITY : 0.f;
+    split_write_empty(Gq, part);
     return;
   }
   const int n_tiles = (int)((t1 - t0 + kF16Tile - 1) / kF16Tile);
@@ -75,31 +65,16 @@ __global__ void __launch_bounds__(32 * kF16Warps) fp16_decode_kernel(const F16Pa
     }
   };
 
-  // q as the B operand (k = d, n = head): reg pair for each 16-wide d step
   uint32_t qb[8][2];
-  {
-    const __half* qh = p.q + ((long long)b * p.Hq + (long long)kh * Gq + g) * kHeadDim;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      if (g < Gq) {
-        qb[ks][0] = *reinterpret_cast<const uint32_t*>(qh + 16 * ks + 2 * c);
-        qb[ks][1] = *reinterpret_cast<const uint32_t*>(qh + 16 * ks + 8 + 2 * c);
-      } else {
-        qb[ks][0] = qb[ks][1] = 0u;
-      }
-    }
-  }
+  split_load_q(qb, p.q + ((long long)b * p.Hq + (long long)kh * Gq + g) * kHeadDim, g < Gq, c);
 
 #pragma unroll
   for (int s = 0; s < kF16Stages - 1; ++s) {
     if (s < n_tiles) load_tile(s, s);
     cp_async_commit();
   }
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  float acc[8][4];
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-  const int mat = lane >> 3, rr = lane & 7;
+  SplitState st;
+  split_init(st);
 
   for (int tile = 0; tile < n_tiles; ++tile) {
     cp_async_wait<kF16Stages - 2>();
@@ -108,115 +83,41 @@ __global__ void __launch_bounds__(32 * kF16Warps) fp16_decode_kernel(const F16Pa
     if (nxt < n_tiles) load_tile(nxt, nxt % kF16Stages);
     cp_async_commit();
     const uint32_t kst = sbase + (tile % kF16Stages) * 2 * kF16TileBytes;
-    const uint32_t vst = kst + kF16TileBytes;
     const int r0 = 16 * warp;  // this warp's 16 tokens of the tile
-    const long long tok0 = t0 + (long long)tile * kF16Tile + r0;
-
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      // A = K rows (tokens x d): matrices (t0-7,d0-7), (t8-15,d0-7), (t0-7,d8-15), (t8-15,d8-15)
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(a0, a1, a2, a3, swz(kst, r0 + rr + ((mat & 1) << 3), 2 * ks + (mat >> 1)));
-      mma_f16(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-    }
-    // mask tokens past the end, scale to base 2
-    const bool v0 = tok0 + g < t1, v1 = tok0 + g + 8 < t1;
-    sc[0] = v0 ? sc[0] * p.scale_log2 : -INFINITY;
-    sc[1] = v0 ? sc[1] * p.scale_log2 : -INFINITY;
-    sc[2] = v1 ? sc[2] * p.scale_log2 : -INFINITY;
-    sc[3] = v1 ? sc[3] * p.scale_log2 : -INFINITY;
-    float bm0 = fmaxf(sc[0], sc[2]), bm1 = fmaxf(sc[1], sc[3]);
-#pragma unroll
-    for (int x = 4; x < 32; x <<= 1) {
-      bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
-      bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
-    }
-    const float mn0 = fmaxf(m_run[0], bm0), mn1 = fmaxf(m_run[1], bm1);
-    if (mn0 != -INFINITY && mn1 != -INFINITY) {
-      const float al0 = ex2f_(m_run[0] - mn0), al1 = ex2f_(m_run[1] - mn1);
-      m_run[0] = mn0;
-      m_run[1] = mn1;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        acc[mt][0] *= al0;
-        acc[mt][1] *= al1;
-        acc[mt][2] *= al0;
-        acc[mt][3] *= al1;
-      }
-      l_run[0] *= al0;
-      l_run[1] *= al1;
-      const float p0 = ex2f_(sc[0] - mn0), p1 = ex2f_(sc[1] - mn1), p2 = ex2f_(sc[2] - mn0), p3 = ex2f_(sc[3] - mn1);
-      l_run[0] += p0 + p2;
-      l_run[1] += p1 + p3;
-      const uint32_t b0 = movmatrix_t(pack_f16x2(p0, p1));
-      const uint32_t b1 = movmatrix_t(pack_f16x2(p2, p3));
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        // A = V^T (d x tokens) from the V rows: matrices (d0-7,t0-7), (d8-15,t0-7), (d0-7,t8-15), (d8-15,t8-15)
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(a0, a1, a2, a3, swz(vst, r0 + rr + ((mat >> 1) << 3), 2 * mt + (mat & 1)));
-        mma_f16(acc[mt], a0, a1, a2, a3, b0, b1);
-      }
-    }
+    split_tile(st, qb, kst, kst + kF16TileBytes, r0, lane, t0 + (long long)tile * kF16Tile + r0, t1, p.scale_log2);
   }
   cp_async_wait<0>();
-#pragma unroll
-  for (int x = 4; x < 32; x <<= 1) {
-    l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], x);
-    l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], x);
-  }
-  if (g == 0) {
-    merge[warp][2 * c][0] = m_run[0];
-    merge[warp][2 * c][1] = l_run[0];
-    merge[warp][2 * c + 1][0] = m_run[1];
-    merge[warp][2 * c + 1][1] = l_run[1];
-  }
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) merge[warp][2 * c + (e & 1)][2 + 16 * mt + g + 8 * (e >> 1)] = acc[mt][e];
-  __syncthreads();
-  for (int i = tid; i < Gq * mstride; i += blockDim.x) {
-    const int h = i / mstride, e = i % mstride;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kF16Warps; ++w) M = fmaxf(M, merge[w][h][0]);
-    float o;
-    if (e == 0) {
-      o = M;
-    } else {
-      o = 0.f;
-#pragma unroll
-      for (int w = 0; w < kF16Warps; ++w)
-        if (merge[w][h][0] != -INFINITY) o += merge[w][h][e] * ex2f_(merge[w][h][0] - M);
-    }
-    part[i] = o;
-  }
+  split_write_partial(st, merge, warp, lane, Gq, part);
 }
 
-__global__ void fp16_combine_kernel(const F16Params p, void* out, int out_fp32) {
+__global__ void split_combine_kernel(const float* ws, int Hq, int Hkv, int n_chunks, void* out, int out_fp32) {
   const int kh = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-  const int Gq = p.Gq, mstride = 2 + kHeadDim;
-  const float* wp = p.ws + ((long long)b * p.Hkv + kh) * p.n_chunks * (long long)Gq * mstride;
+  const int Gq = Hq / Hkv, mstride = kSplitPartStride;
+  const float* wp = ws + ((long long)b * Hkv + kh) * n_chunks * (long long)Gq * mstride;
   for (int h = 0; h < Gq; ++h) {
     float M = -INFINITY;
-    for (int ch = 0; ch < p.n_chunks; ++ch) M = fmaxf(M, wp[((long long)ch * Gq + h) * mstride]);
+    for (int ch = 0; ch < n_chunks; ++ch) M = fmaxf(M, wp[((long long)ch * Gq + h) * mstride]);
     float L = 0.f, a = 0.f;
-    for (int ch = 0; ch < p.n_chunks; ++ch) {
+    for (int ch = 0; ch < n_chunks; ++ch) {
       const float m = wp[((long long)ch * Gq + h) * mstride];
       if (m == -INFINITY) continue;
       const float w = ex2f_(m - M);
       L += wp[((long long)ch * Gq + h) * mstride + 1] * w;
       a += wp[((long long)ch * Gq + h) * mstride + 2 + d] * w;
     }
-    const long long oi = ((long long)b * p.Hq + (long long)kh * Gq + h) * kHeadDim + d;
+    const long long oi = ((long long)b * Hq + (long long)kh * Gq + h) * kHeadDim + d;
     const float o = a / L;
     if (out_fp32)
       static_cast<float*>(out)[oi] = o;
     else
       static_cast<__half*>(out)[oi] = __float2half_rn(o);
   }
+}
+
+palu_status split_combine(const float* ws, long long batch, int Hq, int Hkv, int n_chunks, void* out, int out_fp32,
+                          cudaStream_t stream) {
+  split_combine_kernel<<<dim3(Hkv, (unsigned)batch), kHeadDim, 0, stream>>>(ws, Hq, Hkv, n_chunks, out, out_fp32);
+  return cuda_check(cudaGetLastError(), "split_combine_kernel launch");
 }
 
 static int f16_chunks(int64_t batch, int32_t kv_heads, int64_t seq_cap, int* tiles_per_chunk) {
@@ -278,6 +179,5 @@ extern "C" palu_status palu_fp16_decode_attn(const void* k, const void* v, int64
   fp16_decode_kernel<<<dim3(p.n_chunks, kv_heads, (unsigned)batch), 32 * kF16Warps, smem, strm>>>(p);
   st = cuda_check(cudaGetLastError(), "fp16_decode_kernel launch");
   if (st != PALU_OK) return st;
-  fp16_combine_kernel<<<dim3(kv_heads, (unsigned)batch), kHeadDim, 0, strm>>>(p, out, out_fp32);
-  return cuda_check(cudaGetLastError(), "fp16_combine_kernel launch");
+  return split_combine(p.ws, batch, q_heads, kv_heads, p.n_chunks, out, out_fp32, strm);
 }

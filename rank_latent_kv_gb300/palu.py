@@ -1,4 +1,4 @@
-"""Thin ctypes binding of libpalu (include/palu.h).
+"""Thin ctypes binding of libpalu (include/palu.h, include/kivi.h).
 
 Argument marshalling only: every step of the fit, append and decode runs in
 the library's CUDA kernels.  PyTorch provides device memory and the current
@@ -50,6 +50,12 @@ class palu_stats(ctypes.Structure):
                 ("bits_with_meta", c_double)]
 
 
+class palu_kivi_cache(ctypes.Structure):
+    _fields_ = [("magic", c_int32), ("batch", c_int32), ("kv_heads", c_int32), ("bits", c_int32),
+                ("capacity", c_int64), ("n_blk_cap", c_int64), ("records", c_void_p), ("window", c_void_p),
+                ("length", c_int64)]
+
+
 _P = POINTER
 _SIGNATURES = {
     "palu_last_error": (ctypes.c_char_p, []),
@@ -79,6 +85,12 @@ _SIGNATURES = {
     "palu_fp16_decode_workspace_size": (c_int32, [c_int64, c_int32, c_int64, c_int32, _P(c_size_t)]),
     "palu_fp16_decode_attn": (c_int32, [c_void_p, c_void_p, c_int64, c_int32, c_int64, c_int64, c_void_p, c_int32,
                                         c_float, c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
+    "palu_kivi_cache_size": (c_int32, [c_int64, c_int32, c_int64, _P(c_size_t), _P(c_size_t)]),
+    "palu_kivi_cache_init": (c_int32, [_P(palu_kivi_cache), c_int64, c_int32, c_int64, c_void_p, c_void_p]),
+    "palu_kivi_append": (c_int32, [_P(palu_kivi_cache), c_void_p, c_void_p, c_int64, c_void_p]),
+    "palu_kivi_decode_workspace_size": (c_int32, [_P(palu_kivi_cache), c_int32, _P(c_size_t)]),
+    "palu_kivi_decode_attn": (c_int32, [_P(palu_kivi_cache), c_void_p, c_int32, c_float, c_void_p, c_int32,
+                                        c_void_p, c_size_t, c_void_p]),
 }
 
 _lib = None
@@ -247,6 +259,35 @@ def palu_fp16_decode_attn(k, v, seq, q, out, workspace, softmax_scale=0.0, strea
                                        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
+def palu_kivi_cache_size(batch, kv_heads, capacity):
+    r, w = c_size_t(), c_size_t()
+    _check(lib().palu_kivi_cache_size(batch, kv_heads, capacity, ctypes.byref(r), ctypes.byref(w)))
+    return r.value, w.value
+
+
+def palu_kivi_cache_init(batch, kv_heads, capacity, records, window) -> palu_kivi_cache:
+    c = palu_kivi_cache()
+    _check(lib().palu_kivi_cache_init(ctypes.byref(c), batch, kv_heads, capacity, _ptr(records), _ptr(window)))
+    return c
+
+
+def palu_kivi_append(cache: palu_kivi_cache, k, v, tokens=None, stream=None):
+    n = k.shape[2] if tokens is None else tokens
+    _check(lib().palu_kivi_append(ctypes.byref(cache), _ptr(k), _ptr(v), n, _stream(stream)))
+
+
+def palu_kivi_decode_workspace_size(cache: palu_kivi_cache, q_heads: int) -> int:
+    n = c_size_t()
+    _check(lib().palu_kivi_decode_workspace_size(ctypes.byref(cache), q_heads, ctypes.byref(n)))
+    return n.value
+
+
+def palu_kivi_decode_attn(cache: palu_kivi_cache, q, out, workspace, softmax_scale=0.0, stream=None):
+    _check(lib().palu_kivi_decode_attn(ctypes.byref(cache), _ptr(q), q.shape[1], softmax_scale, _ptr(out),
+                                       1 if out.dtype == torch.float32 else 0, _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
 # ------------------------------------------------------------------ buffer helpers
 
 def _dev_bytes(n, device):
@@ -314,6 +355,43 @@ class LatentCache:
         bT = st[basis_off:basis_off + 4 * ng * r * 128].view("float32").reshape(ng, r, 128)
         mu = st[mu_off:mu_off + 4 * ng * 128].view("float32").reshape(ng, 128)
         return bT.transpose(0, 2, 1).copy(), mu.copy()
+
+
+class KiviCache:
+    """A KIVI-2bit cache of one layer (keys and values) with torch-allocated buffers."""
+
+    def __init__(self, batch, kv_heads, capacity, device):
+        rec, win = palu_kivi_cache_size(batch, kv_heads, capacity)
+        self.records = _dev_bytes(rec, device)
+        self.window = _dev_bytes(win, device)
+        self.c = palu_kivi_cache_init(batch, kv_heads, capacity, self.records, self.window)
+
+    @property
+    def length(self):
+        return self.c.length
+
+    def append(self, k, v, stream=None):
+        palu_kivi_append(self.c, k, v, k.shape[2], stream)
+
+    def decode(self, q, out_dtype=torch.float32, softmax_scale=0.0, stream=None, workspace=None, out=None):
+        if workspace is None:
+            workspace = _dev_bytes(palu_kivi_decode_workspace_size(self.c, q.shape[1]), q.device)
+        if out is None:
+            out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+        palu_kivi_decode_attn(self.c, q, out, workspace, softmax_scale, stream)
+        return out
+
+    def record_array(self):
+        """Block records as a host uint8 array [B, Hkv, n_blk_cap, 3072]."""
+        c = self.c
+        n = c.batch * c.kv_heads * c.n_blk_cap * 3072
+        return self.records[:n].cpu().numpy().reshape(c.batch, c.kv_heads, c.n_blk_cap, 3072)
+
+    def window_array(self):
+        """The window as host fp16 [B, Hkv, 2 (keys, values), 32, 128]."""
+        c = self.c
+        n = c.batch * c.kv_heads * 2 * 32 * 128 * 2
+        return self.window[:n].cpu().numpy().view("float16").reshape(c.batch, c.kv_heads, 2, 32, 128)
 
 
 def fit(cfg, x, stream=None):

@@ -1,4 +1,4 @@
-"""The C-ABI library loads, exports every symbol declared in include/palu.h,
+"""The C-ABI library loads, exports every symbol declared in include/*.h,
 its structs match the binding's, and host-side validation works (no GPU)."""
 import ctypes
 import os
@@ -11,6 +11,7 @@ import pytest
 from tests.conftest import ROOT
 
 HEADER = os.path.join(ROOT, "include", "palu.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
 
 
 @pytest.fixture(scope="session")
@@ -24,7 +25,7 @@ def palu():
 
 
 def declared_functions():
-    src = open(HEADER).read()
+    src = "".join(open(h).read() for h in HEADERS)
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(palu_[a-z0-9_]+)\s*\(", src)))
 
@@ -143,3 +144,64 @@ def test_uninitialised_cache_is_rejected(palu):
 def test_fp16_comparator_validation(palu):
     with pytest.raises(palu.PaluError):
         palu.palu_fp16_decode_workspace_size(1, 4, 128, 40)   # 10 query heads per KV head
+
+
+def test_kivi_struct_layout_and_sizes(palu):
+    prog = r'''
+#include <stdio.h>
+#include <stddef.h>
+#include "kivi.h"
+int main(void) {
+  printf("%zu %zu %zu %zu\n", sizeof(palu_kivi_cache), offsetof(palu_kivi_cache, capacity),
+         offsetof(palu_kivi_cache, records), offsetof(palu_kivi_cache, length));
+  return 0;
+}'''
+    with tempfile.TemporaryDirectory() as d:
+        src = os.path.join(d, "t.c")
+        exe = os.path.join(d, "t")
+        open(src, "w").write(prog)
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), src, "-o", exe], check=True)
+        vals = list(map(int, subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()))
+    K = palu.palu_kivi_cache
+    assert vals == [ctypes.sizeof(K), K.capacity.offset, K.records.offset, K.length.offset]
+    from oracle import kivi_oracle
+    # records: one 3072-byte record per complete block; window: 2 x 32 x 128 fp16 per stream
+    rec, win = palu.palu_kivi_cache_size(3, 4, 32 * 10 + 17)
+    assert rec == -(-(12 * 10 * kivi_oracle.RECORD) // 256) * 256 and win == 12 * 2 * 32 * 128 * 2
+
+
+def test_kivi_host_validation(palu):
+    """Errors the host detects without launching anything (fake, aligned device addresses)."""
+    c = palu.palu_kivi_cache()
+    with pytest.raises(palu.PaluError) as e:
+        palu._check(palu.lib().palu_kivi_append(ctypes.byref(c), ctypes.c_void_p(256), ctypes.c_void_p(256), 1, None))
+    assert e.value.status == 4  # not initialised
+    c = palu.palu_kivi_cache_init(2, 2, 100, torch_like(1 << 20), torch_like(1 << 21))
+    assert (c.length, c.n_blk_cap, c.bits) == (0, 3, 2)
+    with pytest.raises(palu.PaluError) as e:
+        palu._check(palu.lib().palu_kivi_append(ctypes.byref(c), ctypes.c_void_p(256), ctypes.c_void_p(256), 101,
+                                                None))
+    assert e.value.status == 3  # capacity
+    with pytest.raises(palu.PaluError) as e:
+        palu._check(palu.lib().palu_kivi_append(ctypes.byref(c), ctypes.c_void_p(8), ctypes.c_void_p(256), 1, None))
+    assert e.value.status == 1  # misaligned
+    assert palu.lib().palu_kivi_append(ctypes.byref(c), ctypes.c_void_p(256), ctypes.c_void_p(256), 0, None) == 0
+    n = ctypes.c_size_t()
+    assert palu.lib().palu_kivi_decode_workspace_size(ctypes.byref(c), 3, ctypes.byref(n)) == 1   # 3 % 2
+    assert palu.lib().palu_kivi_decode_workspace_size(ctypes.byref(c), 18, ctypes.byref(n)) == 2  # 9 per KV head
+    # decoding an empty cache
+    assert palu.lib().palu_kivi_decode_attn(ctypes.byref(c), ctypes.c_void_p(256), 2, 0.0, ctypes.c_void_p(256), 1,
+                                            ctypes.c_void_p(256), 1 << 20, None) == 1
+    for bad in ((0, 2, 10), (1, 0, 10), (1, 2, 0)):
+        with pytest.raises(palu.PaluError):
+            palu.palu_kivi_cache_size(*bad)
+
+
+class torch_like:
+    """An object with a data_ptr() for the binding's pointer marshalling (never dereferenced)."""
+
+    def __init__(self, addr):
+        self.addr = addr
+
+    def data_ptr(self):
+        return self.addr
