@@ -157,9 +157,11 @@ __device__ __forceinline__ uint4 dequant8(uint32_t cw, const uint4& s, const uin
   return o;
 }
 
-__global__ void __launch_bounds__(32 * kSplitWarps) kivi_decode_kernel(const KiviDecodeParams p) {
+static_assert(sizeof(float) * kSplitWarps * 8 * kSplitPartStride <= kKiviStages * kKiviStageBytes,
+              "the warp merge area fits in the stage buffers");
+
+__global__ void __launch_bounds__(32 * kSplitWarps, 4) kivi_decode_kernel(const KiviDecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float merge[kSplitWarps][8][kSplitPartStride];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
   const int chunk = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
   const int Gq = p.Gq;
@@ -246,7 +248,10 @@ __global__ void __launch_bounds__(32 * kSplitWarps) kivi_decode_kernel(const Kiv
     split_tile(st, qb, kt, vt, r0, lane, t0 + (long long)tile * kSplitTile + r0, t1, p.scale_log2);
   }
   cp_async_wait<0>();
-  split_write_partial(st, merge, warp, lane, Gq, part);
+  // every stage was consumed in the loop (no copy is in flight) and the last
+  // tile's dequantization ended before the barrier above: the stage buffers
+  // are free for the warps' merge
+  split_write_partial(st, reinterpret_cast<float (*)[8][kSplitPartStride]>(smem), warp, lane, Gq, part);
 }
 
 static palu_status kivi_chunks(long long batch, int kv_heads, long long seq, int* n_chunks, int* tiles_per_chunk) {
