@@ -181,10 +181,11 @@ def decode_source_sha():
     return h.hexdigest()
 
 
-def traffic_record():
-    """DRAM bytes per decode-kernel launch from the committed ncu summary, if
-    it was taken on the current decode sources (null otherwise)."""
-    path = os.path.join(ROOT, "profiles", "latent_decode_qwen7b.md")
+def traffic_record(workload):
+    """DRAM bytes per decode-kernel launch from the committed ncu summary of
+    this workload, if there is one and it was taken on the current decode
+    sources (null otherwise)."""
+    path = os.path.join(ROOT, "profiles", f"latent_decode_{workload}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
@@ -458,7 +459,7 @@ def run_palu(args, w, world, rank, local):
         "roofline": {"bound": "hbm",
                      "kernel": "palu_decode_attn (q-prep + split decode with in-kernel merge), graph of all layers",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "traffic": traffic_record(),
+                     "peak_kind": peak_kind, "traffic": traffic_record(w.name),
                      "algorithmic_bytes_per_launch": bytes_launch, "avg_launch_us": avg_launch * 1e3,
                      "launches_timed": n_launch},
         "clocks": clk.summary(),

@@ -278,10 +278,12 @@ static palu_status plan_decode(const palu_cache* k, const palu_cache* v, int32_t
   const int sms = device_sm_count();
   // the end phase reuses the rings when they are large enough
   const EndLayout el = end_layout(k->rank, v->rank, v->quantize, rec_v);
-  // 16 warps in one CTA per SM when the rings fit (every warp of an SM then
-  // has the same scheduling age, and their ranges end together), else 8
+  // one CTA per SM with as many warps as the kernel's registers allow (16
+  // for the exact-octet kernels, 12 for the per-class ones) when the rings
+  // fit: every warp of an SM then has the same scheduling age, and their
+  // ranges end together; else 8
   const bool exact = k->n_oct <= 8 && v->n_oct <= 8;
-  for (int nw = exact ? kMaxDecWarps : kMaxDecWarps / 2; nw >= 8; nw /= 2) {
+  for (int nw = exact ? kMaxDecWarps : kClassDecWarps; nw >= 8; nw = nw > 8 ? 8 : 0) {
     pl->nw = nw;
     pl->ring_off = (int)align_up(kDecBarOff + 8 * (nw * pl->ns + 2), 128);
     const size_t rings = (size_t)nw * pl->ns * pl->stage_bytes;

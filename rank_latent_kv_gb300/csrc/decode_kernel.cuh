@@ -51,6 +51,10 @@ namespace palu {
 constexpr int kMaxDecWarps = 16;  // warps per decode CTA: 16 (one CTA per SM) or 8; the class
                                   // kernels (large ranks, many registers) always run 8
 constexpr int kMaxDecThreads = 32 * kMaxDecWarps;
+// the per-class kernels: up to 12 warps (at most 168 registers a thread), or
+// 8 when their rings do not fit
+constexpr int kClassDecWarps = 12;
+constexpr int kClassDecThreads = 32 * kClassDecWarps;
 constexpr float kLazyTau = 8.f;   // log2 headroom before the running max is raised
 constexpr int kDecFlagOff = 0;                  // decode CTA shared memory: flags int [2 * warps]
 constexpr int kDecInfoOff = 8 * kMaxDecWarps;   // then the first CTA's streams' CTA ranges int [8]
@@ -411,7 +415,7 @@ __device__ __forceinline__ long long block_owner(long long i, long long T, long 
 // kernel (programmatic dependent launch: the first copies are in flight
 // before the packed query factors are read).
 template <int KC, int VC, bool VQ, int KE, int VE>
-__global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 1)
+__global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kClassDecThreads, 1)
     latent_decode_kernel(const DecodeParams p) {
   using GK = Geom<KC, KE, true>;
   using GV = Geom<VC, VE, VQ>;
@@ -422,7 +426,7 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
   uint8_t* ring = smem + p.ring_off;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
-  const int nw = blockDim.x >> 5, nt = blockDim.x;  // 16 or 8 warps
+  const int nw = blockDim.x >> 5, nt = blockDim.x;  // 16, 12 or 8 warps
   // After a step prologue (one token appended per stream), this launch owns
   // the length update: the prologue leaves the stored length alone, every
   // CTA reads it as it was before the step, and the last CTA to finish
@@ -759,7 +763,7 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
   auto end_stream = [&](int x, const EndSmem& es, uint64_t* ebar, uint32_t& epar, int& bv_group, int ltid, int lnt,
                         int bar_id) {
     const int lw = ltid >> 5, lnw = lnt >> 5;
-    const int hpt = 8 * kHeadDim / lnt;  // query heads per thread in the projection: 4 or 2
+    const int hpt = (8 * kHeadDim + lnt - 1) / lnt;  // query heads per thread in the projection: 4, 3 or 2
     const int d = ltid & (kHeadDim - 1), h0 = (ltid >> 7) * hpt;
     long long c_first, c_last;
     const int xi = x - info_s[0];
@@ -925,7 +929,7 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
         const float b2 = es.bv[(j2 + 2) * kHeadDim + d], b3 = es.bv[(j2 + 3) * kHeadDim + d];
 #pragma unroll
         for (int hh = 0; hh < 4; ++hh) {
-          if (hh < hpt) {
+          if (hh < hpt && h0 + hh < Gq) {
             const float4 o = *reinterpret_cast<const float4*>(es.ol + (h0 + hh) * kHeadDim + j2);
             o4[hh] = fmaf(o.x, b0, fmaf(o.y, b1, fmaf(o.z, b2, fmaf(o.w, b3, o4[hh]))));
           }
@@ -935,7 +939,7 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kMaxDecThreads / 2, 
         const float bvj = es.bv[j2 * kHeadDim + d];
 #pragma unroll
         for (int hh = 0; hh < 4; ++hh)
-          if (hh < hpt) o4[hh] = fmaf(es.ol[(h0 + hh) * kHeadDim + j2], bvj, o4[hh]);
+          if (hh < hpt && h0 + hh < Gq) o4[hh] = fmaf(es.ol[(h0 + hh) * kHeadDim + j2], bvj, o4[hh]);
       }
     }
     const float mu = __ldg(p.v.mu + (size_t)gv * kHeadDim + d);

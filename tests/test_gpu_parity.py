@@ -216,6 +216,15 @@ def test_decode_ranks(P, rk, rv):
     run_decode_case(P, B=1, Hkv=4, Gq=3, S=257, rk=rk, rv=rv, seed=rk + rv)
 
 
+# the per-class kernels (more than 8 octets on a side; 12-warp CTAs when the
+# rings fit) with 7 and 8 query heads per KV head, on streams that one CTA
+# finishes and on streams split over several CTAs and merged by the last one
+@pytest.mark.parametrize("Gq", [7, 8])
+@pytest.mark.parametrize("B,Hkv,S,rk,rv", [(8, 8, 300, 74, 100), (1, 2, 20011, 74, 74), (2, 2, 5000, 128, 128)])
+def test_decode_class_kernels_wide_gqa(P, Gq, B, Hkv, S, rk, rv):
+    run_decode_case(P, B=B, Hkv=Hkv, Gq=Gq, S=S, rk=rk, rv=rv, n_groups=2, seed=Gq + S, steps=1)
+
+
 def _rank_for_octets(n):
     """Smallest rank whose mixed-bit record has n octets (oracle layout)."""
     for r in range(1, 129):
