@@ -20,7 +20,9 @@
 //   2. reduce_kernel: chunk partials summed in fp64, centred in fp64.
 //   3. jacobi_kernel: one CTA per group diagonalises the 128x128 matrix with
 //      parallel-ordered cyclic Jacobi rotations (64 disjoint pairs per round),
-//      A in fp64 and the rotations accumulated in fp32, all in shared memory;
+//      A as fp32 float pairs (about 48 significant bits; error-free updates
+//      on the fp32 pipes), rotation angles in fp64 and the rotations
+//      accumulated in fp32, all in shared memory;
 //      then eigenvalues sorted descending and each direction's sign fixed so
 //      its largest-magnitude entry is positive.
 //   4. host: energy-threshold rank per group, r = minimum.
@@ -297,6 +299,10 @@ __global__ void gram_reduce_kernel(const float* __restrict__ part, const float* 
 constexpr int kJacThreads = 512;
 constexpr int kLdA = kHeadDim + 1;  // padded rows (fp64 and fp32)
 constexpr int kMaxSweeps = 40;
+// Rotate a pair while |a_pq| > max(kJacRel sqrt|a_pp a_qq|, kJacFloor ||A||_F):
+// a few hundred units of the float pairs' rounding (2^-48)
+constexpr double kJacRel = 1e-13;
+constexpr double kJacFloor = 1e-14;
 
 // Pairs of round `rnd` (0..126) of the round-robin (circle) ordering of 128 indices.
 __device__ __forceinline__ void rr_pair(int rnd, int i, int& p, int& q) {
@@ -315,18 +321,56 @@ __device__ __forceinline__ void rr_pair(int rnd, int i, int& p, int& q) {
   }
 }
 
+// The matrix being diagonalised is held as float pairs (hi + lo, about 48
+// significant bits): every rotation update runs on the fp32 pipes with
+// error-free transformations, where this part's fp64 rate would make it the
+// fit's bottleneck.  A product of two pairs, unnormalised (p + e):
+__device__ __forceinline__ void df_prod(float ah, float al, float bh, float bl, float& p, float& e) {
+  p = __fmul_rn(ah, bh);
+  e = __fmaf_rn(ah, bh, -p);
+  e = __fmaf_rn(ah, bl, e);
+  e = __fmaf_rn(al, bh, e);
+}
+// (p1 + e1) + (p2 + e2) as a normalised pair
+__device__ __forceinline__ void df_sum(float p1, float e1, float p2, float e2, float& hi, float& lo) {
+  float s, err;
+  two_sum(p1, p2, s, err);
+  const float t = __fadd_rn(__fadd_rn(e1, e2), err);
+  hi = __fadd_rn(s, t);
+  lo = __fsub_rn(t, __fsub_rn(hi, s));
+}
+// (x, y) <- (c x - s y, s x + c y) for pairs x, y and rotation (c, s)
+__device__ __forceinline__ void df_rotate(float ch, float cl, float sh, float sl, float& xh, float& xl, float& yh,
+                                          float& yl) {
+  float p1, e1, p2, e2, nxh, nxl, nyh, nyl;
+  df_prod(ch, cl, xh, xl, p1, e1);
+  df_prod(-sh, -sl, yh, yl, p2, e2);
+  df_sum(p1, e1, p2, e2, nxh, nxl);
+  df_prod(sh, sl, xh, xl, p1, e1);
+  df_prod(ch, cl, yh, yl, p2, e2);
+  df_sum(p1, e1, p2, e2, nyh, nyl);
+  xh = nxh;
+  xl = nxl;
+  yh = nyh;
+  yl = nyl;
+}
+
 __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const double* __restrict__ G, float* basis,
                                                              double* eigvals, unsigned int* err) {
   extern __shared__ __align__(128) uint8_t smem[];
-  double* A = reinterpret_cast<double*>(smem);                                    // [128][129]
-  float* V = reinterpret_cast<float*>(smem + sizeof(double) * kHeadDim * kLdA);   // [128][129]
-  double* cs = reinterpret_cast<double*>(smem + sizeof(double) * kHeadDim * kLdA + sizeof(float) * kHeadDim * kLdA);
-  double* sn = cs + 64;
-  int* pp = reinterpret_cast<int*>(sn + 64);
+  float* Ah = reinterpret_cast<float*>(smem);                     // [128][129] high parts
+  float* Al = Ah + kHeadDim * kLdA;                                // [128][129] low parts
+  float* V = Al + kHeadDim * kLdA;                                 // [128][129]
+  float* csh = V + kHeadDim * kLdA;                                // rotations of the round: c, s as pairs
+  float* csl = csh + 64;
+  float* snh = csl + 64;
+  float* snl = snh + 64;
+  int* pp = reinterpret_cast<int*>(snl + 64);
   int* qq = pp + 64;
   int* cnt = qq + 64;          // rotations this sweep
   double* red = reinterpret_cast<double*>(cnt + 4);  // [kJacThreads]
   int* order = reinterpret_cast<int*>(red + kJacThreads);  // [128]
+  auto a64 = [&](int i, int j) { return (double)Ah[i * kLdA + j] + (double)Al[i * kLdA + j]; };
 
   const int tid = threadIdx.x, grp = blockIdx.x;
   const double* Gg = G + (size_t)grp * kHeadDim * kHeadDim;
@@ -334,7 +378,9 @@ __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const double* __res
   for (int e = tid; e < kHeadDim * kHeadDim; e += kJacThreads) {
     const int i = e / kHeadDim, j = e % kHeadDim;
     const double a = Gg[e];
-    A[i * kLdA + j] = a;
+    const float ah = (float)a;
+    Ah[i * kLdA + j] = ah;
+    Al[i * kLdA + j] = (float)(a - (double)ah);
     V[i * kLdA + j] = (i == j) ? 1.f : 0.f;
     fro += a * a;
   }
@@ -344,7 +390,8 @@ __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const double* __res
     if (tid < s) red[tid] += red[tid + s];
     __syncthreads();
   }
-  const double floor_abs = 1e-16 * sqrt(red[0]);
+  // off-diagonal entries below these bounds are at the pairs' rounding level
+  const double floor_abs = kJacFloor * sqrt(red[0]);
   __syncthreads();
 
   int sweep = 0;
@@ -355,9 +402,9 @@ __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const double* __res
       if (tid < 64) {
         int p, q;
         rr_pair(rnd, tid, p, q);
-        const double apq = A[p * kLdA + q], app = A[p * kLdA + p], aqq = A[q * kLdA + q];
+        const double apq = a64(p, q), app = a64(p, p), aqq = a64(q, q);
         double c = 1.0, s = 0.0;
-        if (fabs(apq) > fmax(1e-15 * sqrt(fabs(app * aqq)), floor_abs)) {
+        if (fabs(apq) > fmax(kJacRel * sqrt(fabs(app * aqq)), floor_abs)) {
           const double theta = (aqq - app) / (2.0 * apq);
           const double t = (theta >= 0.0 ? 1.0 : -1.0) / (fabs(theta) + sqrt(theta * theta + 1.0));
           c = 1.0 / sqrt(t * t + 1.0);
@@ -366,43 +413,50 @@ __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const double* __res
         }
         pp[tid] = p;
         qq[tid] = q;
-        cs[tid] = c;
-        sn[tid] = s;
+        const float ch = (float)c, sh = (float)s;
+        csh[tid] = ch;
+        csl[tid] = (float)(c - (double)ch);
+        snh[tid] = sh;
+        snl[tid] = (float)(s - (double)sh);
       }
       __syncthreads();
       // A <- J^T A (rows p, q)
       for (int e = tid; e < 64 * kHeadDim; e += kJacThreads) {
         const int i = e / kHeadDim, k = e % kHeadDim;
-        const double s = sn[i];
-        if (s != 0.0) {
-          const double c = cs[i];
+        if (snh[i] != 0.f) {
           const int p = pp[i], q = qq[i];
-          const double ap = A[p * kLdA + k], aq = A[q * kLdA + k];
-          A[p * kLdA + k] = c * ap - s * aq;
-          A[q * kLdA + k] = s * ap + c * aq;
+          float xh = Ah[p * kLdA + k], xl = Al[p * kLdA + k], yh = Ah[q * kLdA + k], yl = Al[q * kLdA + k];
+          df_rotate(csh[i], csl[i], snh[i], snl[i], xh, xl, yh, yl);
+          Ah[p * kLdA + k] = xh;
+          Al[p * kLdA + k] = xl;
+          Ah[q * kLdA + k] = yh;
+          Al[q * kLdA + k] = yl;
         }
       }
       __syncthreads();
       // A <- A J (columns p, q) and V <- V J
       for (int e = tid; e < 64 * kHeadDim; e += kJacThreads) {
         const int i = e % 64, k = e / 64;
-        const double s = sn[i];
-        if (s != 0.0) {
-          const double c = cs[i];
+        if (snh[i] != 0.f) {
           const int p = pp[i], q = qq[i];
-          const double ap = A[k * kLdA + p], aq = A[k * kLdA + q];
-          A[k * kLdA + p] = c * ap - s * aq;
-          A[k * kLdA + q] = s * ap + c * aq;
-          const float cf = (float)c, sf = (float)s;
+          float xh = Ah[k * kLdA + p], xl = Al[k * kLdA + p], yh = Ah[k * kLdA + q], yl = Al[k * kLdA + q];
+          df_rotate(csh[i], csl[i], snh[i], snl[i], xh, xl, yh, yl);
+          Ah[k * kLdA + p] = xh;
+          Al[k * kLdA + p] = xl;
+          Ah[k * kLdA + q] = yh;
+          Al[k * kLdA + q] = yl;
+          const float cf = csh[i], sf = snh[i];
           const float vp = V[k * kLdA + p], vq = V[k * kLdA + q];
           V[k * kLdA + p] = cf * vp - sf * vq;
           V[k * kLdA + q] = sf * vp + cf * vq;
         }
       }
       __syncthreads();
-      if (tid < 64 && sn[tid] != 0.0) {
-        A[pp[tid] * kLdA + qq[tid]] = 0.0;
-        A[qq[tid] * kLdA + pp[tid]] = 0.0;
+      if (tid < 64 && snh[tid] != 0.f) {
+        Ah[pp[tid] * kLdA + qq[tid]] = 0.f;
+        Al[pp[tid] * kLdA + qq[tid]] = 0.f;
+        Ah[qq[tid] * kLdA + pp[tid]] = 0.f;
+        Al[qq[tid] * kLdA + pp[tid]] = 0.f;
       }
       __syncthreads();
     }
@@ -413,10 +467,10 @@ __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const double* __res
 
   // sort by descending eigenvalue (stable: ties keep index order)
   if (tid < kHeadDim) {
-    const double li = A[tid * kLdA + tid];
+    const double li = a64(tid, tid);
     int pos = 0;
     for (int j = 0; j < kHeadDim; ++j) {
-      const double lj = A[j * kLdA + j];
+      const double lj = a64(j, j);
       pos += (lj > li) || (lj == li && j < tid);
     }
     order[pos] = tid;
@@ -437,13 +491,13 @@ __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const double* __res
     const float sgn = V[arg * kLdA + src] < 0.f ? -1.f : 1.f;
     float* bg = basis + (size_t)grp * kHeadDim * kHeadDim;
     for (int d = 0; d < kHeadDim; ++d) bg[d * kHeadDim + tid] = sgn * V[d * kLdA + src];
-    eigvals[(size_t)grp * kHeadDim + tid] = fmax(A[src * kLdA + src], 0.0);
+    eigvals[(size_t)grp * kHeadDim + tid] = fmax(a64(src, src), 0.0);
   }
 }
 
 static size_t jacobi_smem() {
-  return sizeof(double) * kHeadDim * kLdA + sizeof(float) * kHeadDim * kLdA + sizeof(double) * 128 +
-         sizeof(int) * 128 + sizeof(int) * 4 + sizeof(double) * kJacThreads + sizeof(int) * kHeadDim;
+  return 3 * sizeof(float) * kHeadDim * kLdA + sizeof(float) * 256 + sizeof(int) * 128 + sizeof(int) * 4 +
+         sizeof(double) * kJacThreads + sizeof(int) * kHeadDim;
 }
 
 struct FitLayout {
