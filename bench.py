@@ -174,10 +174,18 @@ def peaks():
 DECODE_SOURCES = ("decode_kernel.cuh", "decode.cu")
 
 
+def code_only(src: str) -> str:
+    """A C/CUDA source without its comments and whitespace, so that the hash
+    below follows changes to the code, not to its comments."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return "".join(src.split())
+
+
 def decode_source_sha():
     h = hashlib.sha256()
     for f in DECODE_SOURCES:
-        h.update(open(os.path.join(ROOT, "rank_latent_kv_gb300", "csrc", f), "rb").read())
+        h.update(code_only(open(os.path.join(ROOT, "rank_latent_kv_gb300", "csrc", f)).read()).encode())
     return h.hexdigest()
 
 
@@ -189,7 +197,7 @@ def traffic_record(workload):
     if not os.path.exists(path):
         return None
     txt = open(path).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(decode sources sha256 ([0-9a-f]{12,64})\)", txt)
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(decode sources sha256 ([0-9a-f]{12,64})[^)]*\)", txt)
     if not m:
         return None
     return float(m.group(1)) if decode_source_sha().startswith(m.group(2)) else None

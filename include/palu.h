@@ -220,8 +220,9 @@ palu_status palu_decode_step(palu_cache* k, palu_cache* v, const void* k_new, co
  * captured in a graph together with appends. */
 palu_status palu_cache_truncate(palu_cache* cache, int64_t length, void* stream);
 
-/* Cache save and restore (page 4, "prompt cache": the cache of a prompt
- * prefix saved and reused by a later request; SURVEY "next" row).  An image
+/* Cache save and restore (the prompt cache of page "add TurboQuant KV cache
+ * compression", the pull request's description and review: the cache of a
+ * prompt prefix saved and reused by a later request).  An image
  * holds a fixed 128-byte header, the cache's state (basis, mean, largest
  * stored scale), the records of every stream's stored blocks, and the fp32
  * tail: host memory, plain bytes.

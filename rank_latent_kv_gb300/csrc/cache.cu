@@ -512,10 +512,10 @@ extern "C" palu_status palu_cache_truncate(palu_cache* cache, int64_t length, vo
 }
 
 // ------------------------------------------------------------------ save / restore
-// A cache image ("prompt cache", page 4: a saved prompt prefix reused by a
-// later request): a fixed header, then the state (basis, mean, header with the
-// largest stored scale), the records of the stream's stored blocks, and the
-// fp32 tail.  Plain bytes in host memory; little-endian as the host.
+// A cache image (the "prompt cache" of page "add TurboQuant KV cache
+// compression": a saved prompt prefix reused by a later request): a fixed
+// header, then the state (basis, mean, header with the largest stored
+// scale), the records of the stream's stored blocks, and the fp32 tail.  Plain bytes in host memory; little-endian as the host.
 namespace palu {
 constexpr uint64_t kImageMagic = 0x50414C55494D4731ull;  // "PALUIMG1"
 struct ImageHeader {

@@ -169,10 +169,10 @@ __global__ void __launch_bounds__(256) latent_qprep_kernel(const DecodeParams p)
 }
 
 // ------------------------------------------------------------------ step prologue
-// One decode step's work before attention (SURVEY "next" row: fused per-step
-// pipeline), in one launch: grid (streams, 3).  CTA (X, 0) appends stream
-// X's new key token, CTA (X, 1) the new value token, CTA (X, 2) prepares
-// stream X's query factors; the three run side by side.  The stored lengths
+// One decode step's work before attention (the fused per-step pipeline), in
+// one launch: grid (streams, 3).  CTA (X, 0) appends stream X's new key
+// token, CTA (X, 1) the new value token, CTA (X, 2) prepares stream X's
+// query factors; the three run side by side.  The stored lengths
 // stay as they were: the decode launch that follows advances them.
 // Launched as a programmatic dependent: the basis rows, which no launch
 // writes, are fetched before waiting for the preceding launch.  The q-prep

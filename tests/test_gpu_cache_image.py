@@ -1,5 +1,6 @@
-"""Cache save and restore (the "prompt cache" of page 4: a prompt prefix's
-cache saved to host memory and reused by a later request), through the C ABI.
+"""Cache save and restore (the "prompt cache" of page "add TurboQuant KV cache
+compression": a prompt prefix's cache saved to host memory and reused by a
+later request), through the C ABI.
 
 A restored cache must be the saved one: the same records, tail, basis and
 length, the same decode attention bit for bit, and the same results after
