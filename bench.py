@@ -190,17 +190,20 @@ def decode_source_sha():
 
 
 def traffic_record(workload):
-    """DRAM bytes per decode-kernel launch from the committed ncu summary of
-    this workload, if there is one and it was taken on the current decode
-    sources (null otherwise)."""
+    """DRAM traffic of one decode-kernel launch from the committed ncu summary
+    of this workload, if there is one and it was taken on the current decode
+    sources (else None).  Returns (traffic bytes, the captured launch's own
+    algorithmic bytes or None): the capture is of one layer, whose ranks (and
+    so algorithmic bytes) differ from the all-layer average in `achieved`."""
     path = os.path.join(ROOT, "profiles", f"latent_decode_{workload}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(decode sources sha256 ([0-9a-f]{12,64})[^)]*\)", txt)
-    if not m:
+    if not m or not decode_source_sha().startswith(m.group(2)):
         return None
-    return float(m.group(1)) if decode_source_sha().startswith(m.group(2)) else None
+    a = re.search(r"algorithmic_bytes_of_captured_launch:\s*([0-9.eE+]+)", txt)
+    return float(m.group(1)), (float(a.group(1)) if a else None)
 
 
 # ------------------------------------------------------------------ CPU oracle leg
@@ -446,6 +449,10 @@ def run_palu(args, w, world, rank, local):
         comp_kivi = run_kivi_comparator(P, w, s, L, int(round(s_ctx)), dev, world)
 
     stats_k, stats_v = kc0.stats(), vc0.stats()
+    # traffic: DRAM bytes of the profiled launch (one layer); beside it that
+    # launch's own algorithmic bytes, so their ratio (record padding and
+    # re-reads) is explicit
+    traffic = traffic_record(w.name)
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -467,7 +474,9 @@ def run_palu(args, w, world, rank, local):
         "roofline": {"bound": "hbm",
                      "kernel": "palu_decode_attn (q-prep + split decode with in-kernel merge), graph of all layers",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "traffic": traffic_record(w.name),
+                     "peak_kind": peak_kind, "traffic": traffic[0] if traffic else None,
+                     "traffic_captured_algorithmic_bytes": traffic[1] if traffic else None,
+                     "traffic_over_algorithmic": (traffic[0] / traffic[1]) if traffic and traffic[1] else None,
                      "algorithmic_bytes_per_launch": bytes_launch, "avg_launch_us": avg_launch * 1e3,
                      "launches_timed": n_launch},
         "clocks": clk.summary(),

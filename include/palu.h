@@ -274,6 +274,18 @@ palu_status palu_cache_stats(const palu_cache* cache, palu_stats* stats);
  * bits in the message and in *device_error if not NULL) when it was set. */
 palu_status palu_cache_sync(palu_cache* cache, uint32_t* device_error, void* stream);
 
+/* Test hook for the device error path (the group-size guard of page "add
+ * TurboQuant KV cache compression", review thread, asks for actionable
+ * errors instead of silent failure; this lets a test see one without faulting
+ * the GPU).  Launches one CTA that waits, with the library's bounded wait and
+ * a limit of spin_limit attempts (1 .. 2^20), on a shared-memory barrier
+ * that it completes itself when signal != 0 and otherwise leaves pending.
+ * No copy is issued on the barrier, so nothing is in flight when the wait
+ * gives up.  A wait that runs out sets PALU_DEVERR_TIMEOUT in the cache's
+ * device error word, reported by palu_cache_sync().  The cache is not
+ * otherwise touched.  Asynchronous on `stream`. */
+palu_status palu_debug_wait_probe(palu_cache* cache, uint32_t spin_limit, int32_t signal, void* stream);
+
 /* Comparator: plain split-K decode attention on uncompressed fp16 K and V
  * (the dense baseline the latent cache is measured against).
  *   k, v  device fp16 [batch, kv_heads, seq_cap, D]; tokens 0..seq-1 are used.

@@ -206,6 +206,13 @@ __device__ __forceinline__ float append_one_token(const CacheView& cv, const __h
 
   if (!cv.quantize) {
     uint8_t* gdst = cv.blocks + (sidx * cv.n_blk_cap + blk) * cv.rec_bytes;
+    if (pos == 0) {
+      // the block opens: clear its record, so the token slots not yet
+      // written (and the padding channels) hold zeros, not stale bytes
+      for (int i = tid; i < cv.rec_bytes / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(gdst)[i] = make_uint4(0u, 0u, 0u, 0u);
+      __syncthreads();
+    }
     for (int j = tid; j < r; j += blockDim.x)
       *reinterpret_cast<__half*>(gdst + latent_off(pos, j)) = __float2half_rn(lat[pos * ld + j]);
     return 0.f;

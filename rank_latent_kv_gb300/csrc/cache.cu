@@ -677,6 +677,35 @@ extern "C" palu_status palu_cache_stats(const palu_cache* c, palu_stats* s) {
   return PALU_OK;
 }
 
+namespace palu {
+// One CTA waits, with the library's bounded wait, on an mbarrier that its
+// thread 0 either completes (signal != 0) or leaves pending.  No copy is ever
+// issued on the barrier, so nothing is in flight when the wait gives up and
+// the CTA returns.  A wait that runs out sets the TIMEOUT bit, as every
+// bounded wait of the library does.
+__global__ void wait_probe_kernel(StateHeader* hdr, uint32_t limit, int signal) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && signal) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&bar)) : "memory");
+  const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar, 0, limit));
+  if (!ok && threadIdx.x == 0) set_dev_error(hdr, PALU_DEVERR_TIMEOUT);
+}
+}  // namespace palu
+
+extern "C" palu_status palu_debug_wait_probe(palu_cache* c, uint32_t spin_limit, int32_t signal, void* stream) {
+  palu_status st = check_cache(c, "cache");
+  if (st != PALU_OK) return st;
+  if (spin_limit < 1 || spin_limit > (1u << 20))
+    return fail(PALU_ERR_INVALID_ARG, "spin_limit must be in [1, 2^20]");
+  wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<StateHeader*>(c->state), spin_limit,
+                                                                      signal ? 1 : 0);
+  return cuda_check(cudaGetLastError(), "wait_probe_kernel launch");
+}
+
 extern "C" palu_status palu_cache_sync(palu_cache* c, uint32_t* device_error, void* stream) {
   palu_status st = check_cache(c, "cache");
   if (st != PALU_OK) return st;

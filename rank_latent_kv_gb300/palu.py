@@ -82,6 +82,7 @@ _SIGNATURES = {
     "palu_cache_save": (c_int32, [_P(palu_cache), c_void_p, c_size_t, c_void_p]),
     "palu_cache_restore": (c_int32, [_P(palu_cache), c_void_p, c_size_t, c_void_p]),
     "palu_cache_sync": (c_int32, [_P(palu_cache), _P(c_uint32), c_void_p]),
+    "palu_debug_wait_probe": (c_int32, [_P(palu_cache), c_uint32, c_int32, c_void_p]),
     "palu_fp16_decode_workspace_size": (c_int32, [c_int64, c_int32, c_int64, c_int32, _P(c_size_t)]),
     "palu_fp16_decode_attn": (c_int32, [c_void_p, c_void_p, c_int64, c_int32, c_int64, c_int64, c_void_p, c_int32,
                                         c_float, c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
@@ -244,6 +245,11 @@ def palu_cache_sync(cache, stream=None) -> int:
     e = c_uint32()
     _check(lib().palu_cache_sync(ctypes.byref(cache), ctypes.byref(e), _stream(stream)))
     return e.value
+
+
+def palu_debug_wait_probe(cache, spin_limit, signal, stream=None):
+    """Run the library's bounded wait on a barrier that is signalled or left pending."""
+    _check(lib().palu_debug_wait_probe(ctypes.byref(cache), spin_limit, 1 if signal else 0, _stream(stream)))
 
 
 def palu_fp16_decode_workspace_size(batch, kv_heads, seq_cap, q_heads) -> int:

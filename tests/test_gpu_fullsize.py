@@ -1,9 +1,10 @@
 """Full-size parity: one layer of each of the five workloads at its real
 batch, head count and prefill length, in the launch configuration the
 benchmark uses.  The oracle checks sampled outputs it can compute one by one:
-the fit of every group (subspace residual, ranks), sampled block records
-(bit-exact codes and scale/zero against the oracle's encode on the GPU's
-basis), and sampled query heads of the decode attention after decode-step
+the fit of every group (subspace residual, ranks), 256 sampled block records
+per tensor (codes and scale/zero against the oracle's encode on the GPU's
+basis, with the mismatch fractions counted over all sampled values against
+1e-5), and sampled query heads of the decode attention after decode-step
 appends (2e-3 relative, on the same stored codes)."""
 import math
 
@@ -16,6 +17,8 @@ import oracle as O
 pytestmark = pytest.mark.gpu
 
 WORKLOADS = ["tiny", "llama3b", "serving", "longctx", "qwen7b"]
+CODE_MISMATCH_TOL = 1e-5   # fraction of codes (and of scale/zero values) allowed to differ
+N_SAMPLED_BLOCKS = 256     # block records sampled per tensor (all of them when there are fewer)
 
 
 @pytest.fixture(scope="module")
@@ -79,29 +82,48 @@ def test_full_size_layer(P, name):
     torch.cuda.synchronize()
     assert kc.sync() == 0 and vc.sync() == 0
 
-    # ---- sampled block records vs the oracle's encode on the GPU basis
+    # ---- sampled block records vs the oracle's encode on the GPU basis.
+    # The bar is aggregate over every sampled code of a tensor: at most
+    # CODE_MISMATCH_TOL of the codes may differ (and then by one level), and
+    # at most that fraction of the fp16 scales, zeros or unquantized latents.
     for c, (xh, quant), role in ((kc, fits[0], O.ROLE_KEY), (vc, fits[1], O.ROLE_VALUE)):
         Vr, mu = c.basis_array()
         cc = c.c
         lay = O.Layout(role, cc.rank, cc.n_hi, quant)
         rec = c.record_array()
         nb = w.prefill // 32
-        for _ in range(24):
-            b, h, blk = rng.integers(w.batch), rng.integers(w.hkv), rng.integers(nb)
+        all_blocks = [(b, h, k) for b in range(w.batch) for h in range(w.hkv) for k in range(nb)]
+        pick = rng.choice(len(all_blocks), size=min(N_SAMPLED_BLOCKS, len(all_blocks)), replace=False)
+        n_codes = n_code_bad = n_sz = n_sz_bad = n_lat = n_lat_bad = 0
+        max_diff = 0
+        for i in pick:
+            b, h, blk = all_blocks[i]
             g = h // (w.hkv // w.n_groups)
             lat = O.project(xh[b, h, 32 * blk:32 * blk + 32], Vr[g], mu[g])[None]
+            got = rec[b, h, blk][None]
             if quant:
                 codes, s_h, z_h = O.quantize_blocks(lat, cc.n_hi)
-                ref = lay.pack(codes, s_h, z_h)[0]
-                got = rec[b, h, blk]
-                if not np.array_equal(ref, got):
-                    cg, sg, zg = lay.unpack(got[None])
-                    diff = np.abs(cg.astype(int) - codes.astype(int))
-                    assert diff.max() <= 1 and (diff > 0).sum() <= 1, f"block {(b, h, blk)}"
+                cg, sg, zg = lay.unpack(got)
+                diff = np.abs(cg.astype(int) - codes.astype(int))
+                max_diff = max(max_diff, int(diff.max()))
+                n_codes += diff.size
+                n_code_bad += int((diff > 0).sum())
+                n_sz += 2 * s_h.size
+                n_sz_bad += int((sg.view(np.uint16) != s_h.view(np.uint16)).sum())
+                n_sz_bad += int((zg.view(np.uint16) != z_h.view(np.uint16)).sum())
             else:
                 ref = lay.unpack_latents(lay.pack_latents(lat.astype(np.float16)))
-                got = lay.unpack_latents(rec[b, h, blk][None])
-                assert (ref.view(np.uint16) != got.view(np.uint16)).sum() <= 1
+                gl = lay.unpack_latents(got)
+                n_lat += ref.size
+                n_lat_bad += int((ref.view(np.uint16) != gl.view(np.uint16)).sum())
+        print(f"{name} role {role}: {len(pick)} blocks, codes {n_code_bad}/{n_codes} differ (max {max_diff}), "
+              f"scale/zero {n_sz_bad}/{n_sz}, fp16 latents {n_lat_bad}/{n_lat}")
+        if quant:
+            assert max_diff <= 1, f"{name} role {role}: a code differs by {max_diff}"
+            assert n_code_bad <= CODE_MISMATCH_TOL * n_codes, f"{name} role {role}: {n_code_bad}/{n_codes} codes differ"
+            assert n_sz_bad <= CODE_MISMATCH_TOL * n_sz, f"{name} role {role}: {n_sz_bad}/{n_sz} scale/zero differ"
+        else:
+            assert n_lat_bad <= CODE_MISMATCH_TOL * n_lat, f"{name} role {role}: {n_lat_bad}/{n_lat} latents differ"
 
     # ---- sampled decode heads vs the oracle on the same stored codes
     views = []

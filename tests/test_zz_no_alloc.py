@@ -7,9 +7,10 @@ caller workspace.  This file is collected last on purpose, so a run that
 stops at the first failure has already run every other test.
 
 Checked through the C ABI: two calls in a row (different queries and one
-appended token between them, so a stale scratch would show) agree with the
-workspace entry point within the attention tolerance, and a cache set whose
-partials exceed the fixed scratch is refused with a clear error."""
+appended token between them, so a stale scratch would show) agree within the
+attention tolerance with the CPU oracle on the stored codes and with the
+workspace entry point, and a cache set whose partials exceed the fixed
+scratch is refused with a clear error."""
 import ctypes
 import math
 
@@ -39,7 +40,14 @@ def _lowrank(rng, B, H, S):
     return (rng.standard_normal((B, H, S, 24)) @ A + rng.standard_normal(128) * 0.7).astype(np.float16)
 
 
-def test_noalloc_matches_workspace_decode_on_two_calls(P):
+def _oracle_view(c, role):
+    Vr, mu = c.basis_array()
+    cc = c.c
+    return O.OracleCache.from_buffers(role, Vr, mu, cc.rank, cc.batch, cc.kv_heads, cc.capacity, bool(cc.quantize),
+                                      c.record_array(), c.tail_array(), cc.length)
+
+
+def test_noalloc_matches_oracle_and_workspace_decode_on_two_calls(P):
     rng = np.random.default_rng(42)
     B, H, Gq, S = 2, 4, 3, 301
     caches = []
@@ -67,9 +75,14 @@ def test_noalloc_matches_workspace_decode_on_two_calls(P):
                                           H * Gq, ctypes.c_float(0.0), ctypes.c_void_p(out.data_ptr()), 1, stream)
         assert st == P.PALU_OK, P.palu_last_error()
         torch.cuda.synchronize()
-        err = O.relative_error(out.cpu().numpy(), ref.cpu().numpy())
-        assert np.isfinite(err).all() and err.max() <= ATTN_TOL, f"call {call}: {err.max():.3e}"
-    assert kc.sync() == 0 and vc.sync() == 0
+        assert kc.sync() == 0 and vc.sync() == 0
+        got = out.cpu().numpy()
+        # the oracle: naive fp64 attention over K and V rebuilt from the stored codes
+        ora = O.attend(q.cpu().numpy(), _oracle_view(kc, O.ROLE_KEY), _oracle_view(vc, O.ROLE_VALUE))
+        err = O.relative_error(got, ora)
+        assert np.isfinite(err).all() and err.max() <= ATTN_TOL, f"call {call} vs oracle: {err.max():.3e}"
+        err_ws = O.relative_error(got, ref.cpu().numpy())
+        assert np.isfinite(err_ws).all() and err_ws.max() <= ATTN_TOL, f"call {call} vs workspace: {err_ws.max():.3e}"
 
 
 def test_noalloc_refuses_partials_larger_than_its_scratch(P):
