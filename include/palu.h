@@ -59,7 +59,8 @@ enum {
   PALU_DEVERR_CAPACITY = 1u,        /* append beyond capacity (nothing written) */
   PALU_DEVERR_TIMEOUT = 2u,         /* a bounded wait on a copy ran out */
   PALU_DEVERR_LENGTH_MISMATCH = 4u, /* key and value caches differ in length */
-  PALU_DEVERR_NOT_CONVERGED = 8u    /* eigen-solver hit its sweep limit */
+  PALU_DEVERR_NOT_CONVERGED = 8u,   /* eigen-solver hit its sweep limit */
+  PALU_DEVERR_ROLLBACK = 16u        /* a per-sequence rollback was refused (that sequence kept its length) */
 };
 
 /* Configuration, mirroring the page's KVCacheConfig fields (section "Usage"):
@@ -219,6 +220,43 @@ palu_status palu_decode_step(palu_cache* k, palu_cache* v, const void* k_new, co
  * length.  Sets the device-side length with a one-thread kernel, so it can be
  * captured in a graph together with appends. */
 palu_status palu_cache_truncate(palu_cache* cache, int64_t length, void* stream);
+
+/* Ragged per-sequence lengths (page "add TurboQuant KV cache compression",
+ * the pull request's description and review: prompts of different lengths
+ * in one batch, a restored prompt prefix, speculative rollback).  The
+ * sequences of a batch keep one basis and mean per head group; a sequence's
+ * KV heads share its length, and its blocks and tail follow the uniform rules
+ * at its own positions.  The first ragged call switches the cache to
+ * per-sequence lengths (each sequence starting from the shared one); every
+ * later append, decode step and decode attention then works at each
+ * sequence's own position, and decode attention of sequence b covers exactly
+ * its own tokens.  Up to 4096 sequences (PALU_ERR_UNSUPPORTED beyond).
+ * cache->length (host) becomes an upper bound of the longest sequence;
+ * palu_cache_sync or palu_cache_lengths makes it exact (do that before
+ * palu_cache_save).  Every sequence must hold at least one token when
+ * attention runs.
+ *
+ * palu_encode_append_ragged: sequence b appends the first counts[b] of its
+ *   `tokens` rows of x.
+ *     x       device fp16 [batch, kv_heads, tokens, D], contiguous, 16-byte aligned.
+ *     counts  device int32 [batch], each in [0, tokens] (device memory, so a
+ *             captured graph can replay with new counts).
+ *   A sequence whose append would pass the capacity (or whose count is out
+ *   of range) writes nothing and keeps its length, and PALU_DEVERR_CAPACITY
+ *   is set.  Three kernel launches on `stream`.
+ * palu_cache_truncate_ragged: sequence b goes back to lengths[b] tokens
+ *   (device int64 [batch]) under palu_cache_truncate's rule (no growth; for
+ *   quantized caches a multiple of 32 or a length inside the current partial
+ *   block); a refused sequence keeps its length and PALU_DEVERR_ROLLBACK is
+ *   set.  (palu_cache_truncate on a ragged cache rolls every longer sequence
+ *   back to its length, under the same rule.)
+ * palu_cache_lengths: synchronises `stream` and writes each sequence's
+ *   length into lengths (host int64 [batch]; the shared length for a cache
+ *   without ragged lengths); refreshes cache->length. */
+palu_status palu_encode_append_ragged(palu_cache* cache, const void* x, int64_t tokens, const int32_t* counts,
+                                      void* stream);
+palu_status palu_cache_truncate_ragged(palu_cache* cache, const int64_t* lengths, void* stream);
+palu_status palu_cache_lengths(palu_cache* cache, int64_t* lengths, void* stream);
 
 /* Cache save and restore (the prompt cache of page "add TurboQuant KV cache
  * compression", the pull request's description and review: the cache of a

@@ -275,13 +275,15 @@ __device__ __forceinline__ float append_one_token(const CacheView& cv, const __h
   return smax;
 }
 
-// Called by one thread of each of the n_cta CTAs that appended at p0, after
-// its CTA's writes: the last to arrive advances the length.
+// Called by one thread of each of the n_cta CTAs that appended one token at
+// p0 (their sequence's position), after its CTA's writes: the last to arrive
+// advances the length(s).
 __device__ __forceinline__ void publish_length(const CacheView& cv, long long p0, unsigned int n_cta) {
   __threadfence();
   const unsigned int t = atomicAdd(&cv.hdr->ticket, 1u);
   if (t == n_cta - 1) {
-    cv.hdr->length = p0 + 1;
+    if (cv.hdr->ragged) advance_ragged_lengths(cv, nullptr, 1);
+    else cv.hdr->length = p0 + 1;
     cv.hdr->ticket = 0u;
     __threadfence();
   }

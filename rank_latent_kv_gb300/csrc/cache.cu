@@ -43,6 +43,7 @@ __global__ void cache_init_kernel(const float* __restrict__ basis, int ld, const
     hdr->err = 0;
     hdr->ticket = 0;
     hdr->max_scale = 0;
+    hdr->ragged = 0;
   }
 }
 
@@ -72,8 +73,10 @@ __host__ __device__ inline EncodeSmem encode_smem(int r, int rec_bytes) {
 // writes that partial block (the tail) and publishes the new length.  A
 // single launch would race: the CTA completing the old partial block reads
 // the tail rows the CTA of the new partial block overwrites.
+// counts (device [batch], or NULL): sequence b appends the first counts[b]
+// of its T rows; NULL appends all T rows of every sequence.
 __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const __half* __restrict__ x,
-                                                            long long T, int Hkv, int phase) {
+                                                            long long T, int Hkv, int phase, const int* counts) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int r = cv.r;
   const EncodeSmem L = encode_smem(r, cv.rec_bytes);
@@ -86,20 +89,26 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
 
   const int tid = threadIdx.x;
   const int h = blockIdx.y, b = blockIdx.z;
-  const long long p0 = __ldcg(&cv.hdr->length);
-  const long long p1 = p0 + T;
+  const bool ragged = __ldcg(&cv.hdr->ragged) != 0;
+  const long long p0 = ragged ? __ldcg(cv.seq_len + b) : __ldcg(&cv.hdr->length);
+  const long long n_b = counts ? (long long)__ldcg(counts + b) : T;
+  const long long p1 = p0 + n_b;
   const unsigned int n_cta = gridDim.x * gridDim.y * gridDim.z;
 
-  if (p1 > cv.capacity) {
+  if (!ragged && p1 > cv.capacity) {
     if (blockIdx.x == 0 && h == 0 && b == 0 && tid == 0) set_dev_error(cv.hdr, PALU_DEVERR_CAPACITY);
     return;  // nothing written, length unchanged (no CTA takes a ticket)
   }
+  // ragged: a sequence whose append would pass the capacity (or whose count
+  // is out of range) writes nothing and keeps its length
+  const bool refused = ragged && (n_b < 0 || n_b > T || p1 > cv.capacity);
+  if (refused && blockIdx.x == 0 && h == 0 && tid == 0) set_dev_error(cv.hdr, PALU_DEVERR_CAPACITY);
 
   // phase 1: block p0 / 32 + blockIdx.x; phase 2: the block holding token p1
   const long long blk = phase == 2 ? p1 / kBlock : p0 / kBlock + blockIdx.x;
   const long long lo = blk * kBlock;
   const bool last_partial = blk == p1 / kBlock && p1 % kBlock != 0;
-  if (lo < p1 && last_partial == (phase == 2)) {
+  if (!refused && lo < p1 && last_partial == (phase == 2)) {
     const long long new_lo = lo > p0 ? lo : p0;
     const long long hi = (lo + kBlock < p1) ? lo + kBlock : p1;
     const int off_new = (int)(new_lo - lo);
@@ -270,14 +279,15 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
     }
   }
 
-  // the last CTA of phase 2 to finish publishes the new length
+  // the last CTA of phase 2 to finish publishes the new length(s)
   if (phase != 2) return;
   __syncthreads();
   if (tid == 0) {
     __threadfence();
     const unsigned int t = atomicAdd(&cv.hdr->ticket, 1u);
     if (t == n_cta - 1) {
-      cv.hdr->length = p1;
+      if (ragged) advance_ragged_lengths(cv, counts, T);
+      else cv.hdr->length = p1;
       cv.hdr->ticket = 0u;
       __threadfence();
     }
@@ -303,21 +313,73 @@ __global__ void __launch_bounds__(kEncOneThreads) encode_one_kernel(CacheView cv
     mbar_arrive_expect_tx(&bar, (uint32_t)r * 512u);
     bulk_g2s(sm.bas, cv.basisT + (size_t)(h / cv.heads_per_group) * r * kHeadDim, (uint32_t)r * 512u, &bar);
   }
-  const long long p0 = __ldcg(&cv.hdr->length);
+  const long long p0 = seq_length(cv, b);
   __syncthreads();  // barrier initialised
   const bool got = mbar_wait_bounded(&bar, 0);  // also drains the copy before any early exit
   if (!got && tid == 0) set_dev_error(cv.hdr, PALU_DEVERR_TIMEOUT);
-  if (p0 + 1 > cv.capacity) {
+  if (__ldcg(&cv.hdr->length) + 1 > cv.capacity) {
+    // the longest sequence is full: nothing written, lengths unchanged (no CTA takes a ticket)
     if (h == 0 && b == 0 && tid == 0) set_dev_error(cv.hdr, PALU_DEVERR_CAPACITY);
-    return;  // nothing written, length unchanged (no CTA takes a ticket)
+    return;
   }
   append_one_token(cv, x + ((long long)b * Hkv + h) * kHeadDim, p0, h, b, Hkv, sm);
   __syncthreads();
   if (tid == 0) publish_length(cv, p0, gridDim.x * gridDim.y);
 }
 
+// Switches a cache to ragged lengths (once): every sequence starts from the
+// shared length.
+__global__ void cache_make_ragged_kernel(StateHeader* hdr, long long* seq_len, int batch) {
+  if (hdr->ragged) return;
+  for (int b = 0; b < batch; ++b) seq_len[b] = hdr->length;
+  hdr->ragged = 1u;
+  __threadfence();
+}
+
+// Per-sequence rollback: sequence b goes back to lengths[b] tokens when that
+// is allowed (no growth; for quantized caches a block boundary or a length
+// inside the current partial block), else keeps its length and the
+// rollback error bit is set.
+__global__ void cache_truncate_ragged_kernel(StateHeader* hdr, long long* seq_len, int batch,
+                                             const long long* lengths, int quantize) {
+  long long mx = 0;
+  bool bad = false;
+  for (int b = 0; b < batch; ++b) {
+    const long long cur = seq_len[b], n = lengths[b];
+    const bool ok = n >= 0 && n <= cur && (!quantize || n % kBlock == 0 || n / kBlock == cur / kBlock);
+    const long long nl = ok ? n : cur;
+    bad |= !ok;
+    seq_len[b] = nl;
+    mx = nl > mx ? nl : mx;
+  }
+  hdr->length = mx;
+  if (bad) hdr->err |= PALU_DEVERR_ROLLBACK;
+}
+
 // Sets the device length (the host has checked that no quantized block is reopened).
-__global__ void cache_truncate_kernel(StateHeader* hdr, long long length) {
+// With ragged lengths every sequence longer than `length` goes back to it
+// when the rollback rule allows (else it keeps its length and the rollback
+// error bit is set); shorter sequences keep theirs.
+__global__ void cache_truncate_kernel(StateHeader* hdr, long long* seq_len, int batch, long long length,
+                                      int quantize) {
+  if (hdr->ragged) {
+    long long mx = 0;
+    bool bad = false;
+    for (int b = 0; b < batch; ++b) {
+      const long long cur = seq_len[b];
+      long long nl = cur;
+      if (length < cur) {
+        const bool ok = !quantize || length % kBlock == 0 || length / kBlock == cur / kBlock;
+        bad |= !ok;
+        if (ok) nl = length;
+      }
+      seq_len[b] = nl;
+      mx = nl > mx ? nl : mx;
+    }
+    hdr->length = mx;
+    if (bad) hdr->err |= PALU_DEVERR_ROLLBACK;
+    return;
+  }
   if (length > hdr->length) {
     hdr->err |= PALU_DEVERR_CAPACITY;
     return;
@@ -393,7 +455,7 @@ extern "C" palu_status palu_cache_size(const palu_config* cfg, int32_t role, int
   const bool quant = cfg->quantize || role == PALU_ROLE_KEY;
   if (block_bytes) *block_bytes = align_up((size_t)batch * kv_heads * n_blk * g.rec_bytes, 256);
   if (tail_bytes) *tail_bytes = quant ? align_up(sizeof(float) * (size_t)batch * kv_heads * kBlock * rank, 256) : 0;
-  if (state_bytes) *state_bytes = state_layout(cfg->n_head_groups, rank, batch * (int64_t)kv_heads).total;
+  if (state_bytes) *state_bytes = state_layout(cfg->n_head_groups, rank, batch, kv_heads).total;
   return PALU_OK;
 }
 
@@ -433,7 +495,7 @@ extern "C" palu_status palu_cache_init(palu_cache* cache, const palu_config* cfg
   c.tail = quant ? static_cast<float*>(tail) : nullptr;
   c.state = state;
   c.length = 0;
-  const StateLayout sl = state_layout(c.n_groups, rank, batch * (int64_t)kv_heads);
+  const StateLayout sl = state_layout(c.n_groups, rank, batch, kv_heads);
   uint8_t* s = static_cast<uint8_t*>(state);
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
   cache_init_kernel<<<dim3(rank, c.n_groups), kHeadDim, 0, strm>>>(
@@ -441,8 +503,8 @@ extern "C" palu_status palu_cache_init(palu_cache* cache, const palu_config* cfg
       reinterpret_cast<float2*>(s + sl.mv_off), reinterpret_cast<StateHeader*>(s), rank);
   st = cuda_check(cudaGetLastError(), "cache_init_kernel launch");
   if (st != PALU_OK) return st;
-  st = cuda_check(cudaMemsetAsync(s + sl.smax_off, 0, sizeof(unsigned int) * (size_t)batch * kv_heads, strm),
-                  "cudaMemsetAsync(largest scales)");
+  st = cuda_check(cudaMemsetAsync(s + sl.smax_off, 0, sl.total - sl.smax_off, strm),
+                  "cudaMemsetAsync(largest scales, sequence lengths)");
   if (st != PALU_OK) return st;
   *cache = c;
   return PALU_OK;
@@ -486,7 +548,7 @@ extern "C" palu_status palu_encode_append(palu_cache* cache, const void* x, int6
   for (int phase = 1; phase <= 2; ++phase) {
     encode_append_kernel<<<dim3(phase == 1 ? (unsigned)nblk : 1u, cache->kv_heads, cache->batch), 128, smem,
                            static_cast<cudaStream_t>(stream)>>>(cv, static_cast<const __half*>(x), tokens,
-                                                                cache->kv_heads, phase);
+                                                                cache->kv_heads, phase, nullptr);
     st = cuda_check(cudaGetLastError(), "encode_append_kernel launch");
     if (st != PALU_OK) return st;
   }
@@ -494,17 +556,91 @@ extern "C" palu_status palu_encode_append(palu_cache* cache, const void* x, int6
   return PALU_OK;
 }
 
+extern "C" palu_status palu_encode_append_ragged(palu_cache* cache, const void* x, int64_t tokens,
+                                                 const int32_t* counts, void* stream) {
+  palu_status st = check_cache(cache, "cache");
+  if (st != PALU_OK) return st;
+  if (tokens < 0) return fail(PALU_ERR_INVALID_ARG, "tokens must be >= 0");
+  if (tokens == 0) return PALU_OK;
+  if (!x || ((uintptr_t)x & 15)) return fail(PALU_ERR_INVALID_ARG, "x must be a non-NULL, 16-byte aligned device pointer");
+  if (!counts || ((uintptr_t)counts & 3)) return fail(PALU_ERR_INVALID_ARG, "counts must be a non-NULL int32 device pointer");
+  if (cache->batch > kMaxRaggedBatch)
+    return fail(PALU_ERR_UNSUPPORTED, "ragged lengths are supported up to " + std::to_string(kMaxRaggedBatch) + " sequences");
+  const int64_t nblk = (tokens + kBlock - 1) / kBlock + 1;  // blocks touched from any start offset
+  if (nblk > 2147483647LL) return fail(PALU_ERR_UNSUPPORTED, "too many tokens in one append");
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  const CacheView cv = make_view(cache);
+  cache_make_ragged_kernel<<<1, 1, 0, strm>>>(cv.hdr, cv.seq_len, cache->batch);
+  st = cuda_check(cudaGetLastError(), "cache_make_ragged_kernel launch");
+  if (st != PALU_OK) return st;
+  const int smem = encode_smem(cache->rank, cache->record_bytes).total;
+  int per_sm = 0;
+  st = kernel_occupancy(reinterpret_cast<const void*>(encode_append_kernel), 128, smem, &per_sm);
+  if (st != PALU_OK) return st;
+  for (int phase = 1; phase <= 2; ++phase) {
+    encode_append_kernel<<<dim3(phase == 1 ? (unsigned)nblk : 1u, cache->kv_heads, cache->batch), 128, smem, strm>>>(
+        cv, static_cast<const __half*>(x), tokens, cache->kv_heads, phase, counts);
+    st = cuda_check(cudaGetLastError(), "encode_append_kernel launch");
+    if (st != PALU_OK) return st;
+  }
+  // the host count stays an upper bound of the longest sequence (the counts
+  // are on the device); palu_cache_sync or palu_cache_lengths makes it exact
+  cache->length = std::min<int64_t>(cache->length + tokens, cache->capacity);
+  return PALU_OK;
+}
+
+extern "C" palu_status palu_cache_truncate_ragged(palu_cache* cache, const int64_t* lengths, void* stream) {
+  palu_status st = check_cache(cache, "cache");
+  if (st != PALU_OK) return st;
+  if (!lengths || ((uintptr_t)lengths & 7)) return fail(PALU_ERR_INVALID_ARG, "lengths must be a non-NULL int64 device pointer");
+  if (cache->batch > kMaxRaggedBatch)
+    return fail(PALU_ERR_UNSUPPORTED, "ragged lengths are supported up to " + std::to_string(kMaxRaggedBatch) + " sequences");
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  const CacheView cv = make_view(cache);
+  cache_make_ragged_kernel<<<1, 1, 0, strm>>>(cv.hdr, cv.seq_len, cache->batch);
+  st = cuda_check(cudaGetLastError(), "cache_make_ragged_kernel launch");
+  if (st != PALU_OK) return st;
+  cache_truncate_ragged_kernel<<<1, 1, 0, strm>>>(cv.hdr, cv.seq_len, cache->batch,
+                                                reinterpret_cast<const long long*>(lengths), cache->quantize);
+  return cuda_check(cudaGetLastError(), "cache_truncate_ragged_kernel launch");
+}
+
+extern "C" palu_status palu_cache_lengths(palu_cache* cache, int64_t* lengths, void* stream) {
+  palu_status st = check_cache(cache, "cache");
+  if (st != PALU_OK) return st;
+  if (!lengths) return fail(PALU_ERR_INVALID_ARG, "lengths is NULL");
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  st = cuda_check(cudaStreamSynchronize(strm), "cudaStreamSynchronize");
+  if (st != PALU_OK) return st;
+  const CacheView cv = make_view(cache);
+  StateHeader h;
+  st = cuda_check(cudaMemcpy(&h, cv.hdr, sizeof(h), cudaMemcpyDeviceToHost), "read cache state");
+  if (st != PALU_OK) return st;
+  if (h.ragged) {
+    st = cuda_check(cudaMemcpy(lengths, cv.seq_len, sizeof(int64_t) * (size_t)cache->batch, cudaMemcpyDeviceToHost),
+                    "read sequence lengths");
+    if (st != PALU_OK) return st;
+  } else {
+    for (int b = 0; b < cache->batch; ++b) lengths[b] = h.length;
+  }
+  cache->length = h.length;
+  return PALU_OK;
+}
+
 extern "C" palu_status palu_cache_truncate(palu_cache* cache, int64_t length, void* stream) {
   palu_status st = check_cache(cache, "cache");
   if (st != PALU_OK) return st;
+  // (on a cache with ragged lengths the kernel sets every sequence to `length`
+  // only if each allows it; palu_cache_truncate_ragged is the general call)
   if (length < 0 || length > cache->length)
     return fail(PALU_ERR_INVALID_ARG, "truncate length must be in [0, current length]");
   const int64_t open_block = (cache->length / kBlock) * kBlock;
   if (cache->quantize && length % kBlock != 0 && length < open_block)
     return fail(PALU_ERR_INVALID_ARG,
                 "truncate to a length inside an already quantized 32-token block is not possible; use a multiple of 32");
-  cache_truncate_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<StateHeader*>(cache->state), length);
+  const CacheView cv = make_view(cache);
+  cache_truncate_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(cv.hdr, cv.seq_len, cache->batch, length,
+                                                                        cache->quantize);
   st = cuda_check(cudaGetLastError(), "cache_truncate_kernel launch");
   if (st != PALU_OK) return st;
   cache->length = length;
@@ -548,7 +684,7 @@ static ImageHeader image_header(const palu_cache* c) {
   h.record_bytes = c->record_bytes;
   h.length = c->length;
   h.n_blocks = stored_blocks(c, c->length);
-  h.state_bytes = (int64_t)state_layout(c->n_groups, c->rank, (int64_t)c->batch * c->kv_heads).total;
+  h.state_bytes = (int64_t)state_layout(c->n_groups, c->rank, c->batch, c->kv_heads).total;
   h.block_bytes = (int64_t)c->batch * c->kv_heads * h.n_blocks * c->record_bytes;
   h.tail_bytes = c->quantize ? (int64_t)sizeof(float) * c->batch * c->kv_heads * kBlock * c->rank : 0;
   return h;

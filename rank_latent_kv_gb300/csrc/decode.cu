@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(256) latent_step_prologue_kernel(const DecodeP
   }
   grid_dep_wait();
   grid_dep_launch();
-  const long long p0 = __ldcg(&cv.hdr->length);
+  const long long p0 = seq_length(cv, b);  // this sequence's position
   __syncthreads();
   const bool got = mbar_wait_bounded(&bar, 0);
   if (!got && tid == 0) set_dev_error(cv.hdr, PALU_DEVERR_TIMEOUT);

@@ -433,15 +433,27 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kClassDecThreads, 1)
   // stores the new one.  Copies of blocks the prologue did not write may
   // start before its results are awaited; a block the appended token
   // completed may not.
+  // With ragged lengths the split is that of the longest sequence (the
+  // header length): every stream gets the same range of block positions, and
+  // a warp skips the positions past its stream's own full blocks.
+  const bool ragged = __ldcg(&p.k.hdr->ragged) != 0;
   const long long len0 = __ldcg(&p.k.hdr->length);
   const bool grows = p.after_append && len0 < p.k.capacity;
   const long long len = len0 + (grows ? 1 : 0);
-  if (grows && len % kBlock == 0) grid_dep_wait();
+  if (grows && (ragged || len % kBlock == 0)) grid_dep_wait();
   grid_dep_launch();
   const long long nf = len / kBlock;
   const long long T = p.streams * nf;
-  if (tid == 0 && blockIdx.x == 0 && __ldcg(&p.v.hdr->length) != len0)
-    set_dev_error(p.k.hdr, PALU_DEVERR_LENGTH_MISMATCH);
+  // tokens of stream x at this launch (after a step prologue, one more)
+  auto stream_len = [&](long long x) -> long long {
+    return ragged ? __ldcg(p.k.seq_len + x / p.Hkv) + (grows ? 1 : 0) : len;
+  };
+  if (tid == 0 && blockIdx.x == 0) {
+    bool bad = __ldcg(&p.v.hdr->length) != len0 || __ldcg(&p.v.hdr->ragged) != (ragged ? 1u : 0u);
+    if (ragged && !bad)
+      for (int b = 0; b < p.k.batch; ++b) bad |= __ldcg(p.k.seq_len + b) != __ldcg(p.v.seq_len + b);
+    if (bad) set_dev_error(p.k.hdr, PALU_DEVERR_LENGTH_MISMATCH);
+  }
   // every warp works on its own: the flat range of full blocks is split over
   // at most T warps, so each warp that takes part owns >= 1 block and the
   // warps covering a stream are consecutive
@@ -486,7 +498,7 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kClassDecThreads, 1)
       const int g0 = (int)(x0 % p.Hkv) / p.v.heads_per_group, g1 = (int)(x1 % p.Hkv) / p.v.heads_per_group;
       prefetch_l2(p.v.basisT + (size_t)g0 * p.v.r * kHeadDim, (uint32_t)p.v.r * 512u);
       if (g1 != g0) prefetch_l2(p.v.basisT + (size_t)g1 * p.v.r * kHeadDim, (uint32_t)p.v.r * 512u);
-      if (len % kBlock != 0 && b_end == (x1 + 1) * nf) {
+      if (!ragged && len % kBlock != 0 && b_end == (x1 + 1) * nf) {
         prefetch_l2(p.k.tail + (size_t)x1 * kBlock * p.k.r, (uint32_t)(kBlock * p.k.r * 4));
         if (p.v.quantize)
           prefetch_l2(p.v.tail + (size_t)x1 * kBlock * p.v.r, (uint32_t)(kBlock * p.v.r * 4));
@@ -535,8 +547,11 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kClassDecThreads, 1)
       set_dev_error(p.k.hdr, PALU_DEVERR_CAPACITY);
       break;
     }
-    // ---- this warp's segment of stream X, two blocks per stage
-    const long long wb0 = max(R0, X * nf) - X * nf, wb1 = min(R1, (X + 1) * nf) - X * nf;
+    // ---- this warp's segment of stream X, two blocks per stage (clipped to
+    // the stream's own full blocks)
+    const long long nfX = ragged ? stream_len(X) / kBlock : nf;
+    const long long wb1 = min(min(R1, (X + 1) * nf) - X * nf, nfX);
+    const long long wb0 = min(max(R0, X * nf) - X * nf, wb1);
     const int n_my = (int)(wb1 - wb0), n_st = timed_out ? 0 : (n_my + 1) >> 1;
     // Stage i holds blocks 2i, 2i+1 of the warp's range.  Every stage reads
     // two real records, so that no byte the compute touches is stale: an odd
@@ -544,7 +559,7 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kClassDecThreads, 1)
     // block counted already, is masked), or, for a one-block range, the pair
     // that starts there (second slot masked); a stream of one full block
     // cannot pair up, and its stage copies the block twice.
-    const long long blk_last = (long long)nf - 1;  // last full block of the stream
+    const long long blk_last = nfX - 1;  // last full block of the stream
     int odd_shift = 0, odd_mask = 1;               // odd last stage: source shift, slot to mask
     if (n_my & 1) {
       if (n_my >= 2 || wb0 >= 1) {
@@ -754,7 +769,6 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kClassDecThreads, 1)
     xlo = blockIdx.x * nw;
     xhi = (int)min((long long)xlo + nw, p.streams) - 1;
   }
-  const int n_tail = (int)(len % kBlock);
   const int rk = p.k.r, rv = p.v.r, tks = rk | 1, rvp = p.rvp;
   const float* wpa = reinterpret_cast<const float*>(smem + p.wp_off);
 
@@ -778,6 +792,9 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kClassDecThreads, 1)
       }
     }
     const int cslot = (int)(blockIdx.x - c_first), nseg = (int)(c_last - c_first + 1);
+    const long long len_x = stream_len(x);  // this stream's tokens: its full blocks, then the tail
+    const long long nf_x = len_x / kBlock;
+    const int n_tail = (int)(len_x % kBlock);
     const bool tail_here = n_tail > 0 && blockIdx.x == c_last;
     const int kh = (int)(x % p.Hkv), bb = (int)(x / p.Hkv);
     const int gv = kh / p.v.heads_per_group;
@@ -797,7 +814,7 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kClassDecThreads, 1)
         bulk_g2s(es.qt, p.qt + (size_t)x * 8 * kHeadDim, 4096u, ebar);
         bulk_g2s(es.cq, p.cq + (size_t)x * 8, 32u, ebar);
         const void* src = p.v.quantize ? static_cast<const void*>(p.v.tail + (size_t)x * kBlock * rv)
-                                       : static_cast<const void*>(p.v.blocks + ((size_t)x * p.v.n_blk_cap + nf) * p.v.rec_bytes);
+                                       : static_cast<const void*>(p.v.blocks + ((size_t)x * p.v.n_blk_cap + nf_x) * p.v.rec_bytes);
         bulk_g2s(es.tv, src, tv, ebar);
       }
     }
@@ -1040,8 +1057,13 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kClassDecThreads, 1)
       const unsigned int prev = atomicAdd(p.tickets + p.streams, 1u);
       if (prev + 1 == gridDim.x) {
         __threadfence();
-        p.k.hdr->length = len;
-        p.v.hdr->length = len;
+        if (ragged) {
+          advance_ragged_lengths(p.k, nullptr, 1);
+          advance_ragged_lengths(p.v, nullptr, 1);
+        } else {
+          p.k.hdr->length = len;
+          p.v.hdr->length = len;
+        }
         p.tickets[p.streams] = 0u;
         __threadfence();
       }

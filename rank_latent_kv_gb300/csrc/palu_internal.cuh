@@ -27,35 +27,43 @@ constexpr uint32_t kSpinLimit = 1u << 22;
 
 // ---------------------------------------------------------------- state
 // Device state of a cache, in one caller-owned buffer:
-//   [0, 64)        header: length, error word, ticket, largest stored scale
+//   [0, 64)        header: length, error word, ticket, largest stored scale, ragged flag
 //   basisT         fp32 [n_groups][rank][D]   (row j = direction j)
 //   mu             fp32 [n_groups][D]
 //   mv             fp32 [n_groups][rank][2]   mu_g . V_g[:, j] as a float pair (hi, lo)
+//   smax           u32  [batch * kv_heads]    largest stored fp16 scale per stream
+//   seq_len        i64  [batch]               tokens per sequence (ragged caches)
 struct StateHeader {
-  long long length;
+  long long length;        // tokens of every sequence; with ragged lengths, the largest
   unsigned int err;
   unsigned int ticket;
   unsigned int max_scale;  // bits of the largest fp16 scale stored so far in any stream (a non-negative float)
-  unsigned int pad[11];
+  unsigned int ragged;     // 1: seq_len holds each sequence's own length (set by the ragged calls)
+  unsigned int pad[10];
 };
 static_assert(sizeof(StateHeader) == 64, "state header size");
 
 struct StateLayout {
-  size_t basis_off, mu_off, mv_off, smax_off, total;
+  size_t basis_off, mu_off, mv_off, smax_off, slen_off, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// streams = batch * kv_heads: one largest-scale word per stream follows mv.
-inline StateLayout state_layout(int n_groups, int rank, long long streams) {
+// One largest-scale word per stream (batch * kv_heads) follows mv, then one
+// length per sequence.
+inline StateLayout state_layout(int n_groups, int rank, long long batch, long long kv_heads) {
   StateLayout s;
   s.basis_off = 256;
   s.mu_off = align_up(s.basis_off + sizeof(float) * (size_t)n_groups * rank * kHeadDim, 256);
   s.mv_off = align_up(s.mu_off + sizeof(float) * (size_t)n_groups * kHeadDim, 256);
   s.smax_off = align_up(s.mv_off + sizeof(float) * 2 * (size_t)n_groups * rank, 256);
-  s.total = align_up(s.smax_off + sizeof(unsigned int) * (size_t)streams, 256);
+  s.slen_off = align_up(s.smax_off + sizeof(unsigned int) * (size_t)(batch * kv_heads), 256);
+  s.total = align_up(s.slen_off + sizeof(long long) * (size_t)batch, 256);
   return s;
 }
+
+// Ragged per-sequence lengths are supported up to this many sequences.
+constexpr int kMaxRaggedBatch = 4096;
 
 // Everything a kernel needs to know about one cache.
 struct CacheView {
@@ -66,15 +74,16 @@ struct CacheView {
   const float* mu;       // [n_g][D]
   const float2* mv;      // [n_g][r]
   unsigned int* smax;    // [batch * kv_heads] bits of each stream's largest stored fp16 scale
+  long long* seq_len;    // [batch] tokens per sequence (authoritative when hdr->ragged)
   int64_t n_blk_cap;
   int64_t capacity;
   int r, n_hi, n_hi_oct, n_lo_oct, n_oct, rec_bytes;
-  int heads_per_group, quantize, role;
+  int heads_per_group, quantize, role, batch, kv_heads;
 };
 
 inline CacheView make_view(const palu_cache* c) {
   CacheView v;
-  StateLayout s = state_layout(c->n_groups, c->rank, (long long)c->batch * c->kv_heads);
+  StateLayout s = state_layout(c->n_groups, c->rank, c->batch, c->kv_heads);
   uint8_t* st = static_cast<uint8_t*>(c->state);
   v.blocks = static_cast<uint8_t*>(c->blocks);
   v.tail = c->tail;
@@ -83,6 +92,7 @@ inline CacheView make_view(const palu_cache* c) {
   v.mu = reinterpret_cast<const float*>(st + s.mu_off);
   v.mv = reinterpret_cast<const float2*>(st + s.mv_off);
   v.smax = reinterpret_cast<unsigned int*>(st + s.smax_off);
+  v.seq_len = reinterpret_cast<long long*>(st + s.slen_off);
   v.n_blk_cap = c->n_blk_cap;
   v.capacity = c->capacity;
   v.r = c->rank;
@@ -94,7 +104,32 @@ inline CacheView make_view(const palu_cache* c) {
   v.heads_per_group = c->heads_per_group;
   v.quantize = c->quantize;
   v.role = c->role;
+  v.batch = c->batch;
+  v.kv_heads = c->kv_heads;
   return v;
+}
+
+// Tokens held by sequence b, read on the device: its own length when the
+// cache has ragged lengths, else the shared one.
+__device__ __forceinline__ long long seq_length(const CacheView& v, long long b) {
+  return __ldcg(&v.hdr->ragged) ? __ldcg(v.seq_len + b) : __ldcg(&v.hdr->length);
+}
+
+// Ragged lengths: every sequence's length advances by its own count (counts,
+// device [batch]) or by `delta` when counts is NULL; a sequence whose append
+// would pass the capacity keeps its length (its CTAs wrote nothing).  The
+// shared length becomes the largest.  One thread, after every CTA of the
+// append has read the old lengths.
+__device__ __forceinline__ void advance_ragged_lengths(const CacheView& cv, const int* counts, long long delta) {
+  long long mx = 0;
+  for (int b = 0; b < cv.batch; ++b) {
+    const long long l0 = cv.seq_len[b];
+    const long long n = counts ? (long long)counts[b] : delta;
+    const long long l1 = (n >= 0 && l0 + n <= cv.capacity) ? l0 + n : l0;
+    cv.seq_len[b] = l1;
+    mx = l1 > mx ? l1 : mx;
+  }
+  cv.hdr->length = mx;
 }
 
 // Real latent channel of padded channel p (octet p/8, slot p%8), or -1 for padding.
@@ -135,6 +170,12 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                : "memory");
+}
+
+// Arrive once (release semantics: this thread's earlier writes, and those of
+// threads that synchronised with it before, are visible to the waiter).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {

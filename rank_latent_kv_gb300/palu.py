@@ -25,6 +25,7 @@ PALU_DEVERR_CAPACITY = 1
 PALU_DEVERR_TIMEOUT = 2
 PALU_DEVERR_LENGTH_MISMATCH = 4
 PALU_DEVERR_NOT_CONVERGED = 8
+PALU_DEVERR_ROLLBACK = 16
 STATUS_NAMES = {0: "PALU_OK", 1: "PALU_ERR_INVALID_ARG", 2: "PALU_ERR_UNSUPPORTED", 3: "PALU_ERR_CAPACITY",
                 4: "PALU_ERR_NOT_INITIALIZED", 5: "PALU_ERR_CUDA", 6: "PALU_ERR_DEVICE"}
 
@@ -83,6 +84,9 @@ _SIGNATURES = {
     "palu_cache_restore": (c_int32, [_P(palu_cache), c_void_p, c_size_t, c_void_p]),
     "palu_cache_sync": (c_int32, [_P(palu_cache), _P(c_uint32), c_void_p]),
     "palu_debug_wait_probe": (c_int32, [_P(palu_cache), c_uint32, c_int32, c_void_p]),
+    "palu_encode_append_ragged": (c_int32, [_P(palu_cache), c_void_p, c_int64, c_void_p, c_void_p]),
+    "palu_cache_truncate_ragged": (c_int32, [_P(palu_cache), c_void_p, c_void_p]),
+    "palu_cache_lengths": (c_int32, [_P(palu_cache), _P(c_int64), c_void_p]),
     "palu_fp16_decode_workspace_size": (c_int32, [c_int64, c_int32, c_int64, c_int32, _P(c_size_t)]),
     "palu_fp16_decode_attn": (c_int32, [c_void_p, c_void_p, c_int64, c_int32, c_int64, c_int64, c_void_p, c_int32,
                                         c_float, c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
@@ -247,6 +251,25 @@ def palu_cache_sync(cache, stream=None) -> int:
     return e.value
 
 
+def palu_encode_append_ragged(cache: palu_cache, x, counts, stream=None):
+    """x [B, Hkv, T, D] fp16 (device); counts int32 [B] (device): sequence b appends its first counts[b] rows."""
+    assert x.is_cuda and x.dtype == torch.float16 and counts.is_cuda and counts.dtype == torch.int32
+    _check(lib().palu_encode_append_ragged(ctypes.byref(cache), _ptr(x), x.shape[2], _ptr(counts), _stream(stream)))
+
+
+def palu_cache_truncate_ragged(cache: palu_cache, lengths, stream=None):
+    """lengths int64 [B] (device): per-sequence rollback."""
+    assert lengths.is_cuda and lengths.dtype == torch.int64
+    _check(lib().palu_cache_truncate_ragged(ctypes.byref(cache), _ptr(lengths), _stream(stream)))
+
+
+def palu_cache_lengths(cache: palu_cache, stream=None) -> list:
+    """Each sequence's length (synchronises)."""
+    out = (c_int64 * cache.batch)()
+    _check(lib().palu_cache_lengths(ctypes.byref(cache), out, _stream(stream)))
+    return list(out)
+
+
 def palu_debug_wait_probe(cache, spin_limit, signal, stream=None):
     """Run the library's bounded wait on a barrier that is signalled or left pending."""
     _check(lib().palu_debug_wait_probe(ctypes.byref(cache), spin_limit, 1 if signal else 0, _stream(stream)))
@@ -328,6 +351,16 @@ class LatentCache:
 
     def truncate(self, length, stream=None):
         palu_cache_truncate(self.c, length, stream)
+
+    def append_ragged(self, x, counts, stream=None):
+        """Sequence b appends its first counts[b] rows of x (counts: int32 tensor on the device)."""
+        palu_encode_append_ragged(self.c, x, counts, stream)
+
+    def truncate_ragged(self, lengths, stream=None):
+        palu_cache_truncate_ragged(self.c, lengths, stream)
+
+    def lengths(self, stream=None):
+        return palu_cache_lengths(self.c, stream)
 
     def save(self, stream=None):
         """The cache image in pinned host memory (complete once `stream` has passed the call)."""
