@@ -680,12 +680,16 @@ def main(argv=None):
     ap.add_argument("--no-comparator", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for the CPU baseline")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="replace the workload's prefill length (a reduced case for profiling; not a bench line)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
     from rank_latent_kv_gb300 import synth
     w = synth.WORKLOADS[args.workload]
+    if args.prefill:
+        w = synth.scaled(w, prefill=args.prefill)
     world, rank, local = dist_env()
 
     if args.impl == "reference":
