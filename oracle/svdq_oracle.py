@@ -162,6 +162,65 @@ class SvdqKeyCache:
         return float(np.mean([effective_bits(r, self.D, self.schedule) for r in self.ranks]))
 
 
+# --------------------------------------------------------------------------
+# Record layout of a 32-token block of one (batch, head) stream, as stored
+# by the GPU cache (a storage format of this build; the page fixes only the
+# widths and the LSB-first packing of sub-byte codes).  The kept channels
+# (width > 0) come first, each channel's 32 codes packed LSB-first at its
+# width (token t at bit t * b of the channel's 4 * b bytes), then one fp16
+# (scale, zero) pair per kept channel; the record is padded to 16 bytes.
+# --------------------------------------------------------------------------
+
+def record_layout(r: int, schedule=SCHEDULE):
+    """(bits [r], kept channels, code byte offset per kept channel,
+    byte offset of the scale/zero pairs, record bytes)."""
+    bits = channel_bits(r, schedule)
+    kept = int((bits > 0).sum())
+    ends = np.cumsum(4 * bits[:kept])
+    offs = np.concatenate([[0], ends[:-1]]).astype(np.int64) if kept else np.zeros(0, np.int64)
+    sz_off = int(ends[-1]) if kept else 0
+    return bits, kept, offs, sz_off, -(-(sz_off + 4 * kept) // 16) * 16
+
+
+def pack_record(codes: np.ndarray, s_h: np.ndarray, z_h: np.ndarray, r: int, stride: int,
+                schedule=SCHEDULE) -> np.ndarray:
+    """codes [32, r] uint8, scale/zero [r] fp16 -> one record of `stride` bytes."""
+    bits, kept, offs, sz_off, nbytes = record_layout(r, schedule)
+    assert stride >= nbytes
+    rec = np.zeros(stride, np.uint8)
+    for j in range(kept):
+        b = int(bits[j])
+        for t in range(BLOCK):
+            pos = t * b
+            val = int(codes[t, j]) << (pos % 8)
+            for k in range(-(-(pos % 8 + b) // 8)):
+                rec[offs[j] + pos // 8 + k] |= (val >> (8 * k)) & 0xFF
+    sz = np.stack([np.asarray(s_h, np.float16)[:kept], np.asarray(z_h, np.float16)[:kept]], axis=1)
+    rec[sz_off:sz_off + 4 * kept] = sz.view(np.uint8).reshape(-1)
+    return rec
+
+
+def unpack_record(rec: np.ndarray, r: int, schedule=SCHEDULE):
+    """One record -> codes [32, r] uint8, scale/zero [r] fp16 (0 for the
+    channels that are not stored)."""
+    bits, kept, offs, sz_off, _ = record_layout(r, schedule)
+    rec = np.asarray(rec, np.uint8)
+    codes = np.zeros((BLOCK, r), np.uint8)
+    for j in range(kept):
+        b = int(bits[j])
+        for t in range(BLOCK):
+            pos = t * b
+            word = 0
+            for k in range(-(-(pos % 8 + b) // 8)):
+                word |= int(rec[offs[j] + pos // 8 + k]) << (8 * k)
+            codes[t, j] = (word >> (pos % 8)) & ((1 << b) - 1)
+    sz = rec[sz_off:sz_off + 4 * kept].copy().view(np.float16).reshape(kept, 2)
+    s_h = np.zeros(r, np.float16)
+    z_h = np.zeros(r, np.float16)
+    s_h[:kept], z_h[:kept] = sz[:, 0], sz[:, 1]
+    return codes, s_h, z_h
+
+
 def svdq_attend(q: np.ndarray, kc: SvdqKeyCache, v: np.ndarray, scale: float | None = None,
                 fp16_keys: bool = False) -> np.ndarray:
     """Single-token decode attention, fp64: q [B, Hq, D], values v [B, H, S, D]

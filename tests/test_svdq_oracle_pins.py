@@ -211,3 +211,44 @@ def test_tail_holds_the_tokens_after_the_last_block():
         want = ((x[:, 0, nb * 32:].astype(np.float64) - mus[0].astype(np.float64))
                 @ bases[0].astype(np.float64)).astype(np.float32)
         assert np.array_equal(c.tail[0], want)
+
+
+def test_record_layout_hand_positions():
+    """r = 8: widths 8,4,2,1,1 kept (three 0-bit channels dropped); code bytes
+    32, 16, 8, 4, 4 at offsets 0, 32, 48, 56, 60; scale/zero pairs from byte
+    64; 84 bytes padded to 96.  Worked by hand: token 5 of the 4-bit channel
+    sits in the high nibble of byte 32 + 2; token 13 of the 2-bit channel in
+    bits 2-3 of byte 48 + 3; token 9 of the first 1-bit channel in bit 1 of
+    byte 56 + 1."""
+    bits, kept, offs, sz_off, nbytes = S.record_layout(8)
+    assert bits.tolist() == [8, 4, 2, 1, 1, 0, 0, 0] and kept == 5
+    assert offs.tolist() == [0, 32, 48, 56, 60] and sz_off == 64 and nbytes == 96
+    codes = np.zeros((32, 8), np.uint8)
+    codes[5, 1] = 0xB
+    codes[13, 2] = 0x2
+    codes[9, 3] = 1
+    codes[31, 0] = 0xA7
+    s_h = np.arange(1, 9).astype(np.float16)
+    z_h = -np.arange(1, 9).astype(np.float16)
+    rec = S.pack_record(codes, s_h, z_h, 8, 96)
+    assert rec[32 + 2] == 0xB0 and rec[48 + 3] == 0x08 and rec[56 + 1] == 0x02 and rec[31] == 0xA7
+    assert rec[np.r_[0:31, 33, 35:48, 49:51, 52:56, 56, 58:64]].sum() == 0
+    assert rec[64:68].view(np.float16).tolist() == [1.0, -1.0]       # channel 0: scale, zero
+    assert rec[80:84].view(np.float16).tolist() == [5.0, -5.0]       # channel 4
+    assert (rec[84:] == 0).all()
+
+
+def test_record_round_trip_at_every_width():
+    rng = np.random.default_rng(5)
+    for r in (1, 3, 8, 10, 27, 74, 128):
+        bits, kept, _, _, nbytes = S.record_layout(r)
+        codes = np.zeros((32, r), np.uint8)
+        for j in range(kept):
+            codes[:, j] = rng.integers(0, 2 ** int(bits[j]), size=32)
+        s_h = rng.standard_normal(r).astype(np.float16)
+        z_h = rng.standard_normal(r).astype(np.float16)
+        s_h[kept:] = 0
+        z_h[kept:] = 0
+        c2, s2, z2 = S.unpack_record(S.pack_record(codes, s_h, z_h, r, nbytes + 16), r)
+        assert np.array_equal(c2, codes) and np.array_equal(s2.view(np.uint16), s_h.view(np.uint16))
+        assert np.array_equal(z2.view(np.uint16), z_h.view(np.uint16))
