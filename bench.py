@@ -447,6 +447,7 @@ def run_palu(args, w, world, rank, local):
     if not args.no_comparator:
         comp = run_comparator(P, w, s, L, int(round(s_ctx)), dev, world)
         comp_kivi = run_kivi_comparator(P, w, s, L, int(round(s_ctx)), dev, world)
+        comp_svdq = run_svdq_comparator(P, w, s, L, int(round(s_ctx)), dev, world)
 
     stats_k, stats_v = kc0.stats(), vc0.stats()
     # traffic: DRAM bytes of the profiled launch (one layer); beside it that
@@ -491,6 +492,7 @@ def run_palu(args, w, world, rank, local):
     if comp is not None:
         result["comparator"] = comp
         result["comparator_kivi"] = comp_kivi
+        result["comparator_svdq"] = comp_svdq
     return result
 
 
@@ -662,6 +664,71 @@ def run_kivi_comparator(P, w, s, L, s_ctx, dev, world, steps=20):
             "value": whole_job_rate(world * w.batch * s_ctx * L, ms / 1e3), "unit": UNIT, "ms_per_step": ms,
             "achieved_gbs": bytes_step / (ms / 1e3) / 1e9, "bytes_per_step": bytes_step,
             "bits_per_element_with_meta": 3.0, "gpu_launches_per_step": 2 * L}
+
+
+SVDQ_SCHEDULE = (8, 4, 2, 1, 1, 0, 0, 0)
+
+
+def _svdq_widths(r):
+    """Widths of an SVDq head's r channels: the schedule over equal contiguous
+    channel groups, larger groups first."""
+    return [b for g, b in enumerate(SVDQ_SCHEDULE) for _ in range(r // 8 + (1 if g < r % 8 else 0))]
+
+
+def run_svdq_comparator(P, w, s, L, s_ctx, dev, world, steps=20):
+    """The SVDq keys-only cache (per-head bases at the energy threshold 0.95,
+    bit schedule 8,4,2,1,1,0,0,0; fp16 values) on the same shapes and
+    context: keys from the workload's generator, per-head fit, one prefill
+    append per layer, decode attention timed in a graph of all layers."""
+    from rank_latent_kv_gb300 import synth
+    caches, values, ranks_all = [], [], []
+    cfg = P.palu_config_default(n_head_groups=w.hkv, rank=0, energy_threshold=0.95)
+    for l in range(L):
+        k = synth.prefill(w, l, 0, device=dev, tokens=s_ctx)
+        basis, mu, _, _, ranks = P.fit(cfg, k)
+        c = P.SvdqCache(w.batch, w.hkv, ranks, s_ctx, basis, mu)
+        c.append(k)
+        del k, basis, mu
+        caches.append(c)
+        ranks_all.append(list(ranks))
+        values.append(torch.randn(w.batch, w.hkv, s_ctx, 128, dtype=torch.float16, device=dev))
+    torch.cuda.synchronize()
+    q, _, _ = synth.decode_inputs(w, 0, 0, device=dev, n_steps=1)
+    q = q[0]
+    out = torch.empty(w.batch, w.hq, 128, dtype=torch.float16, device=dev)
+    import ctypes
+    need = 256
+    for c in caches:  # the workspace follows each layer's largest rank
+        n = ctypes.c_size_t()
+        P._check(P.lib().palu_svdq_decode_workspace_size(ctypes.byref(c.c), w.hq, ctypes.byref(n)))
+        need = max(need, int(n.value))
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+
+    def calls():
+        for c, v in zip(caches, values):
+            c.decode(v, q, stream=s, workspace=ws, out=out)
+
+    ms = _time_graph(calls, s, steps, world, dev)
+    nf, nt = s_ctx // 32, s_ctx % 32
+    # algorithmic bytes: key codes and scale/zero of the kept channels of full
+    # blocks, the fp32 tail latents, the fp16 values, q and out
+    bytes_step = 0.0
+    for rk in ranks_all:
+        for r in rk:
+            wd = _svdq_widths(r)
+            kept = sum(1 for b in wd if b)
+            bytes_step += w.batch * (nf * 32 * sum(wd) / 8 + nf * 4 * kept + nt * r * 4 + s_ctx * 256)
+    bytes_step += L * w.batch * w.hq * 128 * 4
+    del caches, values
+    torch.cuda.empty_cache()
+    flat = [r for rk in ranks_all for r in rk]
+    return {"what": "SVDq keys-only cache (per-head ranks at energy 0.95, bit schedule 8,4,2,1,1,0,0,0, fp32 "
+                    "scores from the codes) with fp16 values, same shapes and context",
+            "value": whole_job_rate(world * w.batch * s_ctx * L, ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+            "achieved_gbs": bytes_step / (ms / 1e3) / 1e9, "bytes_per_step": bytes_step,
+            "key_ranks_min_mean_max": [min(flat), sum(flat) / len(flat), max(flat)],
+            "key_bits_per_element": sum(sum(_svdq_widths(r)) for r in flat) / (128.0 * len(flat)),
+            "gpu_launches_per_step": 3 * L}
 
 
 # ------------------------------------------------------------------ main

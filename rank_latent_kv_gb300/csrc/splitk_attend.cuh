@@ -57,26 +57,12 @@ __device__ __forceinline__ void split_load_q(uint32_t qb[8][2], const __half* qh
   }
 }
 
-// One warp's 16 tokens (rows r0 .. r0+15 of the tile at kst / vst; token
-// index of row r0 is tok0): scores, mask of tokens >= t1, online softmax and
-// the weighted sum of the V rows.  Rows past t1 must hold finite values.
-__device__ __forceinline__ void split_tile(SplitState& st, const uint32_t qb[8][2], uint32_t kst, uint32_t vst,
-                                           int r0, int lane, long long tok0, long long t1, float scale_log2) {
-  const int g = lane >> 2, mat = lane >> 3, rr = lane & 7;
-  float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    // A = K rows (tokens x d): matrices (t0-7,d0-7), (t8-15,d0-7), (t0-7,d8-15), (t8-15,d8-15)
-    uint32_t a0, a1, a2, a3;
-    ldsm_x4(a0, a1, a2, a3, swz(kst, r0 + rr + ((mat & 1) << 3), 2 * ks + (mat >> 1)));
-    mma_f16(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-  }
-  // mask tokens past the end, scale to base 2
-  const bool v0 = tok0 + g < t1, v1 = tok0 + g + 8 < t1;
-  sc[0] = v0 ? sc[0] * scale_log2 : -INFINITY;
-  sc[1] = v0 ? sc[1] * scale_log2 : -INFINITY;
-  sc[2] = v1 ? sc[2] * scale_log2 : -INFINITY;
-  sc[3] = v1 ? sc[3] * scale_log2 : -INFINITY;
+// The online softmax and weighted sum of one warp's 16 tokens, given their
+// scores in base-2 units (sc[0..1]: token r0 + g, heads 2c and 2c+1;
+// sc[2..3]: token r0 + g + 8; -inf for tokens that do not count).  The V rows
+// of the tile at vst must be finite.
+__device__ __forceinline__ void split_softmax_pv(SplitState& st, float sc[4], uint32_t vst, int r0, int lane) {
+  const int mat = lane >> 3, rr = lane & 7;
   float bm0 = fmaxf(sc[0], sc[2]), bm1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
   for (int x = 4; x < 32; x <<= 1) {
@@ -110,6 +96,29 @@ __device__ __forceinline__ void split_tile(SplitState& st, const uint32_t qb[8][
       mma_f16(st.acc[mt], a0, a1, a2, a3, b0, b1);
     }
   }
+}
+
+// One warp's 16 tokens (rows r0 .. r0+15 of the tile at kst / vst; token
+// index of row r0 is tok0): scores, mask of tokens >= t1, online softmax and
+// the weighted sum of the V rows.  Rows past t1 must hold finite values.
+__device__ __forceinline__ void split_tile(SplitState& st, const uint32_t qb[8][2], uint32_t kst, uint32_t vst,
+                                           int r0, int lane, long long tok0, long long t1, float scale_log2) {
+  const int g = lane >> 2, mat = lane >> 3, rr = lane & 7;
+  float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    // A = K rows (tokens x d): matrices (t0-7,d0-7), (t8-15,d0-7), (t0-7,d8-15), (t8-15,d8-15)
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4(a0, a1, a2, a3, swz(kst, r0 + rr + ((mat & 1) << 3), 2 * ks + (mat >> 1)));
+    mma_f16(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+  }
+  // mask tokens past the end, scale to base 2
+  const bool v0 = tok0 + g < t1, v1 = tok0 + g + 8 < t1;
+  sc[0] = v0 ? sc[0] * scale_log2 : -INFINITY;
+  sc[1] = v0 ? sc[1] * scale_log2 : -INFINITY;
+  sc[2] = v1 ? sc[2] * scale_log2 : -INFINITY;
+  sc[3] = v1 ? sc[3] * scale_log2 : -INFINITY;
+  split_softmax_pv(st, sc, vst, r0, lane);
 }
 
 // Merge the warps' states (fixed warp order) and write the CTA's partial

@@ -57,6 +57,12 @@ class palu_kivi_cache(ctypes.Structure):
                 ("length", c_int64)]
 
 
+class palu_svdq_cache(ctypes.Structure):
+    _fields_ = [("magic", c_int32), ("batch", c_int32), ("kv_heads", c_int32), ("r_max", c_int32),
+                ("record_bytes", c_int32), ("pad0", c_int32), ("capacity", c_int64), ("n_blk_cap", c_int64),
+                ("blocks", c_void_p), ("tail", c_void_p), ("state", c_void_p), ("length", c_int64)]
+
+
 _P = POINTER
 _SIGNATURES = {
     "palu_last_error": (ctypes.c_char_p, []),
@@ -87,6 +93,15 @@ _SIGNATURES = {
     "palu_encode_append_ragged": (c_int32, [_P(palu_cache), c_void_p, c_int64, c_void_p, c_void_p]),
     "palu_cache_truncate_ragged": (c_int32, [_P(palu_cache), c_void_p, c_void_p]),
     "palu_cache_lengths": (c_int32, [_P(palu_cache), _P(c_int64), c_void_p]),
+    "palu_svdq_cache_size": (c_int32, [c_int64, c_int32, _P(c_int32), c_int64, _P(c_size_t), _P(c_size_t),
+                                       _P(c_size_t)]),
+    "palu_svdq_cache_init": (c_int32, [_P(palu_svdq_cache), c_int64, c_int32, _P(c_int32), c_int64, c_void_p, c_int32,
+                                       c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "palu_svdq_append": (c_int32, [_P(palu_svdq_cache), c_void_p, c_int64, c_void_p]),
+    "palu_svdq_decode_workspace_size": (c_int32, [_P(palu_svdq_cache), c_int32, _P(c_size_t)]),
+    "palu_svdq_decode_attn": (c_int32, [_P(palu_svdq_cache), c_void_p, c_int64, c_void_p, c_int32, c_float, c_void_p,
+                                        c_int32, c_void_p, c_size_t, c_void_p]),
+    "palu_svdq_sync": (c_int32, [_P(palu_svdq_cache), _P(c_uint32), c_void_p]),
     "palu_fp16_decode_workspace_size": (c_int32, [c_int64, c_int32, c_int64, c_int32, _P(c_size_t)]),
     "palu_fp16_decode_attn": (c_int32, [c_void_p, c_void_p, c_int64, c_int32, c_int64, c_int64, c_void_p, c_int32,
                                         c_float, c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
@@ -431,6 +446,65 @@ class KiviCache:
         c = self.c
         n = c.batch * c.kv_heads * 2 * 32 * 128 * 2
         return self.window[:n].cpu().numpy().view("float16").reshape(c.batch, c.kv_heads, 2, 32, 128)
+
+
+class SvdqCache:
+    """An SVDq keys-only cache of one layer (include/svdq.h) with torch-allocated buffers.
+    ranks: per-head ranks; basis fp32 [Hkv, D, ld] and mu [Hkv, D] on the device (palu_fit with one head per group)."""
+
+    def __init__(self, batch, kv_heads, ranks, capacity, basis, mu, stream=None):
+        dev = basis.device
+        rk = (c_int32 * kv_heads)(*[int(r) for r in ranks])
+        bb, tb, sb = c_size_t(), c_size_t(), c_size_t()
+        _check(lib().palu_svdq_cache_size(batch, kv_heads, rk, capacity, ctypes.byref(bb), ctypes.byref(tb),
+                                          ctypes.byref(sb)))
+        self.blocks = _dev_bytes(bb.value, dev)
+        self.tail = _dev_bytes(tb.value, dev)
+        self.state = _dev_bytes(sb.value, dev)
+        self.ranks = [int(r) for r in ranks]
+        self.c = palu_svdq_cache()
+        _check(lib().palu_svdq_cache_init(ctypes.byref(self.c), batch, kv_heads, rk, capacity, _ptr(basis),
+                                          basis.shape[-1], _ptr(mu), _ptr(self.blocks), _ptr(self.tail),
+                                          _ptr(self.state), _stream(stream)))
+
+    @property
+    def length(self):
+        return self.c.length
+
+    def append(self, k, stream=None):
+        """k fp16 [B, Hkv, T, D] on the device."""
+        assert k.is_cuda and k.dtype == torch.float16 and k.is_contiguous()
+        _check(lib().palu_svdq_append(ctypes.byref(self.c), _ptr(k), k.shape[2], _stream(stream)))
+
+    def decode(self, v, q, out_dtype=torch.float32, softmax_scale=0.0, stream=None, workspace=None, out=None):
+        """v fp16 [B, Hkv, v_cap, D] (tokens 0..length-1 used), q fp16 [B, Hq, D]; returns out [B, Hq, D]."""
+        if workspace is None:
+            n = c_size_t()
+            _check(lib().palu_svdq_decode_workspace_size(ctypes.byref(self.c), q.shape[1], ctypes.byref(n)))
+            workspace = _dev_bytes(n.value, q.device)
+        if out is None:
+            out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+        _check(lib().palu_svdq_decode_attn(ctypes.byref(self.c), _ptr(v), v.shape[2], _ptr(q), q.shape[1],
+                                           c_float(softmax_scale), _ptr(out), 1 if out.dtype == torch.float32 else 0,
+                                           _ptr(workspace), workspace.numel(), _stream(stream)))
+        return out
+
+    def sync(self, stream=None):
+        e = c_uint32()
+        _check(lib().palu_svdq_sync(ctypes.byref(self.c), ctypes.byref(e), _stream(stream)))
+        return e.value
+
+    def record_array(self):
+        """Block records as a host uint8 array [B, Hkv, n_blk_cap, record_bytes]."""
+        c = self.c
+        n = c.batch * c.kv_heads * c.n_blk_cap * c.record_bytes
+        return self.blocks[:n].cpu().numpy().reshape(c.batch, c.kv_heads, c.n_blk_cap, c.record_bytes)
+
+    def tail_array(self):
+        """The fp32 tail latents [B, Hkv, 32, r_max] (host)."""
+        c = self.c
+        n = c.batch * c.kv_heads * 32 * c.r_max * 4
+        return self.tail[:n].cpu().numpy().view("float32").reshape(c.batch, c.kv_heads, 32, c.r_max)
 
 
 def fit(cfg, x, stream=None):
