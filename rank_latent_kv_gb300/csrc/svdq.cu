@@ -367,29 +367,66 @@ __global__ void __launch_bounds__(128) svdq_qprep_kernel(const SvdqDecParams p) 
 }
 
 constexpr int kSvdqStages = 3;
+constexpr int kSvdqRecSlack = 1024;  // bytes past the last staged record (see svdq_codes_frag)
 struct SvdqDecSmem {
-  int vst, kst, lat, scs, qts, tab, total, ls;
+  int vst, kst, qts, total;
 };
 __host__ __device__ inline SvdqDecSmem svdq_dec_smem(int r_max, int rec_bytes) {
   SvdqDecSmem s;
-  s.ls = r_max | 1;                                              // latent row stride (odd: conflict-free)
-  s.vst = 0;                                                     // V tiles [stages][64][D] fp16, swizzled
-  s.kst = s.vst + kSvdqStages * kSplitTileBytes;                 // key records [stages][2][rec]
-  s.lat = s.kst + kSvdqStages * 2 * rec_bytes;                   // latents [64][ls] fp32
-  s.scs = s.lat + svdq_a16(4 * kSplitTile * s.ls);               // scores [64][8]
-  s.qts = s.scs + 4 * kSplitTile * 8;                            // q~ [r_max][8] (channel-major) and c [8]
-  s.tab = s.qts + svdq_a16(4 * (8 * r_max + 8));                 // code offsets, widths [2][r_max]
-  s.total = s.tab + svdq_a16(8 * r_max);
+  s.vst = 0;                                                            // V tiles [stages][64][D] fp16, swizzled
+  s.kst = s.vst + kSvdqStages * kSplitTileBytes;                        // key records [stages][2][rec] + slack
+  s.qts = s.kst + svdq_a16(kSvdqStages * 2 * rec_bytes + kSvdqRecSlack);  // q~ [8][r_max] and c [8]
+  s.total = s.qts + svdq_a16(4 * (8 * r_max + 8));
   return s;
 }
 
+// The A fragment of one k-step (16 channels of one width W, tokens of one
+// warp's 16-row slice) as exact fp16 codes.  The k-step's channel k holds its
+// 32 codes in W words, token t at bit t*W; lane (g, c) needs channels 2c, 2c+1
+// (registers 0, 1) and 2c+8, 2c+9 (registers 2, 3) of tokens tb0 = 16h + g and
+// tb0 + 8.  A byte permute gathers the two channels' bytes that hold a token's
+// code into the low bytes of the two halves; the lane's bit mask keeps the
+// code, ORed into the fp16 pattern of 1024 (code at mantissa bit o); one
+// fp16x2 FMA by 2^-o with addend -1024 * 2^-o gives the code itself (every
+// step exact).  cw: the words of channel 2c of the k-step.  Lanes whose
+// channels lie past the class read codes of later channels or of the next
+// record (finite, and multiplied by a zero B operand).
+template <int W>
+__device__ __forceinline__ void svdq_codes_frag(const uint32_t* cw, int tb0, uint32_t a[4]) {
+  const int pos0 = tb0 * W, pos1 = pos0 + 8 * W;
+  const int wi0 = pos0 >> 5, wi1 = pos1 >> 5;
+  const uint32_t bs0 = (uint32_t)(pos0 & 31) >> 3, bs1 = (uint32_t)(pos1 & 31) >> 3;
+  const int o = pos0 & 7;
+  const uint32_t sel0 = bs0 | ((bs0 + 4u) << 8), sel1 = bs1 | ((bs1 + 4u) << 8);
+  const uint32_t m = ((1u << W) - 1u) << o, M = m | (m << 16);
+  const uint32_t mul = (uint32_t)(15 - o) << 10, add = 0x8000u | ((uint32_t)(25 - o) << 10);
+  const uint32_t mul2 = mul | (mul << 16), add2 = add | (add << 16);
+  a[0] = __byte_perm(cw[wi0], cw[W + wi0], sel0);
+  a[1] = __byte_perm(cw[wi1], cw[W + wi1], sel1);
+  a[2] = __byte_perm(cw[8 * W + wi0], cw[9 * W + wi0], sel0);
+  a[3] = __byte_perm(cw[8 * W + wi1], cw[9 * W + wi1], sel1);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) a[i] = fma_f16x2((a[i] & M) | 0x64006400u, mul2, add2);
+}
+
+__device__ __forceinline__ float pow2f_(int e) { return __int_as_float((e + 127) << 23); }
+
+// k-step ks of a head: width class (8, 4, 2, 1, 1) and channel offsets within
+// the 16-channel step of lane c (k = 0..3: 2c, 2c+1, 2c+8, 2c+9).
+__host__ __device__ constexpr int svdq_ks_width(int ks) { return ks == 0 ? 8 : ks == 1 ? 4 : ks == 2 ? 2 : 1; }
+__device__ __forceinline__ int svdq_kk(int k) { return (k & 1) + ((k >> 1) << 3); }
+
 // grid (chunks, kv_heads, batch), 4 warps: each CTA a contiguous chunk of
 // 64-token tiles of one stream.  Per tile: the value rows and the key
-// records by cp.async into a 3-stage ring; the key latents of the tile's 64
-// tokens dequantized in fp32 (code * scale + zero, 0 for the channels the
-// schedule drops; fp32 latents for the partial block's tokens); the scores
-// q~ . L_t + c in fp32; then the online softmax and the weighted sum of the
-// value rows on the tensor cores (the comparator's loop).
+// records by cp.async into a 3-stage ring; each warp takes 16 tokens (half a
+// 32-token block).  Scores of a quantized block on the tensor cores:
+//   q~ . L_t + c = sum_j code_tj (q~_j s_j) + (c + sum_j q~_j z_j)
+// with the codes as exact fp16 A operands (one k-step per width class of
+// the schedule) and q~_j s_j as an fp16 hi + lo pair prescaled by a power of
+// two (the block's largest |q~_j s_j| near 2^14), fp32 accumulation; the
+// partial block's tokens from their fp32 latents on the CUDA cores.  Then
+// the online softmax and the weighted sum of the value rows on the tensor
+// cores (the comparator's loop).
 __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const SvdqDecParams p) {
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ float merge[kSplitWarps][8][kSplitPartStride];
@@ -397,14 +434,10 @@ __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const Svd
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int H = p.k.H, rm = p.k.r_max, Gq = p.Gq, rb = p.k.rec_bytes;
   const long long X = (long long)b * H + h;
-  const int r = p.k.head[4 * h], kept = p.k.head[4 * h + 1], szo = p.k.head[4 * h + 2];
+  const int r = p.k.head[4 * h], szo = p.k.head[4 * h + 2];
   const SvdqDecSmem L = svdq_dec_smem(rm, rb);
-  float* lat = reinterpret_cast<float*>(dsm + L.lat);
-  float* scs = reinterpret_cast<float*>(dsm + L.scs);
   float* qts = reinterpret_cast<float*>(dsm + L.qts);
   float* cqs = qts + 8 * rm;
-  int* coffs = reinterpret_cast<int*>(dsm + L.tab);
-  int* bits_s = coffs + rm;
   const long long t0 = (long long)chunk * p.tiles_per_chunk * kSplitTile;
   const long long t1 = min(t0 + (long long)p.tiles_per_chunk * kSplitTile, p.len);
   float* part = p.ws + ((long long)X * p.n_chunks + chunk) * (long long)Gq * kSplitPartStride;
@@ -419,16 +452,26 @@ __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const Svd
   const float* tail = p.k.tail + X * kBlock * rm;
   const uint32_t sbase = smem_addr(dsm);
 
-  // q~ channel-major in shared memory ([j][8]): a thread's four heads in one 128-bit load
-  for (int i = tid; i < 8 * rm; i += blockDim.x) {
-    const int hq = i / rm, j = i - hq * rm;
-    qts[j * 8 + hq] = __ldg(p.qt + (size_t)X * 8 * rm + i);
-  }
+  for (int i = tid; i < 8 * rm; i += blockDim.x) qts[i] = __ldg(p.qt + (size_t)X * 8 * rm + i);
   if (tid < 8) cqs[tid] = __ldg(p.cq + (size_t)X * 8 + tid);
-  for (int j = tid; j < rm; j += blockDim.x) {
-    coffs[j] = __ldg(p.k.coff + (size_t)h * rm + j);
-    bits_s[j] = __ldg(p.k.cbits + (size_t)h * rm + j);
-  }
+
+  // the head's width classes: group sizes r/8 (+1 for the first r%8 groups)
+  const int n8 = r / 8 + (0 < r % 8), n4 = r / 8 + (1 < r % 8), n2 = r / 8 + (2 < r % 8);
+  const int n1 = 2 * (r / 8) + (3 < r % 8) + (4 < r % 8);
+  const int ksn[5] = {n8, n4, n2, min(n1, 16), max(n1 - 16, 0)};
+  const int ksf[5] = {0, n8, n8 + n4, n8 + n4 + n2, n8 + n4 + n2 + 16};
+  const int ksb[5] = {0, 32 * n8, 32 * n8 + 16 * n4, 32 * n8 + 16 * n4 + 8 * n2, 32 * n8 + 16 * n4 + 8 * n2 + 64};
+  // lane's q~ of head g at its channels of each k-step (0 past the class)
+  float qv[5][4];
+#pragma unroll
+  for (int ks = 0; ks < 5; ++ks)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int jj = 2 * c + svdq_kk(k);
+      qv[ks][k] = jj < ksn[ks] ? __ldg(p.qt + ((size_t)X * 8 + g) * rm + ksf[ks] + jj) : 0.f;
+    }
+  const float cq_g = __ldg(p.cq + (size_t)X * 8 + g);
+  const int tb0 = 16 * (warp & 1) + g;
 
   auto load_tile = [&](int tile, int stage) {
     const long long tt = t0 + (long long)tile * kSplitTile;
@@ -463,6 +506,7 @@ __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const Svd
   }
   SplitState st;
   split_init(st);
+  const int r0 = 16 * warp;
   for (int tile = 0; tile < n_tiles; ++tile) {
     cp_async_wait<kSvdqStages - 2>();
     __syncthreads();
@@ -471,60 +515,83 @@ __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const Svd
     cp_async_commit();
     const int stage = tile % kSvdqStages;
     const long long tt = t0 + (long long)tile * kSplitTile;
-    const uint8_t* krec = dsm + L.kst + stage * 2 * rb;
-    // key latents of the tile's tokens: thread (token t, channels of one parity)
-    const int t = tid & (kSplitTile - 1), jp = tid >> 6;
-    const long long tok = tt + t;
-    {
-      float* lr = lat + t * L.ls;
-      if (tok >= t1) {
-        for (int j = jp; j < r; j += 2) lr[j] = 0.f;
-      } else if (tok / kBlock < nf) {
-        const uint8_t* rec = krec + (t >> 5) * rb;
-        const __half2* szr = reinterpret_cast<const __half2*>(rec + szo);
-        const int tb = t & 31;
-        for (int j = jp; j < r; j += 2) {
-          float val = 0.f;
-          if (j < kept) {
-            const int wb = bits_s[j], pos = tb * wb;
-            const uint32_t word = reinterpret_cast<const uint32_t*>(rec + coffs[j])[pos >> 5];
-            const uint32_t code = (word >> (pos & 31)) & ((1u << wb) - 1u);
-            const __half2 szv = szr[j];
-            val = fmaf((float)code, __low2float(szv), __high2float(szv));
-          }
-          lr[j] = val;
+    const long long ta = tt + r0 + g, tb = ta + 8;  // this lane's two tokens
+    float sc[4];
+    if (tt / kBlock + (warp >> 1) < nf) {
+      // quantized block: B = q~_j s_j (hi + lo), A = codes
+      const uint8_t* rec = dsm + L.kst + (stage * 2 + (warp >> 1)) * rb;
+      const __half2* szr = reinterpret_cast<const __half2*>(rec + szo);
+      float av[5][4];
+      float mx = 0.f, cst = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 5; ++ks)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int jj = 2 * c + svdq_kk(k);
+          float2 sz = make_float2(0.f, 0.f);
+          if (jj < ksn[ks]) sz = __half22float2(szr[ksf[ks] + jj]);
+          av[ks][k] = qv[ks][k] * sz.x;
+          cst = fmaf(qv[ks][k], sz.y, cst);
+          mx = fmaxf(mx, fabsf(av[ks][k]));
         }
-      } else {
-        const float* tr = tail + (tok % kBlock) * rm;
-        for (int j = jp; j < r; j += 2) lr[j] = __ldcg(tr + j);
+#pragma unroll
+      for (int x = 1; x < 4; x <<= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, x));
+        cst += __shfl_xor_sync(0xffffffffu, cst, x);
       }
-    }
-    __syncthreads();
-    // scores: thread (token t, query heads 4 jp .. 4 jp + 3)
-    {
-      const int h0 = jp * 4;
-      float acc0 = cqs[h0], acc1 = cqs[h0 + 1], acc2 = cqs[h0 + 2], acc3 = cqs[h0 + 3];
-      const float* lr = lat + t * L.ls;
+      const int e = min(141 - (int)((__float_as_uint(mx) >> 23) & 0xffu), 126);  // max|B| in [2^14, 2^15)
+      const float S = pow2f_(e), invS = pow2f_(-e);
+      sc[0] = sc[1] = sc[2] = sc[3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 5; ++ks) {
+        if (ksn[ks] == 0) continue;  // uniform
+        constexpr int kW[5] = {8, 4, 2, 1, 1};
+        uint32_t a[4];
+        const uint32_t* cw = reinterpret_cast<const uint32_t*>(rec + ksb[ks]) + 2 * c * kW[ks];
+        if (ks == 0) svdq_codes_frag<8>(cw, tb0, a);
+        else if (ks == 1) svdq_codes_frag<4>(cw, tb0, a);
+        else if (ks == 2) svdq_codes_frag<2>(cw, tb0, a);
+        else svdq_codes_frag<1>(cw, tb0, a);
+        const float x0 = av[ks][0] * S, x1 = av[ks][1] * S, x8 = av[ks][2] * S, x9 = av[ks][3] * S;
+        const uint32_t h01 = pack_f16x2(x0, x1), h89 = pack_f16x2(x8, x9);
+        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+        const float2 f89 = __half22float2(*reinterpret_cast<const __half2*>(&h89));
+        const uint32_t l01 = pack_f16x2(x0 - f01.x, x1 - f01.y), l89 = pack_f16x2(x8 - f89.x, x9 - f89.y);
+        mma_f16(sc, a[0], a[1], a[2], a[3], h01, h89);
+        mma_f16(sc, a[0], a[1], a[2], a[3], l01, l89);
+      }
+      // heads 2c, 2c+1: their scale and constant from lanes 8c and 8c+4
+      const float cfull = cst + cq_g;
+      const float iA = __shfl_sync(0xffffffffu, invS, 8 * c), iB = __shfl_sync(0xffffffffu, invS, 8 * c + 4);
+      const float cA = __shfl_sync(0xffffffffu, cfull, 8 * c), cB = __shfl_sync(0xffffffffu, cfull, 8 * c + 4);
+      sc[0] = fmaf(sc[0], iA, cA);
+      sc[1] = fmaf(sc[1], iB, cB);
+      sc[2] = fmaf(sc[2], iA, cA);
+      sc[3] = fmaf(sc[3], iB, cB);
+    } else {
+      // the partial block (or past the end): fp32 latents
+      const float* la = tail + (ta < t1 ? (ta % kBlock) : 0) * rm;
+      const float* lb = tail + (tb < t1 ? (tb % kBlock) : 0) * rm;
+      const float* qa = qts + (2 * c) * rm;
+      const float* qb = qa + rm;
+      float s00 = cqs[2 * c], s01 = cqs[2 * c + 1], s10 = s00, s11 = s01;
       for (int j = 0; j < r; ++j) {
-        const float l = lr[j];
-        const float4 q4 = *reinterpret_cast<const float4*>(qts + j * 8 + h0);
-        acc0 = fmaf(q4.x, l, acc0);
-        acc1 = fmaf(q4.y, l, acc1);
-        acc2 = fmaf(q4.z, l, acc2);
-        acc3 = fmaf(q4.w, l, acc3);
+        const float x = __ldcg(la + j), y = __ldcg(lb + j), u = qa[j], w = qb[j];
+        s00 = fmaf(u, x, s00);
+        s01 = fmaf(w, x, s01);
+        s10 = fmaf(u, y, s10);
+        s11 = fmaf(w, y, s11);
       }
-      const bool valid = tok < t1;
-      float4 o;
-      o.x = valid ? acc0 * p.scale_log2 : -INFINITY;
-      o.y = valid ? acc1 * p.scale_log2 : -INFINITY;
-      o.z = valid ? acc2 * p.scale_log2 : -INFINITY;
-      o.w = valid ? acc3 * p.scale_log2 : -INFINITY;
-      *reinterpret_cast<float4*>(scs + t * 8 + h0) = o;
+      sc[0] = s00;
+      sc[1] = s01;
+      sc[2] = s10;
+      sc[3] = s11;
     }
-    __syncthreads();
-    const int r0 = 16 * warp;
-    float sc[4] = {scs[(r0 + g) * 8 + 2 * c], scs[(r0 + g) * 8 + 2 * c + 1], scs[(r0 + g + 8) * 8 + 2 * c],
-                   scs[(r0 + g + 8) * 8 + 2 * c + 1]};
+    const bool va = ta < t1, vbv = tb < t1;
+    sc[0] = va ? sc[0] * p.scale_log2 : -INFINITY;
+    sc[1] = va ? sc[1] * p.scale_log2 : -INFINITY;
+    sc[2] = vbv ? sc[2] * p.scale_log2 : -INFINITY;
+    sc[3] = vbv ? sc[3] * p.scale_log2 : -INFINITY;
     split_softmax_pv(st, sc, sbase + L.vst + stage * kSplitTileBytes, r0, lane);
   }
   cp_async_wait<0>();
