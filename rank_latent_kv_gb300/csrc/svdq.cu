@@ -366,31 +366,35 @@ __global__ void __launch_bounds__(128) svdq_qprep_kernel(const SvdqDecParams p) 
   }
 }
 
-constexpr int kSvdqStages = 3;
+constexpr int kSvdqTile = 128;                           // tokens per tile: one 32-token block per warp
+constexpr int kSvdqTileBytes = kSvdqTile * kHeadDim * 2;  // 32 KB of values
+constexpr int kSvdqStages = 2;
 constexpr int kSvdqRecSlack = 1024;  // bytes past the last staged record (see svdq_codes_frag)
+static_assert(sizeof(float) * kSplitWarps * 8 * kSplitPartStride <= kSvdqTileBytes,
+              "the end-of-chunk merge scratch fits in one value stage");
 struct SvdqDecSmem {
   int vst, kst, qts, total;
 };
 __host__ __device__ inline SvdqDecSmem svdq_dec_smem(int r_max, int rec_bytes) {
   SvdqDecSmem s;
-  s.vst = 0;                                                            // V tiles [stages][64][D] fp16, swizzled
-  s.kst = s.vst + kSvdqStages * kSplitTileBytes;                        // key records [stages][2][rec] + slack
-  s.qts = s.kst + svdq_a16(kSvdqStages * 2 * rec_bytes + kSvdqRecSlack);  // q~ [8][r_max] and c [8]
+  s.vst = 0;                                                            // V tiles [stages][128][D] fp16, swizzled
+  s.kst = s.vst + kSvdqStages * kSvdqTileBytes;                         // key records [stages][4][rec] + slack
+  s.qts = s.kst + svdq_a16(kSvdqStages * 4 * rec_bytes + kSvdqRecSlack);  // q~ [8][r_max] and c [8]
   s.total = s.qts + svdq_a16(4 * (8 * r_max + 8));
   return s;
 }
 
 // The A fragment of one k-step (16 channels of one width W, tokens of one
-// warp's 16-row slice) as exact fp16 codes.  The k-step's channel k holds its
-// 32 codes in W words, token t at bit t*W; lane (g, c) needs channels 2c, 2c+1
-// (registers 0, 1) and 2c+8, 2c+9 (registers 2, 3) of tokens tb0 = 16h + g and
-// tb0 + 8.  A byte permute gathers the two channels' bytes that hold a token's
-// code into the low bytes of the two halves; the lane's bit mask keeps the
-// code, ORed into the fp16 pattern of 1024 (code at mantissa bit o); one
-// fp16x2 FMA by 2^-o with addend -1024 * 2^-o gives the code itself (every
-// step exact).  cw: the words of channel 2c of the k-step.  Lanes whose
-// channels lie past the class read codes of later channels or of the next
-// record (finite, and multiplied by a zero B operand).
+// 16-row slice of a block) as exact fp16 codes.  The k-step's channel k holds
+// its 32 codes in W words, token t at bit t*W; lane (g, c) needs channels 2c,
+// 2c+1 (registers 0, 1) and 2c+8, 2c+9 (registers 2, 3) of tokens tb0 (16h+g)
+// and tb0 + 8.  A byte permute gathers the two channels' bytes that hold a
+// token's code into the low bytes of the two halves; the lane's bit mask
+// keeps the code, ORed into the fp16 pattern of 1024 (code at mantissa bit
+// o); one fp16x2 FMA by 2^-o with addend -1024 * 2^-o gives the code itself
+// (every step exact).  cw: the words of channel 2c of the k-step.  Lanes
+// whose channels lie past the class read codes of later channels or of the
+// next record (finite, and multiplied by a zero B operand).
 template <int W>
 __device__ __forceinline__ void svdq_codes_frag(const uint32_t* cw, int tb0, uint32_t a[4]) {
   const int pos0 = tb0 * W, pos1 = pos0 + 8 * W;
@@ -411,25 +415,25 @@ __device__ __forceinline__ void svdq_codes_frag(const uint32_t* cw, int tb0, uin
 
 __device__ __forceinline__ float pow2f_(int e) { return __int_as_float((e + 127) << 23); }
 
-// k-step ks of a head: width class (8, 4, 2, 1, 1) and channel offsets within
-// the 16-channel step of lane c (k = 0..3: 2c, 2c+1, 2c+8, 2c+9).
-__host__ __device__ constexpr int svdq_ks_width(int ks) { return ks == 0 ? 8 : ks == 1 ? 4 : ks == 2 ? 2 : 1; }
+// Channel offset of lane c's k-th channel (k = 0..3) within a 16-channel
+// k-step: 2c, 2c+1, 2c+8, 2c+9.
 __device__ __forceinline__ int svdq_kk(int k) { return (k & 1) + ((k >> 1) << 3); }
 
 // grid (chunks, kv_heads, batch), 4 warps: each CTA a contiguous chunk of
-// 64-token tiles of one stream.  Per tile: the value rows and the key
-// records by cp.async into a 3-stage ring; each warp takes 16 tokens (half a
-// 32-token block).  Scores of a quantized block on the tensor cores:
+// 128-token tiles of one stream.  Per tile: the value rows and the key
+// records by cp.async into a 2-stage ring; warp w takes the tile's block w
+// (32 tokens, two 16-row slices).  Scores of a quantized block on the tensor
+// cores:
 //   q~ . L_t + c = sum_j code_tj (q~_j s_j) + (c + sum_j q~_j z_j)
 // with the codes as exact fp16 A operands (one k-step per width class of
-// the schedule) and q~_j s_j as an fp16 hi + lo pair prescaled by a power of
-// two (the block's largest |q~_j s_j| near 2^14), fp32 accumulation; the
-// partial block's tokens from their fp32 latents on the CUDA cores.  Then
-// the online softmax and the weighted sum of the value rows on the tensor
-// cores (the comparator's loop).
+// the schedule: 8, 4, 2 bits, then the 1-bit channels in one or two steps)
+// and q~_j s_j as an fp16 hi + lo B pair prescaled by a power of two (the
+// block's largest |q~_j s_j| near 2^14), fp32 accumulation; the partial
+// block's tokens from their fp32 latents on the CUDA cores.  Then the online
+// softmax and the weighted sum of the value rows on the tensor cores (the
+// comparator's loop), slice by slice.
 __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const SvdqDecParams p) {
   extern __shared__ __align__(128) uint8_t dsm[];
-  __shared__ float merge[kSplitWarps][8][kSplitPartStride];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int H = p.k.H, rm = p.k.r_max, Gq = p.Gq, rb = p.k.rec_bytes;
@@ -438,16 +442,15 @@ __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const Svd
   const SvdqDecSmem L = svdq_dec_smem(rm, rb);
   float* qts = reinterpret_cast<float*>(dsm + L.qts);
   float* cqs = qts + 8 * rm;
-  const long long t0 = (long long)chunk * p.tiles_per_chunk * kSplitTile;
-  const long long t1 = min(t0 + (long long)p.tiles_per_chunk * kSplitTile, p.len);
+  const long long t0 = (long long)chunk * p.tiles_per_chunk * kSvdqTile;
+  const long long t1 = min(t0 + (long long)p.tiles_per_chunk * kSvdqTile, p.len);
   float* part = p.ws + ((long long)X * p.n_chunks + chunk) * (long long)Gq * kSplitPartStride;
   if (t0 >= t1) {
     split_write_empty(Gq, part);
     return;
   }
-  const int n_tiles = (int)((t1 - t0 + kSplitTile - 1) / kSplitTile);
+  const int n_tiles = (int)((t1 - t0 + kSvdqTile - 1) / kSvdqTile);
   const long long nf = p.len / kBlock;  // full (quantized) blocks
-  const __half* vb = p.v + X * p.v_cap * kHeadDim;
   const uint8_t* kb = p.k.blocks + X * p.k.n_blk_cap * rb;
   const float* tail = p.k.tail + X * kBlock * rm;
   const uint32_t sbase = smem_addr(dsm);
@@ -471,31 +474,50 @@ __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const Svd
       qv[ks][k] = jj < ksn[ks] ? __ldg(p.qt + ((size_t)X * 8 + g) * rm + ksf[ks] + jj) : 0.f;
     }
   const float cq_g = __ldg(p.cq + (size_t)X * 8 + g);
-  const int tb0 = 16 * (warp & 1) + g;
 
+  // this thread's cp.async slots: value rows (tid >> 4) + 8i, chunk tid & 15;
+  // record chunks tid and tid + 128 of the tile's four records
+  const int vrow = tid >> 4, vch = tid & 15;
+  const char* vsrc = reinterpret_cast<const char*>(p.v + (X * p.v_cap + t0 + vrow) * kHeadDim + vch * 8);
+  const char* vfall = reinterpret_cast<const char*>(p.v + (X * p.v_cap + t0) * kHeadDim);  // a row below len
+  const uint32_t vdst = swz(sbase + L.vst, vrow, vch);
+  const int rq = rb / 16;
+  const int kbi0 = tid / rq, kq0 = tid % rq, kbi1 = (tid + 128) / rq, kq1 = (tid + 128) % rq;
   auto load_tile = [&](int tile, int stage) {
-    const long long tt = t0 + (long long)tile * kSplitTile;
+    const long long tt = t0 + (long long)tile * kSvdqTile;
+    const char* src = vsrc + (long long)tile * kSvdqTileBytes;
+    const uint32_t dst = vdst + stage * kSvdqTileBytes;
+    if (tt + kSvdqTile <= t1) {
 #pragma unroll
-    for (int i = 0; i < (kSplitTile * 16) / (32 * kSplitWarps); ++i) {
-      const int idx = tid + i * 32 * kSplitWarps;
-      const int row = idx >> 4, ch = idx & 15;
-      const bool valid = tt + row < t1;
-      const long long tok = valid ? tt + row : t0;
-      const uint32_t dv = swz(sbase + L.vst + stage * kSplitTileBytes, row, ch);
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dv), "l"(vb + tok * kHeadDim + ch * 8),
-                   "r"(valid ? 16 : 0)
-                   : "memory");
-    }
-    // the key records of the tile's two blocks that are quantized
-    const long long blk0 = tt / kBlock;
-    for (int i = tid; i < 2 * (rb / 16); i += blockDim.x) {
-      const int bi = i / (rb / 16), q = i % (rb / 16);
-      if (blk0 + bi < nf) {
-        const uint32_t dk = sbase + L.kst + (stage * 2 + bi) * rb + 16 * q;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dk),
-                     "l"(kb + (blk0 + bi) * rb + 16 * q)
+      for (int i = 0; i < kSvdqTile / 8; ++i)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + i * 8 * 256), "l"(src + i * 8 * 256)
+                     : "memory");
+    } else {
+#pragma unroll
+      for (int i = 0; i < kSvdqTile / 8; ++i) {
+        const bool valid = tt + vrow + 8 * i < t1;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + i * 8 * 256),
+                     "l"(valid ? src + i * 8 * 256 : vfall), "r"(valid ? 16 : 0)
                      : "memory");
       }
+    }
+    // the key records of the tile's four blocks that are quantized
+    const long long blk0 = tt / kBlock;
+    const uint32_t kdst = sbase + L.kst + stage * 4 * rb;
+    if (kbi0 < 4 && blk0 + kbi0 < nf)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(kdst + kbi0 * rb + 16 * kq0),
+                   "l"(kb + (blk0 + kbi0) * rb + 16 * kq0)
+                   : "memory");
+    if (kbi1 < 4 && blk0 + kbi1 < nf)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(kdst + kbi1 * rb + 16 * kq1),
+                   "l"(kb + (blk0 + kbi1) * rb + 16 * kq1)
+                   : "memory");
+    for (int i = tid + 256; i < 4 * rq; i += blockDim.x) {  // records over 512 bytes
+      const int bi = i / rq, q = i % rq;
+      if (blk0 + bi < nf)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(kdst + bi * rb + 16 * q),
+                     "l"(kb + (blk0 + bi) * rb + 16 * q)
+                     : "memory");
     }
   };
 
@@ -506,7 +528,6 @@ __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const Svd
   }
   SplitState st;
   split_init(st);
-  const int r0 = 16 * warp;
   for (int tile = 0; tile < n_tiles; ++tile) {
     cp_async_wait<kSvdqStages - 2>();
     __syncthreads();
@@ -514,12 +535,12 @@ __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const Svd
     if (nxt < n_tiles) load_tile(nxt, nxt % kSvdqStages);
     cp_async_commit();
     const int stage = tile % kSvdqStages;
-    const long long tt = t0 + (long long)tile * kSplitTile;
-    const long long ta = tt + r0 + g, tb = ta + 8;  // this lane's two tokens
-    float sc[4];
-    if (tt / kBlock + (warp >> 1) < nf) {
-      // quantized block: B = q~_j s_j (hi + lo), A = codes
-      const uint8_t* rec = dsm + L.kst + (stage * 2 + (warp >> 1)) * rb;
+    const long long tt = t0 + (long long)tile * kSvdqTile;
+    const uint32_t vst = sbase + L.vst + stage * kSvdqTileBytes;
+    const long long blk = tt / kBlock + warp;
+    if (blk < nf) {
+      // quantized block: B = q~_j s_j (hi + lo) once, then both slices
+      const uint8_t* rec = dsm + L.kst + (stage * 4 + warp) * rb;
       const __half2* szr = reinterpret_cast<const __half2*>(rec + szo);
       float av[5][4];
       float mx = 0.f, cst = 0.f;
@@ -541,67 +562,83 @@ __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const Svd
       }
       const int e = min(141 - (int)((__float_as_uint(mx) >> 23) & 0xffu), 126);  // max|B| in [2^14, 2^15)
       const float S = pow2f_(e), invS = pow2f_(-e);
-      sc[0] = sc[1] = sc[2] = sc[3] = 0.f;
+      uint32_t bh[5][2], bl[5][2];
 #pragma unroll
       for (int ks = 0; ks < 5; ++ks) {
-        if (ksn[ks] == 0) continue;  // uniform
-        constexpr int kW[5] = {8, 4, 2, 1, 1};
-        uint32_t a[4];
-        const uint32_t* cw = reinterpret_cast<const uint32_t*>(rec + ksb[ks]) + 2 * c * kW[ks];
-        if (ks == 0) svdq_codes_frag<8>(cw, tb0, a);
-        else if (ks == 1) svdq_codes_frag<4>(cw, tb0, a);
-        else if (ks == 2) svdq_codes_frag<2>(cw, tb0, a);
-        else svdq_codes_frag<1>(cw, tb0, a);
         const float x0 = av[ks][0] * S, x1 = av[ks][1] * S, x8 = av[ks][2] * S, x9 = av[ks][3] * S;
-        const uint32_t h01 = pack_f16x2(x0, x1), h89 = pack_f16x2(x8, x9);
-        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-        const float2 f89 = __half22float2(*reinterpret_cast<const __half2*>(&h89));
-        const uint32_t l01 = pack_f16x2(x0 - f01.x, x1 - f01.y), l89 = pack_f16x2(x8 - f89.x, x9 - f89.y);
-        mma_f16(sc, a[0], a[1], a[2], a[3], h01, h89);
-        mma_f16(sc, a[0], a[1], a[2], a[3], l01, l89);
+        bh[ks][0] = pack_f16x2(x0, x1);
+        bh[ks][1] = pack_f16x2(x8, x9);
+        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&bh[ks][0]));
+        const float2 f89 = __half22float2(*reinterpret_cast<const __half2*>(&bh[ks][1]));
+        bl[ks][0] = pack_f16x2(x0 - f01.x, x1 - f01.y);
+        bl[ks][1] = pack_f16x2(x8 - f89.x, x9 - f89.y);
       }
       // heads 2c, 2c+1: their scale and constant from lanes 8c and 8c+4
       const float cfull = cst + cq_g;
-      const float iA = __shfl_sync(0xffffffffu, invS, 8 * c), iB = __shfl_sync(0xffffffffu, invS, 8 * c + 4);
-      const float cA = __shfl_sync(0xffffffffu, cfull, 8 * c), cB = __shfl_sync(0xffffffffu, cfull, 8 * c + 4);
-      sc[0] = fmaf(sc[0], iA, cA);
-      sc[1] = fmaf(sc[1], iB, cB);
-      sc[2] = fmaf(sc[2], iA, cA);
-      sc[3] = fmaf(sc[3], iB, cB);
+      const float iA = __shfl_sync(0xffffffffu, invS, 8 * c) * p.scale_log2;
+      const float iB = __shfl_sync(0xffffffffu, invS, 8 * c + 4) * p.scale_log2;
+      const float cA = __shfl_sync(0xffffffffu, cfull, 8 * c) * p.scale_log2;
+      const float cB = __shfl_sync(0xffffffffu, cfull, 8 * c + 4) * p.scale_log2;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int tb0 = 16 * half + g;
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 5; ++ks) {
+          if (ksn[ks] == 0) continue;  // uniform
+          uint32_t a[4];
+          if (ks == 0) svdq_codes_frag<8>(reinterpret_cast<const uint32_t*>(rec + ksb[0]) + 16 * c, tb0, a);
+          else if (ks == 1) svdq_codes_frag<4>(reinterpret_cast<const uint32_t*>(rec + ksb[1]) + 8 * c, tb0, a);
+          else if (ks == 2) svdq_codes_frag<2>(reinterpret_cast<const uint32_t*>(rec + ksb[2]) + 4 * c, tb0, a);
+          else svdq_codes_frag<1>(reinterpret_cast<const uint32_t*>(rec + ksb[ks]) + 2 * c, tb0, a);
+          mma_f16(sc, a[0], a[1], a[2], a[3], bh[ks][0], bh[ks][1]);
+          mma_f16(sc, a[0], a[1], a[2], a[3], bl[ks][0], bl[ks][1]);
+        }
+        // every token of a quantized block precedes the chunk's end
+        sc[0] = fmaf(sc[0], iA, cA);
+        sc[1] = fmaf(sc[1], iB, cB);
+        sc[2] = fmaf(sc[2], iA, cA);
+        sc[3] = fmaf(sc[3], iB, cB);
+        split_softmax_pv(st, sc, vst, 32 * warp + 16 * half, lane);
+      }
     } else {
       // the partial block (or past the end): fp32 latents
-      const float* la = tail + (ta < t1 ? (ta % kBlock) : 0) * rm;
-      const float* lb = tail + (tb < t1 ? (tb % kBlock) : 0) * rm;
-      const float* qa = qts + (2 * c) * rm;
-      const float* qb = qa + rm;
-      float s00 = cqs[2 * c], s01 = cqs[2 * c + 1], s10 = s00, s11 = s01;
-      for (int j = 0; j < r; ++j) {
-        const float x = __ldcg(la + j), y = __ldcg(lb + j), u = qa[j], w = qb[j];
-        s00 = fmaf(u, x, s00);
-        s01 = fmaf(w, x, s01);
-        s10 = fmaf(u, y, s10);
-        s11 = fmaf(w, y, s11);
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const long long ta = tt + 32 * warp + 16 * half + g, tb = ta + 8;
+        const bool va = ta < t1, vbv = tb < t1;
+        float sc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (__any_sync(0xffffffffu, va)) {
+          const float* la = tail + (va ? (ta % kBlock) : 0) * rm;
+          const float* lb = tail + (vbv ? (tb % kBlock) : 0) * rm;
+          const float* qa = qts + (2 * c) * rm;
+          const float* qb = qa + rm;
+          float s00 = cqs[2 * c], s01 = cqs[2 * c + 1], s10 = s00, s11 = s01;
+          for (int j = 0; j < r; ++j) {
+            const float x = __ldcg(la + j), y = __ldcg(lb + j), u = qa[j], w = qb[j];
+            s00 = fmaf(u, x, s00);
+            s01 = fmaf(w, x, s01);
+            s10 = fmaf(u, y, s10);
+            s11 = fmaf(w, y, s11);
+          }
+          sc[0] = va ? s00 * p.scale_log2 : -INFINITY;
+          sc[1] = va ? s01 * p.scale_log2 : -INFINITY;
+          sc[2] = vbv ? s10 * p.scale_log2 : -INFINITY;
+          sc[3] = vbv ? s11 * p.scale_log2 : -INFINITY;
+        }
+        split_softmax_pv(st, sc, vst, 32 * warp + 16 * half, lane);
       }
-      sc[0] = s00;
-      sc[1] = s01;
-      sc[2] = s10;
-      sc[3] = s11;
     }
-    const bool va = ta < t1, vbv = tb < t1;
-    sc[0] = va ? sc[0] * p.scale_log2 : -INFINITY;
-    sc[1] = va ? sc[1] * p.scale_log2 : -INFINITY;
-    sc[2] = vbv ? sc[2] * p.scale_log2 : -INFINITY;
-    sc[3] = vbv ? sc[3] * p.scale_log2 : -INFINITY;
-    split_softmax_pv(st, sc, sbase + L.vst + stage * kSplitTileBytes, r0, lane);
   }
   cp_async_wait<0>();
-  split_write_partial(st, merge, warp, lane, Gq, part);
+  __syncthreads();  // the merge scratch reuses the value ring
+  split_write_partial(st, reinterpret_cast<float(*)[8][kSplitPartStride]>(dsm + L.vst), warp, lane, Gq, part);
 }
 
 static int svdq_chunks(int64_t streams, int64_t seq, int smem, int* tiles_per_chunk) {
   int per_sm = 1;
   kernel_occupancy(reinterpret_cast<const void*>(svdq_decode_kernel), 32 * kSplitWarps, smem, &per_sm);
-  const int64_t tiles = std::max<int64_t>(1, (seq + kSplitTile - 1) / kSplitTile);
+  const int64_t tiles = std::max<int64_t>(1, (seq + kSvdqTile - 1) / kSvdqTile);
   int64_t nch = std::max<int64_t>(1, (int64_t)device_sm_count() * per_sm / streams);
   nch = std::min(nch, tiles);
   const int64_t tpc = (tiles + nch - 1) / nch;
