@@ -90,34 +90,46 @@ __global__ void __launch_bounds__(32 * kF16Warps) fp16_decode_kernel(const F16Pa
   split_write_partial(st, merge, warp, lane, Gq, part);
 }
 
+// One CTA per (KV head, batch, query head of the group); thread d: channel d.
+// Launched as a programmatic dependent of the split kernel: it may start
+// early and waits here for the partials.
 __global__ void split_combine_kernel(const float* ws, int Hq, int Hkv, int n_chunks, void* out, int out_fp32) {
-  const int kh = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  const int kh = blockIdx.x, b = blockIdx.y, h = blockIdx.z, d = threadIdx.x;
   const int Gq = Hq / Hkv, mstride = kSplitPartStride;
-  const float* wp = ws + ((long long)b * Hkv + kh) * n_chunks * (long long)Gq * mstride;
-  for (int h = 0; h < Gq; ++h) {
-    float M = -INFINITY;
-    for (int ch = 0; ch < n_chunks; ++ch) M = fmaxf(M, wp[((long long)ch * Gq + h) * mstride]);
-    float L = 0.f, a = 0.f;
-    for (int ch = 0; ch < n_chunks; ++ch) {
-      const float m = wp[((long long)ch * Gq + h) * mstride];
-      if (m == -INFINITY) continue;
-      const float w = ex2f_(m - M);
-      L += wp[((long long)ch * Gq + h) * mstride + 1] * w;
-      a += wp[((long long)ch * Gq + h) * mstride + 2 + d] * w;
-    }
-    const long long oi = ((long long)b * Hq + (long long)kh * Gq + h) * kHeadDim + d;
-    const float o = a / L;
-    if (out_fp32)
-      static_cast<float*>(out)[oi] = o;
-    else
-      static_cast<__half*>(out)[oi] = __float2half_rn(o);
+  grid_dep_wait();
+  const float* wp = ws + ((long long)b * Hkv + kh) * n_chunks * (long long)Gq * mstride + (long long)h * mstride;
+  float M = -INFINITY;
+  for (int ch = 0; ch < n_chunks; ++ch) M = fmaxf(M, wp[(long long)ch * Gq * mstride]);
+  float L = 0.f, a = 0.f;
+  for (int ch = 0; ch < n_chunks; ++ch) {
+    const float* pc = wp + (long long)ch * Gq * mstride;
+    const float m = pc[0];
+    if (m == -INFINITY) continue;
+    const float w = ex2f_(m - M);
+    L += pc[1] * w;
+    a += pc[2 + d] * w;
   }
+  const long long oi = ((long long)b * Hq + (long long)kh * Gq + h) * kHeadDim + d;
+  const float o = a / L;
+  if (out_fp32)
+    static_cast<float*>(out)[oi] = o;
+  else
+    static_cast<__half*>(out)[oi] = __float2half_rn(o);
 }
 
 palu_status split_combine(const float* ws, long long batch, int Hq, int Hkv, int n_chunks, void* out, int out_fp32,
                           cudaStream_t stream) {
-  split_combine_kernel<<<dim3(Hkv, (unsigned)batch), kHeadDim, 0, stream>>>(ws, Hq, Hkv, n_chunks, out, out_fp32);
-  return cuda_check(cudaGetLastError(), "split_combine_kernel launch");
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(Hkv, (unsigned)batch, Hq / Hkv);
+  cfg.blockDim = dim3(kHeadDim);
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cuda_check(cudaLaunchKernelEx(&cfg, split_combine_kernel, ws, Hq, Hkv, n_chunks, out, out_fp32),
+                    "split_combine_kernel launch");
 }
 
 static int f16_chunks(int64_t batch, int32_t kv_heads, int64_t seq_cap, int* tiles_per_chunk) {

@@ -18,6 +18,11 @@ constexpr int kSplitTile = 64;                              // tokens per tile (
 constexpr int kSplitTileBytes = kSplitTile * kHeadDim * 2;  // 16 KB per tensor
 constexpr int kSplitPartStride = 2 + kHeadDim;              // (max, sum, acc[128]) per head
 
+// Programmatic dependent launch: wait for the preceding launch's results /
+// let the next launch be scheduled.  Both are no-ops without the attribute.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float ex2f_(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -328,6 +328,7 @@ struct SvdqDecParams {
 __global__ void __launch_bounds__(128) svdq_qprep_kernel(const SvdqDecParams p) {
   __shared__ float q_s[8][kHeadDim];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  grid_dep_launch();  // the split kernel may start its copies; it waits for this grid
   const long long X = blockIdx.x;
   const int H = p.k.H, rm = p.k.r_max, Gq = p.Gq;
   const int h = (int)(X % H), b = (int)(X / H), r = p.k.head[4 * h];
@@ -455,8 +456,7 @@ __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const Svd
   const float* tail = p.k.tail + X * kBlock * rm;
   const uint32_t sbase = smem_addr(dsm);
 
-  for (int i = tid; i < 8 * rm; i += blockDim.x) qts[i] = __ldg(p.qt + (size_t)X * 8 * rm + i);
-  if (tid < 8) cqs[tid] = __ldg(p.cq + (size_t)X * 8 + tid);
+  grid_dep_launch();  // the combine kernel may be scheduled; it waits for this grid
 
   // the head's width classes: group sizes r/8 (+1 for the first r%8 groups)
   const int n8 = r / 8 + (0 < r % 8), n4 = r / 8 + (1 < r % 8), n2 = r / 8 + (2 < r % 8);
@@ -464,17 +464,6 @@ __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const Svd
   const int ksn[5] = {n8, n4, n2, min(n1, 16), max(n1 - 16, 0)};
   const int ksf[5] = {0, n8, n8 + n4, n8 + n4 + n2, n8 + n4 + n2 + 16};
   const int ksb[5] = {0, 32 * n8, 32 * n8 + 16 * n4, 32 * n8 + 16 * n4 + 8 * n2, 32 * n8 + 16 * n4 + 8 * n2 + 64};
-  // lane's q~ of head g at its channels of each k-step (0 past the class)
-  float qv[5][4];
-#pragma unroll
-  for (int ks = 0; ks < 5; ++ks)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int jj = 2 * c + svdq_kk(k);
-      qv[ks][k] = jj < ksn[ks] ? __ldg(p.qt + ((size_t)X * 8 + g) * rm + ksf[ks] + jj) : 0.f;
-    }
-  const float cq_g = __ldg(p.cq + (size_t)X * 8 + g);
-
   // this thread's cp.async slots: value rows (tid >> 4) + 8i, chunk tid & 15;
   // record chunks tid and tid + 128 of the tile's four records
   const int vrow = tid >> 4, vch = tid & 15;
@@ -526,6 +515,21 @@ __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const Svd
     if (s < n_tiles) load_tile(s, s);
     cp_async_commit();
   }
+  // the query factors come from the preceding launch (the cache's codes and
+  // the values from earlier ones, complete before it started)
+  grid_dep_wait();
+  for (int i = tid; i < 8 * rm; i += blockDim.x) qts[i] = __ldcg(p.qt + (size_t)X * 8 * rm + i);
+  if (tid < 8) cqs[tid] = __ldcg(p.cq + (size_t)X * 8 + tid);
+  // lane's q~ of head g at its channels of each k-step (0 past the class)
+  float qv[5][4];
+#pragma unroll
+  for (int ks = 0; ks < 5; ++ks)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int jj = 2 * c + svdq_kk(k);
+      qv[ks][k] = jj < ksn[ks] ? __ldcg(p.qt + ((size_t)X * 8 + g) * rm + ksf[ks] + jj) : 0.f;
+    }
+  const float cq_g = __ldcg(p.cq + (size_t)X * 8 + g);
   SplitState st;
   split_init(st);
   for (int tile = 0; tile < n_tiles; ++tile) {
@@ -843,11 +847,18 @@ extern "C" palu_status palu_svdq_decode_attn(const palu_svdq_cache* cache, const
   svdq_qprep_kernel<<<(unsigned)streams, 128, 0, strm>>>(p);
   st = cuda_check(cudaGetLastError(), "svdq_qprep_kernel launch");
   if (st != PALU_OK) return st;
-  int per_sm = 0;
-  st = kernel_occupancy(reinterpret_cast<const void*>(svdq_decode_kernel), 32 * kSplitWarps, w.smem, &per_sm);
-  if (st != PALU_OK) return st;
-  svdq_decode_kernel<<<dim3(p.n_chunks, cache->kv_heads, (unsigned)cache->batch), 32 * kSplitWarps, w.smem, strm>>>(p);
-  st = cuda_check(cudaGetLastError(), "svdq_decode_kernel launch");
+  // the split kernel as a programmatic dependent of the q-prep
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_chunks, cache->kv_heads, (unsigned)cache->batch);
+  cfg.blockDim = dim3(32 * kSplitWarps);
+  cfg.dynamicSmemBytes = w.smem;
+  cfg.stream = strm;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  st = cuda_check(cudaLaunchKernelEx(&cfg, svdq_decode_kernel, p), "svdq_decode_kernel launch");
   if (st != PALU_OK) return st;
   return split_combine(p.ws, cache->batch, q_heads, cache->kv_heads, p.n_chunks, out, out_fp32, strm);
 }
