@@ -749,6 +749,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for the CPU baseline")
     ap.add_argument("--prefill", type=int, default=0,
                     help="replace the workload's prefill length (a reduced case for profiling; not a bench line)")
+    ap.add_argument("--comparator-only", choices=["fp16", "kivi", "svdq"], default=None,
+                    help="run one comparator alone on --layers layers (a profiling case; not a bench line)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -772,6 +774,17 @@ def main(argv=None):
                                  "sample": ref["sample"]},
                 "e2e": {"value": ref["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
+        return 0
+
+    if args.comparator_only:
+        from rank_latent_kv_gb300 import palu as P
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        P.lib()
+        fn = {"fp16": run_comparator, "kivi": run_kivi_comparator, "svdq": run_svdq_comparator}[args.comparator_only]
+        res = fn(P, w, torch.cuda.Stream(device=dev), args.layers or w.layers, w.prefill, dev, 1, steps=args.steps)
+        print(json.dumps({"comparator_only": args.comparator_only, "workload": w.name,
+                          "layers": args.layers or w.layers, **res}))
         return 0
 
     init_dist(world, "nccl")

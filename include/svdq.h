@@ -10,7 +10,10 @@
  * channel groups (most significant first; a 0-bit channel is not stored and
  * reads back as 0).  Values are not compressed: they stay fp16, in the
  * caller's own buffer.  Decode attention runs on the key codes directly:
- * scores q . K_t = q~ . L_t + q . mean with q~ = q V_h, in fp32.
+ * scores q . K_t = q~ . L_t + q . mean with q~ = q V_h, as
+ * sum_j code_tj (q~_j s_j) + (q . mean + sum_j q~_j z_j): the codes exact,
+ * q~_j s_j as an fp16 hi/lo pair (about 22 significant bits), fp32
+ * accumulation; the zero term and the partial block's fp32 latents in fp32.
  *
  * The per-head fit is palu_fit with n_head_groups = kv_heads (one head per
  * group); its group ranks are the per-head ranks, and its basis [kv_heads,

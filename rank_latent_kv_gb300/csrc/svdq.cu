@@ -5,9 +5,10 @@
 // so the fp32 latents are the correctly rounded ones), quantizes every block
 // that completes (asymmetric min/max, blog post "VeloxQuant-MLX 0.8.0 adds
 // KIVI", "What KIVI is") and packs the codes LSB-first; the decode computes
-// each key score from the codes in fp32 (q~ . L_t + q . mean, q~ = q V_h)
-// and streams the fp16 values through the tensor-core tile loop the dense
-// comparator uses.
+// each key score q~ . L_t + q . mean (q~ = q V_h) from the codes on the
+// tensor cores (exact codes against an fp16 hi/lo pair of q~_j s_j, fp32
+// accumulation) and streams the fp16 values through the tensor-core tile
+// loop the dense comparator uses.
 #include <math.h>
 
 #include <algorithm>
