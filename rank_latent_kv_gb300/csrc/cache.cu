@@ -49,22 +49,164 @@ __global__ void cache_init_kernel(const float* __restrict__ basis, int ld, const
 
 // ------------------------------------------------------------------ encode
 // Shared-memory plan of one encode CTA (one 32-token block of one stream).
+// The staged basis comes last: the tensor-core path (every phase-1 CTA of a
+// quantized cache) reads the basis from global memory and is launched
+// without it.
 struct EncodeSmem {
-  int xs_off, basis_off, lat_off, codes_off, sz_off, rec_off, total;
+  int xs_off, cand_off, lat_off, err_off, codes_off, sz_off, rec_off, work_off, basis_off, total;
 };
 
 __host__ __device__ inline int align16(int x) { return (x + 15) / 16 * 16; }
 
+constexpr int kXsStride = kHeadDim + 8;  // halves per staged row: 272 B, so ldmatrix rows hit distinct banks
+
 __host__ __device__ inline EncodeSmem encode_smem(int r, int rec_bytes) {
   EncodeSmem s;
-  s.xs_off = 0;                                                        // half [32][128]
-  s.basis_off = s.xs_off + kBlock * kHeadDim * 2;                      // float [r][129]
-  s.lat_off = s.basis_off + align16(4 * r * (kHeadDim + 1));           // float [32][r+1]
-  s.codes_off = s.lat_off + align16(4 * kBlock * (r + 1));             // u8 [32][r]
+  s.xs_off = 0;                                                        // half [32][136]
+  s.cand_off = s.xs_off + kBlock * kXsStride * 2;                      // u32 [2][128]: min / max candidates
+  s.lat_off = s.cand_off + 8 * kHeadDim;                               // float [32][r+1]
+  s.err_off = s.lat_off + align16(4 * kBlock * (r + 1));               // float [32][r+1]: bound of |L' - L|
+  s.codes_off = s.err_off + align16(4 * kBlock * (r + 1));             // u8 [32][r]
   s.sz_off = s.codes_off + align16(kBlock * r);                        // half2 [r] (scale, zero)
   s.rec_off = s.sz_off + align16(4 * r);                               // record
-  s.total = s.rec_off + align16(rec_bytes);
+  s.work_off = s.rec_off + align16(rec_bytes);                         // int [2] counts, u16 [32 r] work list
+  s.basis_off = s.work_off + align16(8 + 2 * kBlock * r);              // float [r][129] (exact path only)
+  s.total = s.basis_off + align16(4 * r * (kHeadDim + 1));
   return s;
+}
+
+// One latent (x - mu_g) V_g[:, j] as the encoder stores it: sum_d x_d V_dj
+// accumulated in order d = 0..127 as an unevaluated float pair (error-free
+// products and sums), minus mu_g . V_g[:, j] (a float pair), rounded once to
+// fp32.  Every exact latent of the encoder goes through this sequence, so
+// the two projection paths below store identical values.
+__device__ __forceinline__ void fp_acc(float& S, float& E, float xv, float v) {
+  float pp, pe, s2, se;
+  two_prod(xv, v, pp, pe);
+  two_sum(S, pp, s2, se);
+  S = s2;
+  E = __fadd_rn(E, __fadd_rn(se, pe));
+}
+__device__ __forceinline__ float fp_finish(float S, float E, float2 m) {
+  float a, ae;
+  two_sum(S, -m.x, a, ae);
+  const float low = __fadd_rn(__fsub_rn(E, m.y), ae);
+  return __fadd_rn(a, low);
+}
+// The same sum with four interleaved float pairs (d mod 4) merged by
+// error-free sums at the end: about 48 significant bits like the sequential
+// pair, so its fp32 rounding is the same except when the sum lies within
+// about 2^-48 of a rounding boundary; a quarter of the dependent chain.
+__device__ __noinline__ float exact_latent(const __half* xrow, const float* __restrict__ brow, float2 m) {
+  float S[4] = {0.f, 0.f, 0.f, 0.f}, E[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+  for (int d = 0; d < kHeadDim; d += 4) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(brow + d));
+    const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(xrow + d));
+    const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(xrow + d + 2));
+    fp_acc(S[0], E[0], x01.x, v.x);
+    fp_acc(S[1], E[1], x01.y, v.y);
+    fp_acc(S[2], E[2], x23.x, v.z);
+    fp_acc(S[3], E[3], x23.y, v.w);
+  }
+  float s01, e01, s23, e23, s, e;
+  two_sum(S[0], S[1], s01, e01);
+  two_sum(S[2], S[3], s23, e23);
+  two_sum(s01, s23, s, e);
+  const float lo = __fadd_rn(__fadd_rn(__fadd_rn(E[0], E[1]), __fadd_rn(E[2], E[3])), __fadd_rn(__fadd_rn(e01, e23), e));
+  return fp_finish(s, lo, m);
+}
+
+// The quantizer's code of a latent v (fp32 arithmetic, as the oracle):
+// round((v - z) / s) clamped to [0, qmax]; 0 when s is 0.  Non-decreasing in v.
+__device__ __forceinline__ float quant_code(float v, float z32, float s32, float qmax) {
+  if (s32 == 0.f) return 0.f;
+  return fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v, z32), s32)), 0.f), qmax);
+}
+
+// Tensor-core projection of a complete block's new rows (quantized caches).
+// L'_tj = x_t . (H_j + L_j) 2^-10 - mu.V_j, with H + L the fp16 hi/lo split
+// of 2^10 V_g (mma.sync m16n8k16, the hi and lo products in separate fp32
+// accumulators), for rows t >= off_new; the basis comes from global memory
+// (L2) as B fragments.  A third chain forms S_tj = sum_d |x_d| |V_dj| (from
+// |x| and the fp16 |H|), and err_tj = 2^-16 S_tj + 2^-21 |mu.V_j| bounds
+// |L'_tj - L_tj| with margin: each of the eight accumulation steps of a
+// chain adds a few units of 2^-24 of S_tj, the hi/lo split leaves 2^-22 S_tj,
+// and the final roundings a few units of 2^-24 of S_tj + |mu.V_j|.
+// Warp w takes the 8-channel tiles w, w + 4, ... (two at a time); both
+// 16-row tiles.
+__device__ __forceinline__ void project_tc(const __half* xs, const float* __restrict__ bT, float* lat, float* err,
+                                           int r, const float2* mv, int off_new) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+  const int n_nt = (r + 7) / 8;
+  const uint32_t xbase = smem_addr(xs);
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    if (warp + 8 * pass >= n_nt) break;  // uniform
+    float ah[2][2][4], al[2][2][4], aa[2][2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ah[i][m][e] = al[i][m][e] = aa[i][m][e] = 0.f;
+#pragma unroll 2
+    for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+      uint32_t a[2][4], ab[2][4];
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        ldsm_x4(a[m][0], a[m][1], a[m][2], a[m][3],
+                xbase + 2 * ((16 * m + (lane & 15)) * kXsStride + 16 * ks + 8 * (lane >> 4)));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ab[m][q] = a[m][q] & 0x7fff7fffu;
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int nt = warp + 8 * pass + 4 * i;
+        if (nt < n_nt) {  // uniform
+          const int j = 8 * nt + g;
+          float2 v01 = make_float2(0.f, 0.f), v89 = make_float2(0.f, 0.f);
+          if (j < r) {
+            const float* row = bT + (size_t)j * kHeadDim + 16 * ks + 2 * c;
+            v01 = __ldg(reinterpret_cast<const float2*>(row));
+            v89 = __ldg(reinterpret_cast<const float2*>(row + 8));
+          }
+          const float v[4] = {v01.x * 1024.f, v01.y * 1024.f, v89.x * 1024.f, v89.y * 1024.f};
+          const uint32_t h01 = pack_f16x2(v[0], v[1]), h89 = pack_f16x2(v[2], v[3]);
+          const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+          const float2 f89 = __half22float2(*reinterpret_cast<const __half2*>(&h89));
+          const uint32_t l01 = pack_f16x2(v[0] - f01.x, v[1] - f01.y), l89 = pack_f16x2(v[2] - f89.x, v[3] - f89.y);
+          const uint32_t b01 = h01 & 0x7fff7fffu, b89 = h89 & 0x7fff7fffu;
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            mma_f16(ah[i][m], a[m][0], a[m][1], a[m][2], a[m][3], h01, h89);
+            mma_f16(al[i][m], a[m][0], a[m][1], a[m][2], a[m][3], l01, l89);
+            mma_f16(aa[i][m], ab[m][0], ab[m][1], ab[m][2], ab[m][3], b01, b89);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int nt = warp + 8 * pass + 4 * i;
+      if (nt >= n_nt) continue;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 8 * nt + 2 * c + (e & 1);
+        if (j >= r) continue;
+        const float2 mj = mv[j];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const int t = 16 * m + g + 8 * (e >> 1);
+          if (t < off_new) continue;
+          const float pr = __fmul_rn(__fadd_rn(ah[i][m][e], al[i][m][e]), 1.f / 1024.f);
+          lat[t * (r + 1) + j] = __fsub_rn(__fsub_rn(pr, mj.x), mj.y);
+          // |H| is |V| 2^10 to within 2^-11 relative: 1.001 covers it and the chain's own rounding
+          err[t * (r + 1) + j] = fmaf(aa[i][m][e], 0x1p-26f * 1.001f, fabsf(mj.x) * 0x1p-21f);
+        }
+      }
+    }
+  }
 }
 
 // grid (blocks touched, kv_heads, batch), 128 threads.
@@ -81,6 +223,10 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
   const int r = cv.r;
   const EncodeSmem L = encode_smem(r, cv.rec_bytes);
   __half* xs = reinterpret_cast<__half*>(smem + L.xs_off);
+  float* err = reinterpret_cast<float*>(smem + L.err_off);
+  uint32_t* cand = reinterpret_cast<uint32_t*>(smem + L.cand_off);
+  int* n_work = reinterpret_cast<int*>(smem + L.work_off);
+  uint16_t* work = reinterpret_cast<uint16_t*>(smem + L.work_off + 8);
   float* bas = reinterpret_cast<float*>(smem + L.basis_off);
   float* lat = reinterpret_cast<float*>(smem + L.lat_off);
   uint8_t* codes = smem + L.codes_off;
@@ -116,15 +262,23 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
     const bool complete = (hi - lo) == kBlock;
     const int grp = h / cv.heads_per_group;
 
-    // stage the new tokens' rows and the group basis
+    // Quantized caches project a complete block on the tensor cores and
+    // compute exact latents only where a stored value depends on them (see
+    // the quantizer below); everything else takes the exact path for every
+    // latent, from a staged copy of the basis.
+    const bool tc = cv.quantize && complete;
+    const float* bT = cv.basisT + (size_t)grp * r * kHeadDim;
+
+    // stage the new tokens' rows (and, on the exact path, the group basis)
+    if (tid < 2) n_work[tid] = 0;
     const __half* xsrc = x + (((long long)b * Hkv + h) * T + (new_lo - p0)) * kHeadDim;
     for (int i = tid; i < n_new * (kHeadDim / 8); i += blockDim.x) {
       const int t = i / (kHeadDim / 8), q = i % (kHeadDim / 8);
-      reinterpret_cast<uint4*>(xs + (off_new + t) * kHeadDim)[q] =
+      reinterpret_cast<uint4*>(xs + (off_new + t) * kXsStride)[q] =
           reinterpret_cast<const uint4*>(xsrc + (long long)t * kHeadDim)[q];
     }
-    const float* bsrc = cv.basisT + (size_t)grp * r * kHeadDim;
-    for (int i = tid; i < r * (kHeadDim / 4); i += blockDim.x) {
+    const float* bsrc = bT;
+    for (int i = tid; i < (tc ? 0 : r) * (kHeadDim / 4); i += blockDim.x) {
       const int j = i / (kHeadDim / 4), q = i % (kHeadDim / 4);
       const float4 v = reinterpret_cast<const float4*>(bsrc + (size_t)j * kHeadDim)[q];
       float* dst = bas + j * (kHeadDim + 1) + 4 * q;
@@ -135,11 +289,13 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
     }
     __syncthreads();
 
-    // projection: warp w takes tokens off_new + w + 4i, lane takes channels lane + 32k.
-    // Each (token, channel) latent is sum_d x_d V_dj accumulated as an
-    // unevaluated float pair (error-free products and sums), minus mu_g.V_g[:, j],
-    // then rounded once to fp32.
-    {
+    if (tc) {
+      project_tc(xs, bT, lat, err, r, cv.mv + (size_t)grp * r, off_new);
+    } else {
+      // projection: warp w takes tokens off_new + w + 4i, lane takes channels lane + 32k.
+      // Each (token, channel) latent is sum_d x_d V_dj accumulated as an
+      // unevaluated float pair (error-free products and sums), minus mu_g.V_g[:, j],
+      // then rounded once to fp32.
       const int warp = tid >> 5, lane = tid & 31;
       float S[8][4], E[8][4];
 #pragma unroll
@@ -157,15 +313,9 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           if (i < nt) {
-            const float xv = __half2float(xs[(off_new + warp + 4 * i) * kHeadDim + d]);
+            const float xv = __half2float(xs[(off_new + warp + 4 * i) * kXsStride + d]);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              float pp, pe, s2, se;
-              two_prod(xv, v[k], pp, pe);
-              two_sum(S[i][k], pp, s2, se);
-              S[i][k] = s2;
-              E[i][k] = __fadd_rn(E[i][k], __fadd_rn(se, pe));
-            }
+            for (int k = 0; k < 4; ++k) fp_acc(S[i][k], E[i][k], xv, v[k]);
           }
         }
       }
@@ -175,14 +325,8 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
         if (j < r) {
           const float2 m = cv.mv[(size_t)grp * r + j];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (i < nt) {
-              float a, ae;
-              two_sum(S[i][k], -m.x, a, ae);
-              const float low = __fadd_rn(__fsub_rn(E[i][k], m.y), ae);
-              lat[(off_new + warp + 4 * i) * (r + 1) + j] = __fadd_rn(a, low);
-            }
-          }
+          for (int i = 0; i < 8; ++i)
+            if (i < nt) lat[(off_new + warp + 4 * i) * (r + 1) + j] = fp_finish(S[i][k], E[i][k], m);
         }
       }
     }
@@ -193,37 +337,104 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
 
     if (cv.quantize) {
       if (complete) {
-        // earlier tokens of this block come from the tail
+        // earlier tokens of this block come from the tail (exact)
         for (int i = tid; i < off_new * r; i += blockDim.x) {
           const int t = i / r, j = i % r;
           lat[t * (r + 1) + j] = tail[t * r + j];
+          err[t * (r + 1) + j] = 0.f;
         }
         for (int i = tid; i < cv.rec_bytes / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(rec)[i] = 0u;
         __syncthreads();
-        // quantize: one thread per channel
-        for (int j = tid; j < r; j += blockDim.x) {
-          float mn = lat[j], mx = lat[j];
-          for (int t = 1; t < kBlock; ++t) {
-            const float v = lat[t * (r + 1) + j];
-            mn = fminf(mn, v);
-            mx = fmaxf(mx, v);
-          }
-          const int bits = j < cv.n_hi ? 4 : 2;
-          const float qmax = (float)((1 << bits) - 1);
-          const float scale = __fdiv_rn(__fsub_rn(mx, mn), qmax);
-          const __half sh = __float2half_rn(scale);
-          const __half zh = __float2half_rn(mn);
-          const float s32 = __half2float(sh), z32 = __half2float(zh);
-          sz[j] = __halves2half2(sh, zh);
-          atomicMax(&cv.hdr->max_scale, __float_as_uint(s32));
-          atomicMax(&cv.smax[(long long)b * Hkv + h], __float_as_uint(s32));
-          for (int t = 0; t < kBlock; ++t) {
-            float q = 0.f;
-            if (s32 != 0.f) {
-              q = rintf(__fdiv_rn(__fsub_rn(lat[t * (r + 1) + j], z32), s32));
-              q = fminf(fmaxf(q, 0.f), qmax);
+        {  // complete block of a quantized cache: tc holds
+          // Each new latent is known to within e = 2^-15 (|x_t|_2 |V_j|_2 +
+          // |mu.V_j|) (tail rows exactly).  Only tokens that can hold the
+          // block's minimum or maximum need their exact latent, so scale and
+          // zero are those of the exact latents; a code is taken from the
+          // bound interval when both ends give the same code (the quantizer
+          // is monotone), else from the exact latent.  Channels go warp by
+          // warp (lane = token); the exact latents are computed by all
+          // threads from shared work lists of (token, channel) pairs.
+          const int warp = tid >> 5, lane = tid & 31, t = lane;
+          const uint32_t lt = (1u << lane) - 1u;
+          for (int j = warp; j < r; j += 4) {
+            const float v = lat[t * (r + 1) + j], e = err[t * (r + 1) + j];
+            float min_hi = v + e, max_lo = v - e;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              min_hi = fminf(min_hi, __shfl_xor_sync(0xffffffffu, min_hi, o));
+              max_lo = fmaxf(max_lo, __shfl_xor_sync(0xffffffffu, max_lo, o));
             }
+            const bool cmin = v - e <= min_hi, cmax = v + e >= max_lo;
+            const uint32_t bmin = __ballot_sync(0xffffffffu, cmin), bmax = __ballot_sync(0xffffffffu, cmax);
+            const bool need = (cmin || cmax) && t >= off_new;
+            const uint32_t bneed = __ballot_sync(0xffffffffu, need);
+            int base = 0;
+            if (lane == 0 && bneed) base = atomicAdd(&n_work[0], __popc(bneed));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (need) work[base + __popc(bneed & lt)] = (uint16_t)(t * 128 + j);
+            if (lane == 0) {
+              cand[j] = bmin;
+              cand[kHeadDim + j] = bmax;
+            }
+          }
+          __syncthreads();
+          for (int i = tid; i < n_work[0]; i += blockDim.x) {
+            const int tt = work[i] >> 7, jj = work[i] & 127;
+            lat[tt * (r + 1) + jj] =
+                exact_latent(xs + tt * kXsStride, bT + (size_t)jj * kHeadDim, cv.mv[(size_t)grp * r + jj]);
+          }
+          __syncthreads();
+          for (int j = warp; j < r; j += 4) {
+            const float v = lat[t * (r + 1) + j];
+            const uint32_t bmin = cand[j], bmax = cand[kHeadDim + j];
+            float mn = (bmin >> t) & 1u ? v : INFINITY, mx = (bmax >> t) & 1u ? v : -INFINITY;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            }
+            const float qmax = (float)((1 << (j < cv.n_hi ? 4 : 2)) - 1);
+            const float scale = __fdiv_rn(__fsub_rn(mx, mn), qmax);
+            const __half sh = __float2half_rn(scale);
+            const __half zh = __float2half_rn(mn);
+            const float s32 = __half2float(sh), z32 = __half2float(zh);
+            if (lane == 0) {
+              sz[j] = __halves2half2(sh, zh);
+              atomicMax(&cv.hdr->max_scale, __float_as_uint(s32));
+              atomicMax(&cv.smax[(long long)b * Hkv + h], __float_as_uint(s32));
+            }
+            float q;
+            bool need = false;
+            if (t < off_new || (((bmin | bmax) >> t) & 1u)) {
+              q = quant_code(v, z32, s32, qmax);  // exact latent
+            } else if (s32 == 0.f) {
+              q = 0.f;
+            } else {
+              // the exact code is round(fl((L - z) / s)) for some L in [v - e, v + e]:
+              // it is known when that interval, scaled by an approximate 1/s and
+              // widened by the approximation's error, lies inside one rounding
+              // cell; else it is decided from the exact latent below
+              const float inv = 1.f / s32, e = err[t * (r + 1) + j];
+              const float u = (v - z32) * inv, du = fmaf(e, inv, fmaf(fabsf(u), 0x1p-18f, 0x1p-20f));
+              const float k = rintf(u);
+              need = fabsf(u - k) + du >= 0.5f;
+              q = fminf(fmaxf(k, 0.f), qmax);
+            }
+            const uint32_t bneed = __ballot_sync(0xffffffffu, need);
+            int base = 0;
+            if (lane == 0 && bneed) base = atomicAdd(&n_work[1], __popc(bneed));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (need) work[base + __popc(bneed & lt)] = (uint16_t)(t * 128 + j);
             codes[t * r + j] = (uint8_t)q;
+          }
+          __syncthreads();
+          for (int i = tid; i < n_work[1]; i += blockDim.x) {
+            const int tt = work[i] >> 7, jj = work[i] & 127;
+            const float x =
+                exact_latent(xs + tt * kXsStride, bT + (size_t)jj * kHeadDim, cv.mv[(size_t)grp * r + jj]);
+            const __half2 szj = sz[jj];
+            codes[tt * r + jj] = (uint8_t)quant_code(x, __high2float(szj), __low2float(szj),
+                                                      (float)((1 << (jj < cv.n_hi ? 4 : 2)) - 1));
           }
         }
         __syncthreads();
@@ -540,12 +751,14 @@ extern "C" palu_status palu_encode_append(palu_cache* cache, const void* x, int6
     cache->length += 1;
     return PALU_OK;
   }
-  const int smem = encode_smem(cache->rank, cache->record_bytes).total;
+  const EncodeSmem es = encode_smem(cache->rank, cache->record_bytes);
   int per_sm = 0;
-  st = kernel_occupancy(reinterpret_cast<const void*>(encode_append_kernel), 128, smem, &per_sm);
+  st = kernel_occupancy(reinterpret_cast<const void*>(encode_append_kernel), 128, es.total, &per_sm);
   if (st != PALU_OK) return st;
   const CacheView cv = make_view(cache);
   for (int phase = 1; phase <= 2; ++phase) {
+    // phase 1 of a quantized cache: complete blocks only, the tensor-core path
+    const int smem = (phase == 1 && cache->quantize) ? es.basis_off : es.total;
     encode_append_kernel<<<dim3(phase == 1 ? (unsigned)nblk : 1u, cache->kv_heads, cache->batch), 128, smem,
                            static_cast<cudaStream_t>(stream)>>>(cv, static_cast<const __half*>(x), tokens,
                                                                 cache->kv_heads, phase, nullptr);
@@ -573,11 +786,12 @@ extern "C" palu_status palu_encode_append_ragged(palu_cache* cache, const void* 
   cache_make_ragged_kernel<<<1, 1, 0, strm>>>(cv.hdr, cv.seq_len, cache->batch);
   st = cuda_check(cudaGetLastError(), "cache_make_ragged_kernel launch");
   if (st != PALU_OK) return st;
-  const int smem = encode_smem(cache->rank, cache->record_bytes).total;
+  const EncodeSmem es = encode_smem(cache->rank, cache->record_bytes);
   int per_sm = 0;
-  st = kernel_occupancy(reinterpret_cast<const void*>(encode_append_kernel), 128, smem, &per_sm);
+  st = kernel_occupancy(reinterpret_cast<const void*>(encode_append_kernel), 128, es.total, &per_sm);
   if (st != PALU_OK) return st;
   for (int phase = 1; phase <= 2; ++phase) {
+    const int smem = (phase == 1 && cache->quantize) ? es.basis_off : es.total;  // as palu_encode_append
     encode_append_kernel<<<dim3(phase == 1 ? (unsigned)nblk : 1u, cache->kv_heads, cache->batch), 128, smem, strm>>>(
         cv, static_cast<const __half*>(x), tokens, cache->kv_heads, phase, counts);
     st = cuda_check(cudaGetLastError(), "encode_append_kernel launch");
