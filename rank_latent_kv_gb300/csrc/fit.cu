@@ -296,7 +296,7 @@ __global__ void gram_reduce_kernel(const float* __restrict__ part, const float* 
   if (i == 0) mu[(size_t)grp * kHeadDim + j] = (float)(sj / n_rows);
 }
 
-constexpr int kJacThreads = 512;
+constexpr int kJacThreads = 544;  // 17 warps: a round's 2080 blocks in four passes
 constexpr int kLdA = kHeadDim + 1;  // padded rows (fp64 and fp32)
 constexpr int kMaxSweeps = 40;
 // Rotate a pair while |a_pq| > max(kJacRel sqrt|a_pp a_qq|, kJacFloor ||A||_F):
@@ -355,115 +355,169 @@ __device__ __forceinline__ void df_rotate(float ch, float cl, float sh, float sl
   yl = nyl;
 }
 
+constexpr int kJacBlocks = 64 * 65 / 2;  // 2x2 blocks (pair a, pair b), a <= b, of a round
+
+// A is kept symmetric: entry {i, j} lives once, at row min(i, j), column
+// max(i, j) of the padded array.
+__device__ __forceinline__ int sym(int i, int j) { return i < j ? i * kLdA + j : j * kLdA + i; }
+
 __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const double* __restrict__ G, float* basis,
                                                              double* eigvals, unsigned int* err) {
   extern __shared__ __align__(128) uint8_t smem[];
-  float* Ah = reinterpret_cast<float*>(smem);                     // [128][129] high parts
+  float* Ah = reinterpret_cast<float*>(smem);                     // [128][129] high parts (upper triangle)
   float* Al = Ah + kHeadDim * kLdA;                                // [128][129] low parts
   float* V = Al + kHeadDim * kLdA;                                 // [128][129]
-  float* csh = V + kHeadDim * kLdA;                                // rotations of the round: c, s as pairs
-  float* csl = csh + 64;
-  float* snh = csl + 64;
-  float* snl = snh + 64;
-  int* pp = reinterpret_cast<int*>(snl + 64);
-  int* qq = pp + 64;
-  int* cnt = qq + 64;          // rotations this sweep
-  double* red = reinterpret_cast<double*>(cnt + 4);  // [kJacThreads]
-  int* order = reinterpret_cast<int*>(red + kJacThreads);  // [128]
-  auto a64 = [&](int i, int j) { return (double)Ah[i * kLdA + j] + (double)Al[i * kLdA + j]; };
+  float* rot = V + kHeadDim * kLdA;                                // [2][4][64]: c, s as pairs, two rounds
+  int* pq = reinterpret_cast<int*>(rot + 2 * 4 * 64);              // [2][2][64]: p, q, two rounds
+  int* cnt = pq + 2 * 2 * 64;                                      // rotations this sweep
+  double* red = reinterpret_cast<double*>(cnt + 4);                // [kJacThreads / 32]
+  int* order = reinterpret_cast<int*>(red + kJacThreads / 32);     // [128]
+  uint16_t* blk = reinterpret_cast<uint16_t*>(order + kHeadDim);  // [kJacBlocks]: a * 64 + b
+  auto a64 = [&](int i, int j) { return (double)Ah[sym(i, j)] + (double)Al[sym(i, j)]; };
 
-  const int tid = threadIdx.x, grp = blockIdx.x;
+  const int tid = threadIdx.x, grp = blockIdx.x, warp = tid >> 5, lane = tid & 31;
   const double* Gg = G + (size_t)grp * kHeadDim * kHeadDim;
   double fro = 0.0;
   for (int e = tid; e < kHeadDim * kHeadDim; e += kJacThreads) {
     const int i = e / kHeadDim, j = e % kHeadDim;
     const double a = Gg[e];
-    const float ah = (float)a;
-    Ah[i * kLdA + j] = ah;
-    Al[i * kLdA + j] = (float)(a - (double)ah);
+    if (i <= j) {
+      const float ah = (float)a;
+      Ah[i * kLdA + j] = ah;
+      Al[i * kLdA + j] = (float)(a - (double)ah);
+    }
     V[i * kLdA + j] = (i == j) ? 1.f : 0.f;
     fro += a * a;
   }
-  red[tid] = fro;
-  __syncthreads();
-  for (int s = kJacThreads / 2; s > 0; s >>= 1) {
-    if (tid < s) red[tid] += red[tid + s];
-    __syncthreads();
+  for (int a = tid; a < 64; a += kJacThreads) {
+    const int base = a * 64 - a * (a - 1) / 2;  // blocks (a, a..63) start here
+    for (int b = a; b < 64; ++b) blk[base + b - a] = (uint16_t)(a * 64 + b);
   }
-  // off-diagonal entries below these bounds are at the pairs' rounding level
-  const double floor_abs = kJacFloor * sqrt(red[0]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) fro += __shfl_xor_sync(0xffffffffu, fro, o);
+  if (lane == 0) red[warp] = fro;
+  if (tid == 0) *cnt = 0;
   __syncthreads();
+  double fro_all = 0.0;
+  for (int w = 0; w < kJacThreads / 32; ++w) fro_all += red[w];
+  // off-diagonal entries below these bounds are at the pairs' rounding level
+  const double floor_abs = kJacFloor * sqrt(fro_all);
 
-  int sweep = 0;
-  for (; sweep < kMaxSweeps; ++sweep) {
-    if (tid == 0) *cnt = 0;
-    __syncthreads();
-    for (int rnd = 0; rnd < kHeadDim - 1; ++rnd) {
+  // The rotations of round k (buffer k & 1) from the current A, by warps 0-1
+  // (an fp64 instruction costs a whole warp's issue on this part, active
+  // lanes or not, so the 64 angles go to two full warps).
+  auto angles = [&](int rnd, int buf) {
+    int p, q;
+    rr_pair(rnd, tid, p, q);
+    const double apq = a64(p, q), app = a64(p, p), aqq = a64(q, q);
+    double c = 1.0, s = 0.0;
+    if (fabs(apq) > fmax(kJacRel * sqrt(fabs(app * aqq)), floor_abs)) {
+      const double theta = (aqq - app) / (2.0 * apq);
+      const double t = (theta >= 0.0 ? 1.0 : -1.0) / (fabs(theta) + sqrt(theta * theta + 1.0));
+      c = 1.0 / sqrt(t * t + 1.0);
+      s = t * c;
+      atomicAdd(cnt, 1);
+    }
+    float* r = rot + buf * 256;
+    int* ix = pq + buf * 128;
+    ix[tid] = p;
+    ix[64 + tid] = q;
+    const float ch = (float)c, sh = (float)s;
+    r[tid] = ch;
+    r[64 + tid] = (float)(c - (double)ch);
+    r[128 + tid] = sh;
+    r[192 + tid] = (float)(s - (double)sh);
+  };
+  // V <- V J for the rotations in buffer buf, by threads from t0 on
+  auto rotate_v = [&](int buf, int t0) {
+    const float* r = rot + buf * 256;
+    const int* ix = pq + buf * 128;
+    for (int e = tid - t0; e < 64 * kHeadDim; e += kJacThreads - t0) {
+      const int i = e % 64, k = e / 64;
+      const float sf = r[128 + i];
+      if (sf != 0.f) {
+        const int p = ix[i], q = ix[64 + i];
+        const float cf = r[i];
+        const float vp = V[k * kLdA + p], vq = V[k * kLdA + q];
+        V[k * kLdA + p] = cf * vp - sf * vq;
+        V[k * kLdA + q] = sf * vp + cf * vq;
+      }
+    }
+  };
+
+  if (tid < 64) angles(0, 0);
+  __syncthreads();
+  int sweep = 0, done = 0, gr = 0;  // gr: rounds so far (a sweep has an odd number), picks the buffer
+  for (; sweep < kMaxSweeps && !done; ++sweep) {
+    for (int rnd = 0; rnd < kHeadDim - 1; ++rnd, ++gr) {
+      const int buf = gr & 1;
+      const float* r = rot + buf * 256;
+      const int* ix = pq + buf * 128;
+      // A <- J^T A J block by block: rows of pair a by its rotation, then
+      // columns of pair b by its rotation (the off-diagonal entry of a
+      // rotated pair is annihilated and set to 0)
+      for (int k = tid; k < kJacBlocks; k += kJacThreads) {
+        const int a = blk[k] >> 6, b = blk[k] & 63;
+        const bool ra = r[128 + a] != 0.f, rb = r[128 + b] != 0.f;
+        if (!ra && !rb) continue;
+        const int pa = ix[a], qa = ix[64 + a], pb = ix[b], qb = ix[64 + b];
+        const float cah = r[a], cal = r[64 + a], sah = r[128 + a], sal = r[192 + a];
+        if (a == b) {
+          const int ipp = pa * kLdA + pa, ipq = sym(pa, qa), iqq = qa * kLdA + qa;
+          float x00h = Ah[ipp], x00l = Al[ipp], x01h = Ah[ipq], x01l = Al[ipq], x11h = Ah[iqq], x11l = Al[iqq];
+          float x10h = x01h, x10l = x01l;
+          df_rotate(cah, cal, sah, sal, x00h, x00l, x10h, x10l);  // column p: rows p, q
+          df_rotate(cah, cal, sah, sal, x01h, x01l, x11h, x11l);  // column q
+          df_rotate(cah, cal, sah, sal, x00h, x00l, x01h, x01l);  // row p: columns p, q
+          df_rotate(cah, cal, sah, sal, x10h, x10l, x11h, x11l);  // row q
+          Ah[ipp] = x00h;
+          Al[ipp] = x00l;
+          Ah[iqq] = x11h;
+          Al[iqq] = x11l;
+          Ah[ipq] = 0.f;
+          Al[ipq] = 0.f;
+          continue;
+        }
+        const int i00 = sym(pa, pb), i01 = sym(pa, qb), i10 = sym(qa, pb), i11 = sym(qa, qb);
+        float x00h = Ah[i00], x00l = Al[i00], x01h = Ah[i01], x01l = Al[i01];
+        float x10h = Ah[i10], x10l = Al[i10], x11h = Ah[i11], x11l = Al[i11];
+        if (ra) {
+          df_rotate(cah, cal, sah, sal, x00h, x00l, x10h, x10l);
+          df_rotate(cah, cal, sah, sal, x01h, x01l, x11h, x11l);
+        }
+        if (rb) {
+          const float cbh = r[b], cbl = r[64 + b], sbh = r[128 + b], sbl = r[192 + b];
+          df_rotate(cbh, cbl, sbh, sbl, x00h, x00l, x01h, x01l);
+          df_rotate(cbh, cbl, sbh, sbl, x10h, x10l, x11h, x11l);
+        }
+        Ah[i00] = x00h;
+        Al[i00] = x00l;
+        Ah[i01] = x01h;
+        Al[i01] = x01l;
+        Ah[i10] = x10h;
+        Al[i10] = x10l;
+        Ah[i11] = x11h;
+        Al[i11] = x11l;
+      }
+      __syncthreads();
+      // next round's angles (warps 0-1) beside this round's V update (the rest)
+      const bool last = rnd == kHeadDim - 2;
+      if (last && tid == 0) {
+        done = *cnt == 0;  // read by thread 0 only, shared below
+        red[0] = done;
+        *cnt = 0;
+      }
+      if (last) __syncthreads();
+      if (last) done = red[0] != 0.0;
       if (tid < 64) {
-        int p, q;
-        rr_pair(rnd, tid, p, q);
-        const double apq = a64(p, q), app = a64(p, p), aqq = a64(q, q);
-        double c = 1.0, s = 0.0;
-        if (fabs(apq) > fmax(kJacRel * sqrt(fabs(app * aqq)), floor_abs)) {
-          const double theta = (aqq - app) / (2.0 * apq);
-          const double t = (theta >= 0.0 ? 1.0 : -1.0) / (fabs(theta) + sqrt(theta * theta + 1.0));
-          c = 1.0 / sqrt(t * t + 1.0);
-          s = t * c;
-          atomicAdd(cnt, 1);
-        }
-        pp[tid] = p;
-        qq[tid] = q;
-        const float ch = (float)c, sh = (float)s;
-        csh[tid] = ch;
-        csl[tid] = (float)(c - (double)ch);
-        snh[tid] = sh;
-        snl[tid] = (float)(s - (double)sh);
-      }
-      __syncthreads();
-      // A <- J^T A (rows p, q)
-      for (int e = tid; e < 64 * kHeadDim; e += kJacThreads) {
-        const int i = e / kHeadDim, k = e % kHeadDim;
-        if (snh[i] != 0.f) {
-          const int p = pp[i], q = qq[i];
-          float xh = Ah[p * kLdA + k], xl = Al[p * kLdA + k], yh = Ah[q * kLdA + k], yl = Al[q * kLdA + k];
-          df_rotate(csh[i], csl[i], snh[i], snl[i], xh, xl, yh, yl);
-          Ah[p * kLdA + k] = xh;
-          Al[p * kLdA + k] = xl;
-          Ah[q * kLdA + k] = yh;
-          Al[q * kLdA + k] = yl;
-        }
-      }
-      __syncthreads();
-      // A <- A J (columns p, q) and V <- V J
-      for (int e = tid; e < 64 * kHeadDim; e += kJacThreads) {
-        const int i = e % 64, k = e / 64;
-        if (snh[i] != 0.f) {
-          const int p = pp[i], q = qq[i];
-          float xh = Ah[k * kLdA + p], xl = Al[k * kLdA + p], yh = Ah[k * kLdA + q], yl = Al[k * kLdA + q];
-          df_rotate(csh[i], csl[i], snh[i], snl[i], xh, xl, yh, yl);
-          Ah[k * kLdA + p] = xh;
-          Al[k * kLdA + p] = xl;
-          Ah[k * kLdA + q] = yh;
-          Al[k * kLdA + q] = yl;
-          const float cf = csh[i], sf = snh[i];
-          const float vp = V[k * kLdA + p], vq = V[k * kLdA + q];
-          V[k * kLdA + p] = cf * vp - sf * vq;
-          V[k * kLdA + q] = sf * vp + cf * vq;
-        }
-      }
-      __syncthreads();
-      if (tid < 64 && snh[tid] != 0.f) {
-        Ah[pp[tid] * kLdA + qq[tid]] = 0.f;
-        Al[pp[tid] * kLdA + qq[tid]] = 0.f;
-        Ah[qq[tid] * kLdA + pp[tid]] = 0.f;
-        Al[qq[tid] * kLdA + pp[tid]] = 0.f;
+        if (!(last && (done || sweep + 1 == kMaxSweeps))) angles(last ? 0 : rnd + 1, buf ^ 1);
+      } else {
+        rotate_v(buf, 64);
       }
       __syncthreads();
     }
-    if (*cnt == 0) break;
-    __syncthreads();
   }
-  if (tid == 0 && sweep == kMaxSweeps) atomicOr(err, PALU_DEVERR_NOT_CONVERGED);
+  if (tid == 0 && !done) atomicOr(err, PALU_DEVERR_NOT_CONVERGED);
 
   // sort by descending eigenvalue (stable: ties keep index order)
   if (tid < kHeadDim) {
@@ -496,8 +550,8 @@ __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const double* __res
 }
 
 static size_t jacobi_smem() {
-  return 3 * sizeof(float) * kHeadDim * kLdA + sizeof(float) * 256 + sizeof(int) * 128 + sizeof(int) * 4 +
-         sizeof(double) * kJacThreads + sizeof(int) * kHeadDim;
+  return 3 * sizeof(float) * kHeadDim * kLdA + sizeof(float) * 2 * 256 + sizeof(int) * 2 * 128 + sizeof(int) * 4 +
+         sizeof(double) * (kJacThreads / 32) + sizeof(int) * kHeadDim + sizeof(uint16_t) * kJacBlocks;
 }
 
 struct FitLayout {
