@@ -291,31 +291,54 @@ def run_palu(args, w, world, rank, local):
     s = torch.cuda.Stream(device=dev)
     cap = S + EPISODE + 64
 
-    # ---- prefill: fit + encode each layer (untimed; layer 0 timed for "prefill")
+    # ---- prefill: the keys and values of every layer fitted in one
+    # palu_fit_batch call (timed), then each layer's caches built by one
+    # prefill append (layer 0's encode timed); layer 0's K and V also fitted
+    # alone by palu_fit (timed) for the per-layer figure
     caches = []
     fit_ms = enc_ms = None
-    ranks = None
+    roles = ((0, P.PALU_ROLE_KEY, w.rank_k), (1, P.PALU_ROLE_VALUE, w.rank_v))
+    cfgs = [P.palu_config_default(n_head_groups=w.n_groups, rank=rr, energy_threshold=w.energy_threshold,
+                                  quantize=1 if (tensor == 0 or w.quantize_values) else 0)
+            for _ in range(L) for tensor, _role, rr in roles]
     with torch.cuda.stream(s):
+        xs = [synth.prefill(w, l, tensor, device=dev) for l in range(L) for tensor, _r, _rr in roles]
+        fit_ws = torch.empty(P.palu_fit_batch_workspace_size(cfgs, w.batch, w.hkv, S), dtype=torch.uint8, device=dev)
+        D = 128
+        fb = [torch.empty(c.n_head_groups, D, D, dtype=torch.float32, device=dev) for c in cfgs]
+        fm = [torch.empty(c.n_head_groups, D, dtype=torch.float32, device=dev) for c in cfgs]
+        fe = [torch.empty(c.n_head_groups, D, dtype=torch.float64, device=dev) for c in cfgs]
+        torch.cuda.synchronize()
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(s)
+        branks, _ = P.palu_fit_batch(cfgs, xs, fit_ws, fb, fm, fe, stream=s)
+        b1.record(s)
+        torch.cuda.synchronize()
+        fit_batch_ms = b0.elapsed_time(b1)
+        del fit_ws
+        for tensor in range(2):  # layer 0 alone, as a single palu_fit per tensor
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            P.fit(cfgs[tensor], xs[tensor], stream=s)
+            e1.record(s)
+            torch.cuda.synchronize()
+            fit_ms = (fit_ms or 0) + e0.elapsed_time(e1)
         for l in range(L):
             pair = []
-            for tensor, role, rr in ((0, P.PALU_ROLE_KEY, w.rank_k), (1, P.PALU_ROLE_VALUE, w.rank_v)):
-                x = synth.prefill(w, l, tensor, device=dev)
-                cfg = P.palu_config_default(n_head_groups=w.n_groups, rank=rr, energy_threshold=w.energy_threshold,
-                                            quantize=1 if (tensor == 0 or w.quantize_values) else 0)
-                e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-                e0.record(s)
-                basis, mu, eig, r, _ = P.fit(cfg, x, stream=s)
+            for tensor, role, _rr in roles:
+                i = 2 * l + tensor
+                e1, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e1.record(s)
-                c = P.LatentCache(cfg, role, r, w.batch, w.hkv, cap, basis, mu, stream=s)
-                c.append(x, stream=s)
+                c = P.LatentCache(cfgs[i], role, branks[i], w.batch, w.hkv, cap, fb[i], fm[i], stream=s)
+                c.append(xs[i], stream=s)
                 e2.record(s)
                 torch.cuda.synchronize()
                 if l == 0:
-                    fit_ms = (fit_ms or 0) + e0.elapsed_time(e1)
                     enc_ms = (enc_ms or 0) + e1.elapsed_time(e2)
                 pair.append(c)
-                del x, basis, mu, eig
+                xs[i] = None
             caches.append(pair)
+        del xs, fb, fm, fe
         torch.cuda.synchronize()
     kc0, vc0 = caches[0]
     layer_ranks = [(kc.c.rank, kc.c.n_hi, vc.c.rank, vc.c.n_hi) for kc, vc in caches]
@@ -482,6 +505,7 @@ def run_palu(args, w, world, rank, local):
                      "launches_timed": n_launch},
         "clocks": clk.summary(),
         "prefill": {"fit_ms_layer0_kv": fit_ms, "encode_ms_layer0_kv": enc_ms,
+                    "fit_ms_all_layers_batched": fit_batch_ms, "fit_batched_tensors": 2 * L,
                     "prefill_tokens_per_layer": w.batch * S},
         "bits": {"effective_bits_k": stats_k["effective_bits"], "effective_bits_v": stats_v["effective_bits"],
                  "assigned_avg_bits": max(stats_k["effective_bits"], stats_v["effective_bits"]),

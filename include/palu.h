@@ -143,6 +143,29 @@ palu_status palu_fit(const palu_config* cfg, const void* x, int64_t batch, int32
                      float* mu, double* eigvals, int32_t* rank_out, int32_t* group_ranks,
                      void* stream);
 
+/* Fit n_tensors tensors of the same shape in one call (for example the keys
+ * and values of every layer after a prefill): every tensor's Gram matrices
+ * first, then one eigensolve launch over all their head groups (one SM per
+ * group, up to 256 groups a launch), then one synchronisation of `stream`.
+ * The outputs equal those of palu_fit on each tensor alone.
+ *   cfgs       host [n_tensors] configurations (each its own grouping,
+ *              rank rule and threshold).
+ *   x, basis, mu, eigvals  host [n_tensors] arrays of device pointers, each
+ *              as in palu_fit.
+ *   rank_out   host int32 [n_tensors].
+ *   group_ranks host int32 [sum of n_head_groups], tensor after tensor (may
+ *              be NULL).
+ *   workspace  device, 256-byte aligned, at least
+ *              palu_fit_batch_workspace_size bytes.
+ * Errors: argument errors before any launch; PALU_ERR_DEVICE if an
+ * eigensolve did not converge (the first such tensor is reported). */
+palu_status palu_fit_batch_workspace_size(const palu_config* cfgs, int32_t n_tensors, int64_t batch,
+                                          int32_t kv_heads, int64_t seq, size_t* bytes);
+palu_status palu_fit_batch(const palu_config* cfgs, int32_t n_tensors, const void* const* x, int64_t batch,
+                           int32_t kv_heads, int64_t seq, void* workspace, size_t workspace_bytes,
+                           float* const* basis, float* const* mu, double* const* eigvals, int32_t* rank_out,
+                           int32_t* group_ranks, void* stream);
+
 /* Byte sizes of the three device buffers of a cache (all 256-byte aligned
  * sizes): block records, fp32 tail (0 for unquantized values) and state. */
 palu_status palu_cache_size(const palu_config* cfg, int32_t role, int32_t rank, int64_t batch,

@@ -29,6 +29,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <cstring>
 #include <vector>
 
 #include "palu_internal.cuh"
@@ -361,8 +362,20 @@ constexpr int kJacBlocks = 64 * 65 / 2;  // 2x2 blocks (pair a, pair b), a <= b,
 // max(i, j) of the padded array.
 __device__ __forceinline__ int sym(int i, int j) { return i < j ? i * kLdA + j : j * kLdA + i; }
 
-__global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const double* __restrict__ G, float* basis,
-                                                             double* eigvals, unsigned int* err) {
+// The matrices of one Jacobi launch: CTA i diagonalises matrix i (a head
+// group of one fitted tensor) and writes its sorted basis and eigenvalues.
+constexpr int kMaxJacBatch = 256;
+struct JacMatrix {
+  const double* G;        // [128][128] centred Gram matrix
+  float* basis;           // [128][128]
+  double* eigvals;        // [128]
+  unsigned int* err;      // the tensor's device error word
+};
+struct JacBatch {
+  JacMatrix m[kMaxJacBatch];
+};
+
+__global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const __grid_constant__ JacBatch jb) {
   extern __shared__ __align__(128) uint8_t smem[];
   float* Ah = reinterpret_cast<float*>(smem);                     // [128][129] high parts (upper triangle)
   float* Al = Ah + kHeadDim * kLdA;                                // [128][129] low parts
@@ -375,8 +388,9 @@ __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const double* __res
   uint16_t* blk = reinterpret_cast<uint16_t*>(order + kHeadDim);  // [kJacBlocks]: a * 64 + b
   auto a64 = [&](int i, int j) { return (double)Ah[sym(i, j)] + (double)Al[sym(i, j)]; };
 
-  const int tid = threadIdx.x, grp = blockIdx.x, warp = tid >> 5, lane = tid & 31;
-  const double* Gg = G + (size_t)grp * kHeadDim * kHeadDim;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const JacMatrix& mat = jb.m[blockIdx.x];
+  const double* Gg = mat.G;
   double fro = 0.0;
   for (int e = tid; e < kHeadDim * kHeadDim; e += kJacThreads) {
     const int i = e / kHeadDim, j = e % kHeadDim;
@@ -517,7 +531,7 @@ __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const double* __res
       __syncthreads();
     }
   }
-  if (tid == 0 && !done) atomicOr(err, PALU_DEVERR_NOT_CONVERGED);
+  if (tid == 0 && !done) atomicOr(mat.err, PALU_DEVERR_NOT_CONVERGED);
 
   // sort by descending eigenvalue (stable: ties keep index order)
   if (tid < kHeadDim) {
@@ -543,9 +557,9 @@ __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const double* __res
       }
     }
     const float sgn = V[arg * kLdA + src] < 0.f ? -1.f : 1.f;
-    float* bg = basis + (size_t)grp * kHeadDim * kHeadDim;
+    float* bg = mat.basis;
     for (int d = 0; d < kHeadDim; ++d) bg[d * kHeadDim + tid] = sgn * V[d * kLdA + src];
-    eigvals[(size_t)grp * kHeadDim + tid] = fmax(a64(src, src), 0.0);
+    mat.eigvals[tid] = fmax(a64(src, src), 0.0);
   }
 }
 
@@ -615,46 +629,27 @@ static palu_status check_fit_args(const palu_config* cfg, int64_t batch, int32_t
 
 using namespace palu;
 
-extern "C" palu_status palu_fit_workspace_size(const palu_config* cfg, int64_t batch, int32_t kv_heads, int64_t seq,
-                                               size_t* bytes) {
-  palu_status st = check_fit_args(cfg, batch, kv_heads, seq);
-  if (st != PALU_OK) return st;
-  if (!bytes) return fail(PALU_ERR_INVALID_ARG, "bytes is NULL");
-  *bytes = fit_layout(cfg->n_head_groups, batch * (long long)(kv_heads / cfg->n_head_groups) * seq).total;
-  return PALU_OK;
-}
+namespace palu {
 
-extern "C" palu_status palu_fit(const palu_config* cfg, const void* x, int64_t batch, int32_t kv_heads, int64_t seq,
-                                void* workspace, size_t workspace_bytes, float* basis, float* mu, double* eigvals,
-                                int32_t* rank_out, int32_t* group_ranks, void* stream) {
-  palu_status st = check_fit_args(cfg, batch, kv_heads, seq);
-  if (st != PALU_OK) return st;
-  if (!x || !workspace || !basis || !mu || !eigvals || !rank_out)
-    return fail(PALU_ERR_INVALID_ARG, "x, workspace, basis, mu, eigvals and rank_out must be non-NULL");
-  if (((uintptr_t)x & 15) || ((uintptr_t)workspace & 255))
-    return fail(PALU_ERR_INVALID_ARG, "x must be 16-byte and workspace 256-byte aligned");
+// Gram matrix and mean of one tensor's head groups (prefill steps 1-2): the
+// partial sums go to part / colpart (shared by the tensors of a batch, which
+// run one after the other on the stream), the fp64 reduction to G and mu.
+static palu_status launch_gram(const palu_config* cfg, const void* x, int64_t batch, int32_t kv_heads, int64_t seq,
+                               const FitLayout& fl, uint8_t* part_ws, double* G, float* mu, cudaStream_t strm) {
   const int ng = cfg->n_head_groups;
   const int hg = kv_heads / ng;
   const long long rows_g = batch * (long long)hg * seq;
-  const FitLayout fl = fit_layout(ng, rows_g);
-  if (workspace_bytes < fl.total)
-    return fail(PALU_ERR_INVALID_ARG, "fit workspace too small: need " + std::to_string(fl.total) + " bytes");
-  cudaStream_t strm = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  unsigned int* err = reinterpret_cast<unsigned int*>(ws + fl.err_off);
-  st = cuda_check(cudaMemsetAsync(err, 0, sizeof(unsigned int), strm), "memset");
-  if (st != PALU_OK) return st;
-
   GramParams gp;
   gp.x = static_cast<const __half*>(x);
-  gp.part = reinterpret_cast<float*>(ws + fl.part_off);
-  gp.colpart = reinterpret_cast<float*>(ws + fl.col_off);
+  gp.part = reinterpret_cast<float*>(part_ws + fl.part_off);
+  gp.colpart = reinterpret_cast<float*>(part_ws + fl.col_off);
   gp.seq = seq;
   gp.rows_g = rows_g;
   gp.Hkv = kv_heads;
   gp.hg = hg;
   gp.n_chunks = fl.n_chunks;
   gp.chunk_rows = fl.chunk_rows;
+  palu_status st;
   if (rows_g <= kExactGramRows) {
     gram_exact_kernel<<<dim3(fl.n_chunks, ng), 256, 0, strm>>>(gp);
   } else {
@@ -666,33 +661,63 @@ extern "C" palu_status palu_fit(const palu_config* cfg, const void* x, int64_t b
   }
   st = cuda_check(cudaGetLastError(), "gram_kernel launch");
   if (st != PALU_OK) return st;
-  double* G = reinterpret_cast<double*>(ws + fl.G_off);
   gram_reduce_kernel<<<dim3(kHeadDim * kHeadDim / 256, ng), 256, 0, strm>>>(gp.part, gp.colpart, fl.n_chunks,
                                                                              (double)rows_g, G, mu);
-  st = cuda_check(cudaGetLastError(), "gram_reduce_kernel launch");
-  if (st != PALU_OK) return st;
+  return cuda_check(cudaGetLastError(), "gram_reduce_kernel launch");
+}
+
+// Diagonalise the listed matrices, kMaxJacBatch per launch (one CTA, one SM,
+// each).
+static palu_status launch_jacobi(const std::vector<JacMatrix>& mats, cudaStream_t strm) {
   const size_t jsm = jacobi_smem();
-  {
-    int per_sm = 0;
-    st = kernel_occupancy(reinterpret_cast<const void*>(jacobi_kernel), kJacThreads, (int)jsm, &per_sm);
+  int per_sm = 0;
+  palu_status st = kernel_occupancy(reinterpret_cast<const void*>(jacobi_kernel), kJacThreads, (int)jsm, &per_sm);
+  if (st != PALU_OK) return st;
+  for (size_t i0 = 0; i0 < mats.size(); i0 += kMaxJacBatch) {
+    JacBatch jb;
+    std::memset(&jb, 0, sizeof(jb));
+    const size_t n = std::min<size_t>(kMaxJacBatch, mats.size() - i0);
+    for (size_t i = 0; i < n; ++i) jb.m[i] = mats[i0 + i];
+    jacobi_kernel<<<(unsigned)n, kJacThreads, jsm, strm>>>(jb);
+    st = cuda_check(cudaGetLastError(), "jacobi_kernel launch");
     if (st != PALU_OK) return st;
   }
-  jacobi_kernel<<<ng, kJacThreads, jsm, strm>>>(G, basis, eigvals, err);
-  st = cuda_check(cudaGetLastError(), "jacobi_kernel launch");
-  if (st != PALU_OK) return st;
+  return PALU_OK;
+}
 
-  std::vector<double> lam((size_t)ng * kHeadDim);
-  unsigned int herr = 0;
-  st = cuda_check(cudaMemcpyAsync(lam.data(), eigvals, sizeof(double) * lam.size(), cudaMemcpyDeviceToHost, strm),
-                  "copy eigenvalues");
-  if (st != PALU_OK) return st;
-  st = cuda_check(cudaMemcpyAsync(&herr, err, sizeof(herr), cudaMemcpyDeviceToHost, strm), "copy error word");
-  if (st != PALU_OK) return st;
-  st = cuda_check(cudaStreamSynchronize(strm), "cudaStreamSynchronize(fit)");
-  if (st != PALU_OK) return st;
+// Workspace of a batch: one partial-sum area (the largest any tensor needs),
+// then per tensor its Gram matrices and error word.
+struct BatchLayout {
+  size_t part_bytes;
+  std::vector<FitLayout> fl;
+  std::vector<size_t> g_off, err_off;
+  size_t total;
+};
+static BatchLayout batch_layout(const palu_config* cfgs, int n, int64_t batch, int32_t kv_heads, int64_t seq) {
+  BatchLayout b;
+  b.part_bytes = 0;
+  for (int t = 0; t < n; ++t) {
+    const int ng = cfgs[t].n_head_groups;
+    b.fl.push_back(fit_layout(ng, batch * (long long)(kv_heads / ng) * seq));
+    b.part_bytes = std::max(b.part_bytes, b.fl.back().G_off);
+  }
+  size_t o = align_up(b.part_bytes, 256);
+  for (int t = 0; t < n; ++t) {
+    b.g_off.push_back(o);
+    o = align_up(o + sizeof(double) * (size_t)cfgs[t].n_head_groups * kHeadDim * kHeadDim, 256);
+    b.err_off.push_back(o);
+    o += 256;
+  }
+  b.total = o;
+  return b;
+}
+
+// Ranks from the eigenvalues (prefill step 3) once the stream has finished.
+static palu_status finish_ranks(const palu_config* cfg, const std::vector<double>& lam, unsigned int herr,
+                                int32_t* rank_out, int32_t* group_ranks) {
   if (herr) return fail(PALU_ERR_DEVICE, "eigen-solver did not converge within its sweep limit");
   int rmin = kHeadDim;
-  for (int g = 0; g < ng; ++g) {
+  for (int g = 0; g < cfg->n_head_groups; ++g) {
     const int rg = cfg->rank > 0 ? std::min(cfg->rank, kHeadDim)
                                  : energy_rank(lam.data() + (size_t)g * kHeadDim, kHeadDim, cfg->energy_threshold,
                                                cfg->energy_mode);
@@ -701,4 +726,103 @@ extern "C" palu_status palu_fit(const palu_config* cfg, const void* x, int64_t b
   }
   *rank_out = rmin;
   return PALU_OK;
+}
+
+// Fit n tensors of equal shape: every tensor's Gram matrices first, then one
+// Jacobi launch over all their head groups, then one synchronisation.
+static palu_status fit_many(const palu_config* cfgs, int n, const void* const* xs, int64_t batch, int32_t kv_heads,
+                            int64_t seq, void* workspace, size_t workspace_bytes, float* const* bases,
+                            float* const* mus, double* const* eigvals, int32_t* ranks_out, int32_t* group_ranks,
+                            void* stream) {
+  if (n < 1) return fail(PALU_ERR_INVALID_ARG, "n_tensors must be >= 1");
+  if (!cfgs || !xs || !bases || !mus || !eigvals || !ranks_out)
+    return fail(PALU_ERR_INVALID_ARG, "configs, x, basis, mu, eigvals and rank_out arrays must be non-NULL");
+  for (int t = 0; t < n; ++t) {
+    palu_status st = check_fit_args(&cfgs[t], batch, kv_heads, seq);
+    if (st != PALU_OK) return st;
+    if (!xs[t] || !bases[t] || !mus[t] || !eigvals[t])
+      return fail(PALU_ERR_INVALID_ARG, "x, basis, mu and eigvals must be non-NULL for every tensor");
+    if ((uintptr_t)xs[t] & 15) return fail(PALU_ERR_INVALID_ARG, "x must be 16-byte aligned");
+  }
+  if (!workspace || ((uintptr_t)workspace & 255))
+    return fail(PALU_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
+  const BatchLayout bl = batch_layout(cfgs, n, batch, kv_heads, seq);
+  if (workspace_bytes < bl.total)
+    return fail(PALU_ERR_INVALID_ARG, "fit workspace too small: need " + std::to_string(bl.total) + " bytes");
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  std::vector<JacMatrix> mats;
+  for (int t = 0; t < n; ++t) {
+    unsigned int* err = reinterpret_cast<unsigned int*>(ws + bl.err_off[t]);
+    palu_status st = cuda_check(cudaMemsetAsync(err, 0, sizeof(unsigned int), strm), "memset");
+    if (st != PALU_OK) return st;
+    double* G = reinterpret_cast<double*>(ws + bl.g_off[t]);
+    st = launch_gram(&cfgs[t], xs[t], batch, kv_heads, seq, bl.fl[t], ws, G, mus[t], strm);
+    if (st != PALU_OK) return st;
+    for (int g = 0; g < cfgs[t].n_head_groups; ++g)
+      mats.push_back(JacMatrix{G + (size_t)g * kHeadDim * kHeadDim, bases[t] + (size_t)g * kHeadDim * kHeadDim,
+                               eigvals[t] + (size_t)g * kHeadDim, err});
+  }
+  palu_status st = launch_jacobi(mats, strm);
+  if (st != PALU_OK) return st;
+  std::vector<std::vector<double>> lam(n);
+  std::vector<unsigned int> herr(n, 0u);
+  for (int t = 0; t < n; ++t) {
+    lam[t].resize((size_t)cfgs[t].n_head_groups * kHeadDim);
+    st = cuda_check(cudaMemcpyAsync(lam[t].data(), eigvals[t], sizeof(double) * lam[t].size(), cudaMemcpyDeviceToHost,
+                                    strm),
+                    "copy eigenvalues");
+    if (st != PALU_OK) return st;
+    st = cuda_check(cudaMemcpyAsync(&herr[t], ws + bl.err_off[t], sizeof(unsigned int), cudaMemcpyDeviceToHost, strm),
+                    "copy error word");
+    if (st != PALU_OK) return st;
+  }
+  st = cuda_check(cudaStreamSynchronize(strm), "cudaStreamSynchronize(fit)");
+  if (st != PALU_OK) return st;
+  size_t goff = 0;
+  for (int t = 0; t < n; ++t) {
+    st = finish_ranks(&cfgs[t], lam[t], herr[t], &ranks_out[t], group_ranks ? group_ranks + goff : nullptr);
+    if (st != PALU_OK) return st;
+    goff += cfgs[t].n_head_groups;
+  }
+  return PALU_OK;
+}
+
+}  // namespace palu
+
+extern "C" palu_status palu_fit_workspace_size(const palu_config* cfg, int64_t batch, int32_t kv_heads, int64_t seq,
+                                               size_t* bytes) {
+  palu_status st = check_fit_args(cfg, batch, kv_heads, seq);
+  if (st != PALU_OK) return st;
+  if (!bytes) return fail(PALU_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = batch_layout(cfg, 1, batch, kv_heads, seq).total;
+  return PALU_OK;
+}
+
+extern "C" palu_status palu_fit(const palu_config* cfg, const void* x, int64_t batch, int32_t kv_heads, int64_t seq,
+                                void* workspace, size_t workspace_bytes, float* basis, float* mu, double* eigvals,
+                                int32_t* rank_out, int32_t* group_ranks, void* stream) {
+  if (!cfg) return fail(PALU_ERR_INVALID_ARG, "config is NULL");
+  return fit_many(cfg, 1, &x, batch, kv_heads, seq, workspace, workspace_bytes, &basis, &mu, &eigvals, rank_out,
+                  group_ranks, stream);
+}
+
+extern "C" palu_status palu_fit_batch_workspace_size(const palu_config* cfgs, int32_t n_tensors, int64_t batch,
+                                                     int32_t kv_heads, int64_t seq, size_t* bytes) {
+  if (!cfgs || n_tensors < 1) return fail(PALU_ERR_INVALID_ARG, "configs must be non-NULL and n_tensors >= 1");
+  for (int t = 0; t < n_tensors; ++t) {
+    palu_status st = check_fit_args(&cfgs[t], batch, kv_heads, seq);
+    if (st != PALU_OK) return st;
+  }
+  if (!bytes) return fail(PALU_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = batch_layout(cfgs, n_tensors, batch, kv_heads, seq).total;
+  return PALU_OK;
+}
+
+extern "C" palu_status palu_fit_batch(const palu_config* cfgs, int32_t n_tensors, const void* const* x, int64_t batch,
+                                      int32_t kv_heads, int64_t seq, void* workspace, size_t workspace_bytes,
+                                      float* const* basis, float* const* mu, double* const* eigvals,
+                                      int32_t* rank_out, int32_t* group_ranks, void* stream) {
+  return fit_many(cfgs, n_tensors, x, batch, kv_heads, seq, workspace, workspace_bytes, basis, mu, eigvals, rank_out,
+                  group_ranks, stream);
 }

@@ -71,6 +71,10 @@ _SIGNATURES = {
     "palu_fit_workspace_size": (c_int32, [_P(palu_config), c_int64, c_int32, c_int64, _P(c_size_t)]),
     "palu_fit": (c_int32, [_P(palu_config), c_void_p, c_int64, c_int32, c_int64, c_void_p, c_size_t, c_void_p,
                            c_void_p, c_void_p, _P(c_int32), _P(c_int32), c_void_p]),
+    "palu_fit_batch_workspace_size": (c_int32, [_P(palu_config), c_int32, c_int64, c_int32, c_int64, _P(c_size_t)]),
+    "palu_fit_batch": (c_int32, [_P(palu_config), c_int32, _P(c_void_p), c_int64, c_int32, c_int64, c_void_p,
+                                 c_size_t, _P(c_void_p), _P(c_void_p), _P(c_void_p), _P(c_int32), _P(c_int32),
+                                 c_void_p]),
     "palu_cache_size": (c_int32, [_P(palu_config), c_int32, c_int32, c_int64, c_int32, c_int64, _P(c_size_t),
                                   _P(c_size_t), _P(c_size_t)]),
     "palu_cache_init": (c_int32, [_P(palu_cache), _P(palu_config), c_int32, c_int32, c_int64, c_int32, c_int64,
@@ -185,6 +189,32 @@ def palu_fit(cfg, x, workspace, basis, mu, eigvals, stream=None):
     _check(lib().palu_fit(ctypes.byref(cfg), _ptr(x), B, H, S, _ptr(workspace), workspace.numel() * workspace.element_size(),
                           _ptr(basis), _ptr(mu), _ptr(eigvals), ctypes.byref(r), gr, _stream(stream)))
     return r.value, list(gr)
+
+
+def palu_fit_batch_workspace_size(cfgs, batch, kv_heads, seq):
+    arr = (palu_config * len(cfgs))(*cfgs)
+    n = c_size_t()
+    _check(lib().palu_fit_batch_workspace_size(arr, len(cfgs), batch, kv_heads, seq, ctypes.byref(n)))
+    return n.value
+
+
+def palu_fit_batch(cfgs, xs, workspace, bases, mus, eigvals, stream=None):
+    """Fit len(cfgs) tensors of one shape (xs fp16 [B, Hkv, S, D] each) in one call; outputs as
+    palu_fit, per tensor.  Returns (ranks, group_ranks per tensor)."""
+    n = len(cfgs)
+    B, H, S, _ = xs[0].shape
+    arr = (palu_config * n)(*cfgs)
+    vp = lambda ts: (c_void_p * n)(*[t.data_ptr() for t in ts])
+    r = (c_int32 * n)()
+    ng = [c.n_head_groups for c in cfgs]
+    gr = (c_int32 * sum(ng))()
+    _check(lib().palu_fit_batch(arr, n, vp(xs), B, H, S, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                vp(bases), vp(mus), vp(eigvals), r, gr, _stream(stream)))
+    out, o = [], 0
+    for g in ng:
+        out.append(list(gr[o:o + g]))
+        o += g
+    return list(r), out
 
 
 def palu_cache_size(cfg, role, rank, batch, kv_heads, capacity):
@@ -517,6 +547,19 @@ def fit(cfg, x, stream=None):
     eig = torch.empty(ng, D, dtype=torch.float64, device=x.device)
     r, gr = palu_fit(cfg, x, ws, basis, mu, eig, stream)
     return basis, mu, eig, r, gr
+
+
+def fit_batch(cfgs, xs, stream=None):
+    """Run palu_fit_batch on tensors xs (fp16 [B, Hkv, S, D], one shape) with configurations cfgs;
+    returns [(basis, mu, eigvals, rank, group_ranks)] per tensor."""
+    B, H, S, D = xs[0].shape
+    dev = xs[0].device
+    ws = _dev_bytes(palu_fit_batch_workspace_size(cfgs, B, H, S), dev)
+    bases = [torch.empty(c.n_head_groups, D, D, dtype=torch.float32, device=dev) for c in cfgs]
+    mus = [torch.empty(c.n_head_groups, D, dtype=torch.float32, device=dev) for c in cfgs]
+    eigs = [torch.empty(c.n_head_groups, D, dtype=torch.float64, device=dev) for c in cfgs]
+    ranks, grs = palu_fit_batch(cfgs, xs, ws, bases, mus, eigs, stream)
+    return [(bases[i], mus[i], eigs[i], ranks[i], grs[i]) for i in range(len(cfgs))]
 
 
 def decode(kc: LatentCache, vc: LatentCache, q, out_dtype=torch.float32, softmax_scale=0.0, stream=None,
