@@ -59,50 +59,83 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int ch) {
   return base + row * 256 + ((ch ^ (row & 7)) << 4);
 }
 
+// grid (chunks, groups, 3): CTA z computes the 64 x 64 block (rb, cb) of the
+// chunk's X^T X with (rb, cb) = (0, 0), (0, 1), (1, 1) for z = 0, 1, 2 (the
+// matrix is symmetric: block (1, 0) is written as the transpose of (0, 1)),
+// and the CTAs of the diagonal blocks the column sums of their 64 features.
+// Rows stream through a 3-stage cp.async ring (only the 16-byte chunks of
+// the features a block needs).  8 warps of 32 x 16 C each.
 __global__ void __launch_bounds__(kGramThreads) gram_kernel(const GramParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, c4 = lane & 3;
-  const int chunk = blockIdx.x, grp = blockIdx.y;
+  const int chunk = blockIdx.x, grp = blockIdx.y, z = blockIdx.z;
+  const int rb = z == 2 ? 1 : 0, cb = z == 0 ? 0 : 1;
   const long long R0 = (long long)chunk * p.chunk_rows;
   const long long R1 = min(R0 + p.chunk_rows, p.rows_g);
   const int n_tiles = (int)((R1 - R0 + kGramTile - 1) / kGramTile);
   const uint32_t sbase = smem_addr(smem);
 
+  // This thread's copy slots: rows (tid >> 4) + 16 i of each tile, chunk
+  // tid & 15.  Each row's (batch, head in group, token) position advances
+  // by 64 rows a tile with carries, instead of a division per copy.
+  constexpr int kRowsPer = (kGramTile * 16) / kGramThreads;
+  const int ch = tid & 15;
+  const bool want = z == 1 || (ch >> 3) == rb;  // a diagonal block reads its own 64 features
+  int cb_[kRowsPer], ch_[kRowsPer], ct_[kRowsPer];  // batch, head in group, token of the slot's row
+#pragma unroll
+  for (int i = 0; i < kRowsPer; ++i) {
+    const long long R = R0 + (tid >> 4) + 16 * i;
+    const long long bh = R / p.seq;
+    ct_[i] = (int)(R - bh * p.seq);
+    cb_[i] = (int)(bh / p.hg);
+    ch_[i] = (int)(bh - (long long)cb_[i] * p.hg);
+  }
   auto load_tile = [&](int tile, int stage) {
 #pragma unroll
-    for (int i = 0; i < (kGramTile * 16) / kGramThreads; ++i) {
-      const int idx = tid + i * kGramThreads;
-      const int row = idx >> 4, ch = idx & 15;
+    for (int i = 0; i < kRowsPer; ++i) {
+      const int row = (tid >> 4) + 16 * i;
       const long long R = R0 + (long long)tile * kGramTile + row;
       const bool valid = R < R1;
-      const long long Rc = valid ? R : R0;
-      const long long bb = Rc / ((long long)p.hg * p.seq);
-      const long long rem = Rc % ((long long)p.hg * p.seq);
-      const long long hh = rem / p.seq, t = rem % p.seq;
-      const __half* src = p.x + ((bb * p.Hkv + (long long)grp * p.hg + hh) * p.seq + t) * kHeadDim + ch * 8;
-      uint8_t* dst = smem + stage * (kGramTile * 256) + row * 256 + ((ch ^ (row & 7)) << 4);
-      cp_async16_zfill(dst, src, valid);
+      if (want) {
+        const __half* src = valid ? p.x + (((long long)cb_[i] * p.Hkv + (long long)grp * p.hg + ch_[i]) * p.seq + ct_[i]) *
+                                            kHeadDim + ch * 8
+                                  : p.x;
+        uint8_t* dst = smem + stage * (kGramTile * 256) + row * 256 + ((ch ^ (row & 7)) << 4);
+        cp_async16_zfill(dst, src, valid);
+      }
+      // advance the slot's row by one tile
+      ct_[i] += kGramTile;
+      while (ct_[i] >= p.seq) {
+        ct_[i] -= (int)p.seq;
+        if (++ch_[i] == p.hg) {
+          ch_[i] = 0;
+          ++cb_[i];
+        }
+      }
     }
   };
 
-  const int wm = warp >> 1, wn = warp & 1;  // C rows [32 wm, +32), cols [64 wn, +64)
-  // Each 16-row tensor-core product starts from a zero accumulator and is then
-  // added into an unevaluated fp32 pair (hi, lo) with an error-free sum, so
-  // the only rounding left is that of one 16-term product sum: long fp32
+  const int wm = warp >> 2, wn = warp & 3;
+  const int mbase = 64 * rb + 32 * wm, nbase = 64 * cb + 16 * wn;  // this warp's C rows / columns
+  // Each stage's 64-row product sum (four chained 16-row MMAs) starts from a
+  // zero accumulator and is then added into an unevaluated fp32 pair (hi, lo)
+  // with an error-free sum: the rounding left is that of one 64-term product
+  // sum, a random walk of sqrt(4) times a 16-term sum's; long fp32
   // accumulation chains would lose the ~1e-9 relative accuracy the trailing
   // retained directions of a decaying spectrum need.
-  float Ch[2][8][4], Cl[2][8][4];
+  float Ch[2][2][4], Cl[2][2][4];
 #pragma unroll
   for (int a = 0; a < 2; ++a)
 #pragma unroll
-    for (int b = 0; b < 8; ++b)
+    for (int b = 0; b < 2; ++b)
 #pragma unroll
       for (int e = 0; e < 4; ++e) Ch[a][b][e] = Cl[a][b][e] = 0.f;
-  float Sh[2][4], Sl[2][4];  // column sums: X^T * ones (kept by warps with wn == 0)
+  float Sh[2][4], Sl[2][4];  // column sums: X^T * ones (warps with wn == 0 of a diagonal block)
 #pragma unroll
   for (int a = 0; a < 2; ++a)
 #pragma unroll
     for (int e = 0; e < 4; ++e) Sh[a][e] = Sl[a][e] = 0.f;
+  const bool sums = z != 1 && wn == 0;
   const uint32_t ones = (g8 == 0) ? 0x3C003C00u : 0u;  // B[k][n] = 1 for n = 0
 
 #pragma unroll
@@ -118,53 +151,59 @@ __global__ void __launch_bounds__(kGramThreads) gram_kernel(const GramParams p) 
     cp_async_commit();
     const uint32_t st = sbase + (tile % kGramStages) * (kGramTile * 256);
     const int mat = lane >> 3, rr = lane & 7;
-#pragma unroll 1
+    float T[2][2][4], U[2][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        T[a][0][e] = T[a][1][e] = 0.f;
+        U[a][e] = 0.f;
+      }
+#pragma unroll
     for (int ks = 0; ks < kGramTile / 16; ++ks) {
       const int k0 = 16 * ks;
       uint32_t A[2][4];
 #pragma unroll
       for (int mi = 0; mi < 2; ++mi) {
-        const int m0 = 32 * wm + 16 * mi;
+        const int m0 = mbase + 16 * mi;
         // matrices: (k0-7, m0-7), (k0-7, m8-15), (k8-15, m0-7), (k8-15, m8-15)
         const int row = k0 + rr + ((mat >> 1) << 3);
         const int ch = (m0 >> 3) + (mat & 1);
         ldsm_x4_t(A[mi][0], A[mi][1], A[mi][2], A[mi][3], tile_addr(st, row, ch));
       }
-      uint32_t Bf[8][2];
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        const int n0 = 64 * wn + 16 * np;
+      uint32_t Bf[2][2];
+      {
         // matrices: (k0-7, n0-7), (k8-15, n0-7), (k0-7, n8-15), (k8-15, n8-15)
         const int row = k0 + rr + ((mat & 1) << 3);
-        const int ch = (n0 >> 3) + (mat >> 1);
-        ldsm_x4_t(Bf[2 * np][0], Bf[2 * np][1], Bf[2 * np + 1][0], Bf[2 * np + 1][1], tile_addr(st, row, ch));
+        const int ch = (nbase >> 3) + (mat >> 1);
+        ldsm_x4_t(Bf[0][0], Bf[0][1], Bf[1][0], Bf[1][1], tile_addr(st, row, ch));
       }
 #pragma unroll
       for (int mi = 0; mi < 2; ++mi) {
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-          float T[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_f16(T, A[mi][0], A[mi][1], A[mi][2], A[mi][3], Bf[nt][0], Bf[nt][1]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float s, err;
-            two_sum(Ch[mi][nt][e], T[e], s, err);
-            Ch[mi][nt][e] = s;
-            Cl[mi][nt][e] = __fadd_rn(Cl[mi][nt][e], err);
-          }
-        }
-        if (wn == 0) {
-          float T[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_f16(T, A[mi][0], A[mi][1], A[mi][2], A[mi][3], ones, ones);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float s, err;
-            two_sum(Sh[mi][e], T[e], s, err);
-            Sh[mi][e] = s;
-            Sl[mi][e] = __fadd_rn(Sl[mi][e], err);
-          }
-        }
+        for (int nt = 0; nt < 2; ++nt) mma_f16(T[mi][nt], A[mi][0], A[mi][1], A[mi][2], A[mi][3], Bf[nt][0], Bf[nt][1]);
+        if (sums) mma_f16(U[mi], A[mi][0], A[mi][1], A[mi][2], A[mi][3], ones, ones);
       }
+    }
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float sm, err;
+          two_sum(Ch[mi][nt][e], T[mi][nt][e], sm, err);
+          Ch[mi][nt][e] = sm;
+          Cl[mi][nt][e] = __fadd_rn(Cl[mi][nt][e], err);
+        }
+      if (sums)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float sm, err;
+          two_sum(Sh[mi][e], U[mi][e], sm, err);
+          Sh[mi][e] = sm;
+          Sl[mi][e] = __fadd_rn(Sl[mi][e], err);
+        }
     }
   }
   cp_async_wait<0>();
@@ -173,22 +212,26 @@ __global__ void __launch_bounds__(kGramThreads) gram_kernel(const GramParams p) 
 #pragma unroll
   for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int m = 32 * wm + 16 * mi + g8 + 8 * (e >> 1);
-        const int n = 64 * wn + 8 * nt + 2 * c4 + (e & 1);
+        const int m = mbase + 16 * mi + g8 + 8 * (e >> 1);
+        const int n = nbase + 8 * nt + 2 * c4 + (e & 1);
         dst[m * kHeadDim + n] = Ch[mi][nt][e];
         dst[kHeadDim * kHeadDim + m * kHeadDim + n] = Cl[mi][nt][e];
+        if (z == 1) {  // the transposed block
+          dst[n * kHeadDim + m] = Ch[mi][nt][e];
+          dst[kHeadDim * kHeadDim + n * kHeadDim + m] = Cl[mi][nt][e];
+        }
       }
-  if (wn == 0 && c4 == 0) {
+  if (sums && c4 == 0) {
     float* cdst = p.colpart + ((size_t)grp * p.n_chunks + chunk) * 2 * kHeadDim;
 #pragma unroll
     for (int mi = 0; mi < 2; ++mi) {
-      cdst[32 * wm + 16 * mi + g8] = Sh[mi][0];
-      cdst[32 * wm + 16 * mi + g8 + 8] = Sh[mi][2];
-      cdst[kHeadDim + 32 * wm + 16 * mi + g8] = Sl[mi][0];
-      cdst[kHeadDim + 32 * wm + 16 * mi + g8 + 8] = Sl[mi][2];
+      cdst[mbase + 16 * mi + g8] = Sh[mi][0];
+      cdst[mbase + 16 * mi + g8 + 8] = Sh[mi][2];
+      cdst[kHeadDim + mbase + 16 * mi + g8] = Sl[mi][0];
+      cdst[kHeadDim + mbase + 16 * mi + g8 + 8] = Sl[mi][2];
     }
   }
 }
@@ -574,14 +617,16 @@ struct FitLayout {
   size_t part_off, col_off, G_off, err_off, total;
 };
 
-// Rows per chunk: enough chunks for one CTA per SM over all groups, in whole
-// 64-row tiles, between 64 and 16384 rows.
+// Rows per chunk, in whole 64-row tiles: enough chunks over all groups for
+// one CTA per SM (the exact kernel), or for two CTAs per SM with three block
+// CTAs per chunk (the tensor-core kernel).
 static FitLayout fit_layout(int n_groups, long long rows_g) {
   FitLayout f;
   const long long sms = device_sm_count();
-  long long per = (rows_g * n_groups + sms - 1) / sms;
+  const bool tc = rows_g > kExactGramRows;
+  long long per = (rows_g * n_groups * (tc ? 3 : 1) + (tc ? 2 : 1) * sms - 1) / ((tc ? 2 : 1) * sms);
   per = (per + kGramTile - 1) / kGramTile * kGramTile;
-  f.chunk_rows = std::max<long long>(kGramTile, std::min<long long>(16384, per));
+  f.chunk_rows = std::max<long long>(kGramTile, std::min<long long>(1LL << 20, per));
   f.n_chunks = (int)((rows_g + f.chunk_rows - 1) / f.chunk_rows);
   f.part_off = 0;
   f.col_off = align_up(f.part_off + sizeof(float) * 2 * (size_t)n_groups * f.n_chunks * kHeadDim * kHeadDim, 256);
@@ -657,7 +702,7 @@ static palu_status launch_gram(const palu_config* cfg, const void* x, int64_t ba
     int per_sm = 0;
     st = kernel_occupancy(reinterpret_cast<const void*>(gram_kernel), kGramThreads, gram_smem, &per_sm);
     if (st != PALU_OK) return st;
-    gram_kernel<<<dim3(fl.n_chunks, ng), kGramThreads, gram_smem, strm>>>(gp);
+    gram_kernel<<<dim3(fl.n_chunks, ng, 3), kGramThreads, gram_smem, strm>>>(gp);
   }
   st = cuda_check(cudaGetLastError(), "gram_kernel launch");
   if (st != PALU_OK) return st;
