@@ -226,7 +226,10 @@ struct DecodePlan {
   DecodeKernel kern;
 };
 
-static DecodeKernel pick_kernel(int ke, int ve, int kc, int vc, bool vq) {
+// The decode kernel for the records' octet counts; *ko: the key octets it
+// holds per lane (the q-prep's packing).
+static DecodeKernel pick_kernel(int ke, int ve, int kc, int vc, bool vq, int* ko) {
+  *ko = ke;
   if (ke <= 8 && ve <= 8) {
     switch (ke) {
       case 1: return decode_kernel_exact<1>(ve, vq);
@@ -240,6 +243,8 @@ static DecodeKernel pick_kernel(int ke, int ve, int kc, int vc, bool vq) {
       default: return nullptr;
     }
   }
+  if (DecodeKernel kw = decode_kernel_wide(ke, ve, kc, vc, vq)) return kw;
+  *ko = 4 * kc;
   switch (kc) {
     case 1: return decode_kernel_class<1>(vc, vq);
     case 2: return decode_kernel_class<2>(vc, vq);
@@ -266,9 +271,8 @@ static palu_status plan_decode(const palu_cache* k, const palu_cache* v, int32_t
   pl->VQ = v->quantize != 0;
   if (pl->VQ && pl->VC != v->n_hi_oct) return fail(PALU_ERR_UNSUPPORTED, "unexpected value record layout");
   if (pl->KC != k->n_hi_oct) return fail(PALU_ERR_UNSUPPORTED, "unexpected key record layout");
-  pl->kern = pick_kernel(k->n_oct, v->n_oct, pl->KC, pl->VC, pl->VQ);
+  pl->kern = pick_kernel(k->n_oct, v->n_oct, pl->KC, pl->VC, pl->VQ, &pl->qp_ko);
   if (!pl->kern) return fail(PALU_ERR_UNSUPPORTED, "no decode kernel for this rank");
-  pl->qp_ko = (k->n_oct <= 8 && v->n_oct <= 8) ? k->n_oct : 4 * pl->KC;  // the kernel's key octets
   pl->qp_stride = (2 * pl->qp_ko + 4 + 3) / 4 * 4;
   const int rec_k = k->record_bytes, rec_v = v->record_bytes;
   pl->stage_bytes = 2 * (rec_k + rec_v);

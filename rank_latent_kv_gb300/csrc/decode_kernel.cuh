@@ -415,7 +415,7 @@ __device__ __forceinline__ long long block_owner(long long i, long long T, long 
 // kernel (programmatic dependent launch: the first copies are in flight
 // before the packed query factors are read).
 template <int KC, int VC, bool VQ, int KE, int VE>
-__global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kClassDecThreads, 1)
+__global__ void __launch_bounds__((KE > 0 && KE <= 8) ? kMaxDecThreads : kClassDecThreads, 1)
     latent_decode_kernel(const DecodeParams p) {
   using GK = Geom<KC, KE, true>;
   using GV = Geom<VC, VE, VQ>;
@@ -1074,10 +1074,12 @@ __global__ void __launch_bounds__(KE > 0 ? kMaxDecThreads : kClassDecThreads, 1)
 typedef void (*DecodeKernel)(const DecodeParams);
 
 // Instantiations are spread over translation units (parallel build):
-// exact octet counts up to 8 on both sides, one unit per key count, and the
-// class kernels for the larger ranks, one unit per key class.
+// exact octet counts up to 8 on both sides, one unit per key count; exact
+// wider records that common ranks produce (12 warps, as the class kernels);
+// and the class kernels for the other larger ranks, one unit per key class.
 template <int KE>
 DecodeKernel decode_kernel_exact(int ve, bool vq);
+DecodeKernel decode_kernel_wide(int ke, int ve, int kc, int vc, bool vq);  // nullptr when none
 template <int KC>
 DecodeKernel decode_kernel_class(int vc, bool vq);
 
