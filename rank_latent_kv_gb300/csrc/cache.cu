@@ -69,8 +69,9 @@ __host__ __device__ inline EncodeSmem encode_smem(int r, int rec_bytes) {
   s.codes_off = s.err_off + align16(4 * kBlock * (r + 1));             // u8 [32][r]
   s.sz_off = s.codes_off + align16(kBlock * r);                        // half2 [r] (scale, zero)
   s.rec_off = s.sz_off + align16(4 * r);                               // record
-  s.work_off = s.rec_off + align16(rec_bytes);                         // int [2] counts, u16 [32 r] work list
-  s.basis_off = s.work_off + align16(8 + 2 * kBlock * r);              // float [r][129] (exact path only)
+  s.work_off = s.rec_off + align16(rec_bytes);                         // int [2] counts, u32 [4] warp maxima,
+                                                                       // u16 [32 r] work list
+  s.basis_off = s.work_off + align16(24 + 2 * kBlock * r);             // float [r][129] (exact path only)
   s.total = s.basis_off + align16(4 * r * (kHeadDim + 1));
   return s;
 }
@@ -226,7 +227,8 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
   float* err = reinterpret_cast<float*>(smem + L.err_off);
   uint32_t* cand = reinterpret_cast<uint32_t*>(smem + L.cand_off);
   int* n_work = reinterpret_cast<int*>(smem + L.work_off);
-  uint16_t* work = reinterpret_cast<uint16_t*>(smem + L.work_off + 8);
+  uint32_t* wmax_s = reinterpret_cast<uint32_t*>(smem + L.work_off + 8);  // each warp's largest scale
+  uint16_t* work = reinterpret_cast<uint16_t*>(smem + L.work_off + 24);
   float* bas = reinterpret_cast<float*>(smem + L.basis_off);
   float* lat = reinterpret_cast<float*>(smem + L.lat_off);
   uint8_t* codes = smem + L.codes_off;
@@ -356,25 +358,49 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
           // threads from shared work lists of (token, channel) pairs.
           const int warp = tid >> 5, lane = tid & 31, t = lane;
           const uint32_t lt = (1u << lane) - 1u;
-          for (int j = warp; j < r; j += 4) {
-            const float v = lat[t * (r + 1) + j], e = err[t * (r + 1) + j];
-            float min_hi = v + e, max_lo = v - e;
+          // four channels a pass (j0, j0 + 4, j0 + 8, j0 + 12) so their shuffle
+          // chains overlap; one list reservation per pass
+          for (int j0 = warp; j0 < r; j0 += 16) {
+            float v[4], e[4], mh[4], ml[4];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-              min_hi = fminf(min_hi, __shfl_xor_sync(0xffffffffu, min_hi, o));
-              max_lo = fmaxf(max_lo, __shfl_xor_sync(0xffffffffu, max_lo, o));
+            for (int q = 0; q < 4; ++q) {
+              const bool ok = j0 + 4 * q < r;  // uniform
+              v[q] = ok ? lat[t * (r + 1) + j0 + 4 * q] : 0.f;
+              e[q] = ok ? err[t * (r + 1) + j0 + 4 * q] : 0.f;
+              mh[q] = v[q] + e[q];
+              ml[q] = v[q] - e[q];
             }
-            const bool cmin = v - e <= min_hi, cmax = v + e >= max_lo;
-            const uint32_t bmin = __ballot_sync(0xffffffffu, cmin), bmax = __ballot_sync(0xffffffffu, cmax);
-            const bool need = (cmin || cmax) && t >= off_new;
-            const uint32_t bneed = __ballot_sync(0xffffffffu, need);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                mh[q] = fminf(mh[q], __shfl_xor_sync(0xffffffffu, mh[q], o));
+                ml[q] = fmaxf(ml[q], __shfl_xor_sync(0xffffffffu, ml[q], o));
+              }
+            bool need[4];
+            uint32_t bneed[4];
+            int tot = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int j = j0 + 4 * q;
+              const bool ok = j < r;
+              const bool cmin = ok && v[q] - e[q] <= mh[q], cmax = ok && v[q] + e[q] >= ml[q];
+              const uint32_t bmin = __ballot_sync(0xffffffffu, cmin), bmax = __ballot_sync(0xffffffffu, cmax);
+              need[q] = (cmin || cmax) && t >= off_new;
+              bneed[q] = __ballot_sync(0xffffffffu, need[q]);
+              tot += __popc(bneed[q]);
+              if (lane == 0 && ok) {
+                cand[j] = bmin;
+                cand[kHeadDim + j] = bmax;
+              }
+            }
             int base = 0;
-            if (lane == 0 && bneed) base = atomicAdd(&n_work[0], __popc(bneed));
+            if (lane == 0 && tot) base = atomicAdd(&n_work[0], tot);
             base = __shfl_sync(0xffffffffu, base, 0);
-            if (need) work[base + __popc(bneed & lt)] = (uint16_t)(t * 128 + j);
-            if (lane == 0) {
-              cand[j] = bmin;
-              cand[kHeadDim + j] = bmax;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (need[q]) work[base + __popc(bneed[q] & lt)] = (uint16_t)(t * 128 + j0 + 4 * q);
+              base += __popc(bneed[q]);
             }
           }
           __syncthreads();
@@ -384,50 +410,83 @@ __global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const 
                 exact_latent(xs + tt * kXsStride, bT + (size_t)jj * kHeadDim, cv.mv[(size_t)grp * r + jj]);
           }
           __syncthreads();
-          for (int j = warp; j < r; j += 4) {
-            const float v = lat[t * (r + 1) + j];
-            const uint32_t bmin = cand[j], bmax = cand[kHeadDim + j];
-            float mn = (bmin >> t) & 1u ? v : INFINITY, mx = (bmax >> t) & 1u ? v : -INFINITY;
+          uint32_t wmax = 0u;  // the largest scale of this warp's channels (fp32 bits of a non-negative value)
+          for (int j0 = warp; j0 < r; j0 += 16) {
+            float v[4], mn[4], mx[4];
+            uint32_t ex[4];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-              mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            for (int q = 0; q < 4; ++q) {
+              const bool ok = j0 + 4 * q < r;  // uniform
+              const uint32_t bmin = ok ? cand[j0 + 4 * q] : 0u, bmax = ok ? cand[kHeadDim + j0 + 4 * q] : 0u;
+              v[q] = ok ? lat[t * (r + 1) + j0 + 4 * q] : 0.f;
+              mn[q] = (bmin >> t) & 1u ? v[q] : INFINITY;
+              mx[q] = (bmax >> t) & 1u ? v[q] : -INFINITY;
+              ex[q] = bmin | bmax;
             }
-            const float qmax = (float)((1 << (j < cv.n_hi ? 4 : 2)) - 1);
-            const float scale = __fdiv_rn(__fsub_rn(mx, mn), qmax);
-            const __half sh = __float2half_rn(scale);
-            const __half zh = __float2half_rn(mn);
-            const float s32 = __half2float(sh), z32 = __half2float(zh);
-            if (lane == 0) {
-              sz[j] = __halves2half2(sh, zh);
-              atomicMax(&cv.hdr->max_scale, __float_as_uint(s32));
-              atomicMax(&cv.smax[(long long)b * Hkv + h], __float_as_uint(s32));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                mn[q] = fminf(mn[q], __shfl_xor_sync(0xffffffffu, mn[q], o));
+                mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], o));
+              }
+            bool need[4];
+            uint32_t bneed[4];
+            int tot = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int j = j0 + 4 * q;
+              need[q] = false;
+              if (j < r) {  // uniform
+                const float qmax = (float)((1 << (j < cv.n_hi ? 4 : 2)) - 1);
+                const float scale = __fdiv_rn(__fsub_rn(mx[q], mn[q]), qmax);
+                const __half sh = __float2half_rn(scale);
+                const __half zh = __float2half_rn(mn[q]);
+                const float s32 = __half2float(sh), z32 = __half2float(zh);
+                if (lane == 0) sz[j] = __halves2half2(sh, zh);
+                wmax = max(wmax, __float_as_uint(s32));
+                float qc;
+                if (t < off_new || ((ex[q] >> t) & 1u)) {
+                  qc = quant_code(v[q], z32, s32, qmax);  // exact latent
+                } else if (s32 == 0.f) {
+                  qc = 0.f;
+                } else {
+                  // the exact code is round(fl((L - z) / s)) for some L in [v - e, v + e]:
+                  // it is known when that interval, scaled by an approximate 1/s and
+                  // widened by the approximation's error, lies inside one rounding
+                  // cell; else it is decided from the exact latent below
+                  float inv;
+                  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(s32));
+                  const float e = err[t * (r + 1) + j];
+                  const float u = (v[q] - z32) * inv, du = fmaf(e, inv, fmaf(fabsf(u), 0x1p-18f, 0x1p-20f));
+                  const float k = rintf(u);
+                  need[q] = fabsf(u - k) + du >= 0.5f;
+                  qc = fminf(fmaxf(k, 0.f), qmax);
+                }
+                codes[t * r + j] = (uint8_t)qc;
+              }
+              bneed[q] = __ballot_sync(0xffffffffu, need[q]);
+              tot += __popc(bneed[q]);
             }
-            float q;
-            bool need = false;
-            if (t < off_new || (((bmin | bmax) >> t) & 1u)) {
-              q = quant_code(v, z32, s32, qmax);  // exact latent
-            } else if (s32 == 0.f) {
-              q = 0.f;
-            } else {
-              // the exact code is round(fl((L - z) / s)) for some L in [v - e, v + e]:
-              // it is known when that interval, scaled by an approximate 1/s and
-              // widened by the approximation's error, lies inside one rounding
-              // cell; else it is decided from the exact latent below
-              const float inv = 1.f / s32, e = err[t * (r + 1) + j];
-              const float u = (v - z32) * inv, du = fmaf(e, inv, fmaf(fabsf(u), 0x1p-18f, 0x1p-20f));
-              const float k = rintf(u);
-              need = fabsf(u - k) + du >= 0.5f;
-              q = fminf(fmaxf(k, 0.f), qmax);
-            }
-            const uint32_t bneed = __ballot_sync(0xffffffffu, need);
             int base = 0;
-            if (lane == 0 && bneed) base = atomicAdd(&n_work[1], __popc(bneed));
+            if (lane == 0 && tot) base = atomicAdd(&n_work[1], tot);
             base = __shfl_sync(0xffffffffu, base, 0);
-            if (need) work[base + __popc(bneed & lt)] = (uint16_t)(t * 128 + j);
-            codes[t * r + j] = (uint8_t)q;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (need[q]) work[base + __popc(bneed[q] & lt)] = (uint16_t)(t * 128 + j0 + 4 * q);
+              base += __popc(bneed[q]);
+            }
           }
+          if (lane == 0) wmax_s[warp] = wmax;
           __syncthreads();
+          // the block's largest scale into the stream's and the cache's maxima:
+          // one atomic each per block, and none when the stored value is as large
+          if (tid == 0) {
+            const uint32_t m = max(max(wmax_s[0], wmax_s[1]), max(wmax_s[2], wmax_s[3]));
+            unsigned int* sm = &cv.smax[(long long)b * Hkv + h];
+            if (m > __ldcg(sm)) atomicMax(sm, m);
+            if (m > __ldcg(&cv.hdr->max_scale)) atomicMax(&cv.hdr->max_scale, m);
+          }
           for (int i = tid; i < n_work[1]; i += blockDim.x) {
             const int tt = work[i] >> 7, jj = work[i] & 127;
             const float x =
