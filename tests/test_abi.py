@@ -205,3 +205,73 @@ class torch_like:
 
     def data_ptr(self):
         return self.addr
+
+
+def test_svdq_struct_layout_and_sizes(palu):
+    prog = r'''
+#include <stdio.h>
+#include <stddef.h>
+#include "svdq.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu\n", sizeof(palu_svdq_cache), offsetof(palu_svdq_cache, capacity),
+         offsetof(palu_svdq_cache, blocks), offsetof(palu_svdq_cache, state), offsetof(palu_svdq_cache, length));
+  return 0;
+}'''
+    with tempfile.TemporaryDirectory() as d:
+        src = os.path.join(d, "t.c")
+        exe = os.path.join(d, "t")
+        open(src, "w").write(prog)
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), src, "-o", exe], check=True)
+        vals = list(map(int, subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()))
+    C = palu.palu_svdq_cache
+    assert vals == [ctypes.sizeof(C), C.capacity.offset, C.blocks.offset, C.state.offset, C.length.offset]
+    # record stride: the largest head's record (the oracle's layout), 16-byte multiple; tail: 32 x r_max fp32
+    from oracle import svdq_oracle as S
+    ranks = [1, 74, 128, 7]
+    rk = (ctypes.c_int32 * 4)(*ranks)
+    bb, tb, sb = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    palu._check(palu.lib().palu_svdq_cache_size(3, 4, rk, 100, ctypes.byref(bb), ctypes.byref(tb), ctypes.byref(sb)))
+    stride = max(S.record_layout(r)[4] for r in ranks)
+    assert bb.value == -(-(3 * 4 * 4 * stride) // 256) * 256
+    assert tb.value == -(-(3 * 4 * 32 * 128 * 4) // 256) * 256
+    assert sb.value > 4 * 128 * 128 * 4  # holds the transposed bases
+
+
+def test_svdq_host_validation(palu):
+    """Errors the host detects before any launch."""
+    bb, tb, sb = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    for ranks in ([0, 8], [8, 129]):
+        rk = (ctypes.c_int32 * 2)(*ranks)
+        assert palu.lib().palu_svdq_cache_size(1, 2, rk, 64, ctypes.byref(bb), ctypes.byref(tb), ctypes.byref(sb)) == 1
+    rk = (ctypes.c_int32 * 2)(8, 16)
+    assert palu.lib().palu_svdq_cache_size(0, 2, rk, 64, ctypes.byref(bb), ctypes.byref(tb), ctypes.byref(sb)) == 1
+    assert palu.lib().palu_svdq_cache_size(1, 2, None, 64, ctypes.byref(bb), ctypes.byref(tb), ctypes.byref(sb)) == 1
+    c = palu.palu_svdq_cache()
+    a = ctypes.c_void_p(1 << 20)
+    # misaligned buffers, a NULL basis, and a basis row stride below the largest rank
+    assert palu.lib().palu_svdq_cache_init(ctypes.byref(c), 1, 2, rk, 64, a, 128, a, ctypes.c_void_p(16), a, a,
+                                           None) == 1
+    assert palu.lib().palu_svdq_cache_init(ctypes.byref(c), 1, 2, rk, 64, None, 128, a, a, a, a, None) == 1
+    assert palu.lib().palu_svdq_cache_init(ctypes.byref(c), 1, 2, rk, 64, a, 8, a, a, a, a, None) == 1
+    # an uninitialised cache
+    n = ctypes.c_size_t()
+    assert palu.lib().palu_svdq_decode_workspace_size(ctypes.byref(c), 4, ctypes.byref(n)) == 4
+    assert palu.lib().palu_svdq_append(ctypes.byref(c), a, 1, None) == 4
+    assert "not initialised" in palu.palu_last_error()
+
+
+def test_fit_batch_workspace_and_validation(palu):
+    cfg = palu.palu_config_default(n_head_groups=2)
+    one = palu.palu_fit_workspace_size(cfg, 2, 4, 4096)
+    assert palu.palu_fit_batch_workspace_size([cfg], 2, 4, 4096) == one
+    two = palu.palu_fit_batch_workspace_size([cfg, cfg], 2, 4, 4096)
+    # the partial-sum area is shared: a second tensor adds only its fp64 Gram matrices and error word
+    assert two - one == 2 * 128 * 128 * 8 + 256
+    with pytest.raises(palu.PaluError):
+        palu.palu_fit_batch_workspace_size([cfg, palu.palu_config_default(n_head_groups=3)], 2, 4, 4096)
+    arr = (palu.palu_config * 1)(cfg)
+    n = ctypes.c_size_t()
+    assert palu.lib().palu_fit_batch_workspace_size(arr, 0, 2, 4, 4096, ctypes.byref(n)) == 1
+    r = (ctypes.c_int32 * 1)()
+    assert palu.lib().palu_fit_batch(arr, 1, None, 2, 4, 4096, ctypes.c_void_p(1 << 20), 1 << 30, None, None, None,
+                                     r, None, None) == 1
