@@ -768,13 +768,19 @@ extern "C" palu_status palu_cache_init(palu_cache* cache, const palu_config* cfg
   const StateLayout sl = state_layout(c.n_groups, rank, batch, kv_heads);
   uint8_t* s = static_cast<uint8_t*>(state);
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  // every byte of the state (padding, largest scales, sequence lengths) and
+  // of the tail starts at zero, so cache images are a function of the calls
+  st = cuda_check(cudaMemsetAsync(s, 0, sl.total, strm), "cudaMemsetAsync(state)");
+  if (st != PALU_OK) return st;
+  if (quant) {
+    st = cuda_check(cudaMemsetAsync(tail, 0, sizeof(float) * (size_t)batch * kv_heads * kBlock * rank, strm),
+                    "cudaMemsetAsync(tail)");
+    if (st != PALU_OK) return st;
+  }
   cache_init_kernel<<<dim3(rank, c.n_groups), kHeadDim, 0, strm>>>(
       basis, basis_ld, mu, reinterpret_cast<float*>(s + sl.basis_off), reinterpret_cast<float*>(s + sl.mu_off),
       reinterpret_cast<float2*>(s + sl.mv_off), reinterpret_cast<StateHeader*>(s), rank);
   st = cuda_check(cudaGetLastError(), "cache_init_kernel launch");
-  if (st != PALU_OK) return st;
-  st = cuda_check(cudaMemsetAsync(s + sl.smax_off, 0, sl.total - sl.smax_off, strm),
-                  "cudaMemsetAsync(largest scales, sequence lengths)");
   if (st != PALU_OK) return st;
   *cache = c;
   return PALU_OK;

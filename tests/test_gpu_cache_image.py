@@ -109,3 +109,29 @@ def test_restore_refuses_other_caches_and_small_capacity(P):
     with pytest.raises(P.PaluError) as e:
         kc.restore(img[:img.numel() - 16].clone())
     assert e.value.status == 1  # PALU_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("S,quantize_v", [(95, False), (300, True)])
+def test_images_are_deterministic(P, S, quantize_v):
+    """Two caches built from the same prefill give byte-identical images, the
+    open block's unwritten token slots included (a record is zeroed when its
+    block opens)."""
+    rng = np.random.default_rng(1000 + S)
+    B, Hkv = 2, 4
+    xk = rand_lowrank(rng, B, Hkv, S, n_groups=2)
+    xv = rand_lowrank(rng, B, Hkv, S, n_groups=2)
+    cfg_k = P.palu_config_default(n_head_groups=2, rank=28)
+    cfg_v = P.palu_config_default(n_head_groups=2, rank=36, quantize=1 if quantize_v else 0)
+    images, keep = [], []
+    for i in range(2):
+        # freed device memory holding a different byte pattern each time, for
+        # the caches' buffers to land on
+        junk = torch.full((64 << 20,), 0x11 * (i + 1) + 0x5a, dtype=torch.uint8, device=DEV)
+        del junk
+        kc, vc = make_caches(P, cfg_k, cfg_v, xk, xv, S + 64)
+        torch.cuda.synchronize()
+        images.append((kc.save(), vc.save()))
+        torch.cuda.synchronize()
+        keep.append((kc, vc))
+    for a, b in zip(images[0], images[1]):
+        assert torch.equal(a, b)
