@@ -150,3 +150,28 @@ def test_svdq_explicit_ranks(P, rank):
     _check_storage(c, oracle)
     v = torch.from_numpy(rng.standard_normal((B, H, cap, 128)).astype(np.float16)).to(DEV)
     _check_decode(c, oracle, rng, v, 4, peaked=True)
+
+
+def test_svdq_errors(P):
+    """Refusals: an append past the capacity (nothing written), a decode of an
+    empty cache, query heads that are not a multiple of the KV heads or more
+    than 8 per KV head, a value buffer shorter than the cache."""
+    rng = np.random.default_rng(400)
+    B, H, cap = 1, 2, 64
+    c, oracle = _build(P, rng, B, H, cap)
+    v = torch.zeros(B, H, cap, 128, dtype=torch.float16, device=DEV)
+    q = torch.zeros(B, 2 * H, 128, dtype=torch.float16, device=DEV)
+    with pytest.raises(P.PaluError):
+        c.decode(v, q)                                         # empty
+    _append(c, oracle, _keys(rng, B, H, 40))
+    with pytest.raises(P.PaluError) as e:
+        c.append(torch.from_numpy(_keys(rng, B, H, 25)).to(DEV))   # 65 > 64
+    assert e.value.status == 3  # PALU_ERR_CAPACITY
+    assert c.sync() == 0 and c.length == 40
+    with pytest.raises(P.PaluError):
+        c.decode(v, torch.zeros(B, 3, 128, dtype=torch.float16, device=DEV))
+    with pytest.raises(P.PaluError):
+        c.decode(v, torch.zeros(B, 9 * H, 128, dtype=torch.float16, device=DEV))
+    with pytest.raises(P.PaluError):
+        c.decode(v[:, :, :32], q)
+    _check_storage(c, oracle)                                  # the refused calls changed nothing
