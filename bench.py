@@ -752,7 +752,7 @@ def run_svdq_comparator(P, w, s, L, s_ctx, dev, world, steps=20):
             "achieved_gbs": bytes_step / (ms / 1e3) / 1e9, "bytes_per_step": bytes_step,
             "key_ranks_min_mean_max": [min(flat), sum(flat) / len(flat), max(flat)],
             "key_bits_per_element": sum(sum(_svdq_widths(r)) for r in flat) / (128.0 * len(flat)),
-            "gpu_launches_per_step": 3 * L}
+            "gpu_launches_per_step": 2 * L}
 
 
 # ------------------------------------------------------------------ main

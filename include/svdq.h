@@ -83,7 +83,8 @@ palu_status palu_svdq_decode_workspace_size(const palu_svdq_cache* cache, int32_
  *   q     device fp16 [batch, q_heads, D]; query head h reads KV head
  *         h / (q_heads / kv_heads) (at most 8 per KV head).
  *   out   device [batch, q_heads, D], fp32 if out_fp32 else fp16.
- * Three kernel launches (query factors, split attention, combine). */
+ * Two kernel launches: split attention (each CTA forms its stream's query
+ * factors), then the combine. */
 palu_status palu_svdq_decode_attn(const palu_svdq_cache* cache, const void* v, int64_t v_cap, const void* q,
                                   int32_t q_heads, float softmax_scale, void* out, int32_t out_fp32,
                                   void* workspace, size_t workspace_bytes, void* stream);

@@ -317,25 +317,23 @@ struct SvdqDecParams {
   SvdqView k;
   const __half* v;
   const __half* q;
-  float* qt;   // [streams][8][r_max]: q~ = q V_h of the stream's query heads (0 past the rank and Gq)
-  float* cq;   // [streams][8]: q . mean_h
   float* ws;   // [streams][n_chunks][Gq][2 + D] partials
   long long v_cap, len;
   int Hq, Gq, n_chunks, tiles_per_chunk;
   float scale_log2;
 };
 
-// One CTA per stream: the query factors of its query heads, in fp32.
-__global__ void __launch_bounds__(128) svdq_qprep_kernel(const SvdqDecParams p) {
-  __shared__ float q_s[8][kHeadDim];
+// The query factors of stream X = (b, h) by the calling CTA's 128 threads, in
+// fp32: qts[i][j] = q_i . V_h[:, j] for the stream's query heads i < Gq (0
+// past the rank and for i >= Gq), cqs[i] = q_i . mean_h.  q_s: 4 KB of
+// shared scratch.  Ends with a barrier.
+__device__ __forceinline__ void svdq_query_factors(const SvdqDecParams& p, int h, int b, float* q_s, float* qts,
+                                                   float* cqs) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  grid_dep_launch();  // the split kernel may start its copies; it waits for this grid
-  const long long X = blockIdx.x;
-  const int H = p.k.H, rm = p.k.r_max, Gq = p.Gq;
-  const int h = (int)(X % H), b = (int)(X / H), r = p.k.head[4 * h];
+  const int rm = p.k.r_max, Gq = p.Gq, r = p.k.head[4 * h];
   for (int i = tid; i < 8 * kHeadDim; i += blockDim.x) {
     const int hq = i / kHeadDim, d = i % kHeadDim;
-    q_s[hq][d] = hq < Gq ? __half2float(p.q[((long long)b * p.Hq + (long long)h * Gq + hq) * kHeadDim + d]) : 0.f;
+    q_s[i] = hq < Gq ? __half2float(p.q[((long long)b * p.Hq + (long long)h * Gq + hq) * kHeadDim + d]) : 0.f;
   }
   __syncthreads();
   // thread j: direction j of the head's basis against the 8 query rows
@@ -349,23 +347,24 @@ __global__ void __launch_bounds__(128) svdq_qprep_kernel(const SvdqDecParams p) 
         const float4 v = __ldg(row + d4);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float4 qq = *reinterpret_cast<const float4*>(&q_s[i][4 * d4]);
+          const float4 qq = *reinterpret_cast<const float4*>(q_s + i * kHeadDim + 4 * d4);
           acc[i] = fmaf(qq.x, v.x, fmaf(qq.y, v.y, fmaf(qq.z, v.z, fmaf(qq.w, v.w, acc[i]))));
         }
       }
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) p.qt[((size_t)X * 8 + i) * rm + j] = acc[i];
+    for (int i = 0; i < 8; ++i) qts[i * rm + j] = acc[i];
   }
-  // warp i: q_i . mean_h
+  // warp w: q_i . mean_h for i = w, w + 4
   for (int i = warp; i < 8; i += blockDim.x / 32) {
     const float4 m = __ldg(reinterpret_cast<const float4*>(p.k.mu + (size_t)h * kHeadDim) + lane);
-    const float4 qq = *reinterpret_cast<const float4*>(&q_s[i][4 * lane]);
-    float s = fmaf(qq.x, m.x, fmaf(qq.y, m.y, fmaf(qq.z, m.z, qq.w * m.w)));
+    const float4 qq = *reinterpret_cast<const float4*>(q_s + i * kHeadDim + 4 * lane);
+    float sm = fmaf(qq.x, m.x, fmaf(qq.y, m.y, fmaf(qq.z, m.z, qq.w * m.w)));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) p.cq[(size_t)X * 8 + i] = s;
+    for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+    if (lane == 0) cqs[i] = sm;
   }
+  __syncthreads();
 }
 
 constexpr int kSvdqTile = 128;                           // tokens per tile: one 32-token block per warp
@@ -516,11 +515,11 @@ __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const Svd
     if (s < n_tiles) load_tile(s, s);
     cp_async_commit();
   }
-  // the query factors come from the preceding launch (the cache's codes and
-  // the values from earlier ones, complete before it started)
-  grid_dep_wait();
-  for (int i = tid; i < 8 * rm; i += blockDim.x) qts[i] = __ldcg(p.qt + (size_t)X * 8 * rm + i);
-  if (tid < 8) cqs[tid] = __ldcg(p.cq + (size_t)X * 8 + tid);
+  // the stream's query factors while the first copies are in flight (every
+  // CTA of the stream forms them; scratch: the second value stage, whose
+  // first copy is issued only after the loop's first barrier)
+  static_assert(kSvdqStages >= 2, "the query scratch uses the second value stage");
+  svdq_query_factors(p, h, b, reinterpret_cast<float*>(dsm + L.vst + kSvdqTileBytes), qts, cqs);
   // lane's q~ of head g at its channels of each k-step (0 past the class)
   float qv[5][4];
 #pragma unroll
@@ -528,9 +527,9 @@ __global__ void __launch_bounds__(32 * kSplitWarps) svdq_decode_kernel(const Svd
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int jj = 2 * c + svdq_kk(k);
-      qv[ks][k] = jj < ksn[ks] ? __ldcg(p.qt + ((size_t)X * 8 + g) * rm + ksf[ks] + jj) : 0.f;
+      qv[ks][k] = jj < ksn[ks] ? qts[g * rm + ksf[ks] + jj] : 0.f;
     }
-  const float cq_g = __ldcg(p.cq + (size_t)X * 8 + g);
+  const float cq_g = cqs[g];
   SplitState st;
   split_init(st);
   for (int tile = 0; tile < n_tiles; ++tile) {
@@ -783,7 +782,7 @@ extern "C" palu_status palu_svdq_append(palu_svdq_cache* cache, const void* k, i
 
 namespace palu {
 struct SvdqWs {
-  size_t qt_off, cq_off, part_off, total;
+  size_t part_off, total;
   int n_chunks, tpc, smem;
 };
 static palu_status svdq_ws(const palu_svdq_cache* c, int32_t q_heads, SvdqWs* w) {
@@ -793,10 +792,8 @@ static palu_status svdq_ws(const palu_svdq_cache* c, int32_t q_heads, SvdqWs* w)
   const int64_t streams = (int64_t)c->batch * c->kv_heads;
   w->smem = svdq_dec_smem(c->r_max, c->record_bytes).total;
   w->n_chunks = svdq_chunks(streams, c->capacity, w->smem, &w->tpc);
-  w->qt_off = 0;
-  w->cq_off = align_up(sizeof(float) * (size_t)streams * 8 * c->r_max, 256);
-  w->part_off = align_up(w->cq_off + sizeof(float) * (size_t)streams * 8, 256);
-  w->total = align_up(w->part_off + sizeof(float) * (size_t)streams * w->n_chunks * Gq * kSplitPartStride, 256);
+  w->part_off = 0;
+  w->total = align_up(sizeof(float) * (size_t)streams * w->n_chunks * Gq * kSplitPartStride, 256);
   return PALU_OK;
 }
 }  // namespace palu
@@ -832,8 +829,6 @@ extern "C" palu_status palu_svdq_decode_attn(const palu_svdq_cache* cache, const
   p.v = static_cast<const __half*>(v);
   p.q = static_cast<const __half*>(q);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.qt = reinterpret_cast<float*>(ws + w.qt_off);
-  p.cq = reinterpret_cast<float*>(ws + w.cq_off);
   p.ws = reinterpret_cast<float*>(ws + w.part_off);
   p.v_cap = v_cap;
   p.len = cache->length;
@@ -844,22 +839,10 @@ extern "C" palu_status palu_svdq_decode_attn(const palu_svdq_cache* cache, const
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)kHeadDim);
   p.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
-  const int64_t streams = (int64_t)cache->batch * cache->kv_heads;
-  svdq_qprep_kernel<<<(unsigned)streams, 128, 0, strm>>>(p);
-  st = cuda_check(cudaGetLastError(), "svdq_qprep_kernel launch");
-  if (st != PALU_OK) return st;
-  // the split kernel as a programmatic dependent of the q-prep
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr.val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_chunks, cache->kv_heads, (unsigned)cache->batch);
-  cfg.blockDim = dim3(32 * kSplitWarps);
-  cfg.dynamicSmemBytes = w.smem;
-  cfg.stream = strm;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  st = cuda_check(cudaLaunchKernelEx(&cfg, svdq_decode_kernel, p), "svdq_decode_kernel launch");
+  // in stream order (it reads what earlier launches wrote); the combine
+  // kernel follows as its programmatic dependent
+  svdq_decode_kernel<<<dim3(p.n_chunks, cache->kv_heads, (unsigned)cache->batch), 32 * kSplitWarps, w.smem, strm>>>(p);
+  st = cuda_check(cudaGetLastError(), "svdq_decode_kernel launch");
   if (st != PALU_OK) return st;
   return split_combine(p.ws, cache->batch, q_heads, cache->kv_heads, p.n_chunks, out, out_fp32, strm);
 }
