@@ -218,7 +218,7 @@ __device__ __forceinline__ void project_tc(const __half* xs, const float* __rest
 // the tail rows the CTA of the new partial block overwrites.
 // counts (device [batch], or NULL): sequence b appends the first counts[b]
 // of its T rows; NULL appends all T rows of every sequence.
-__global__ void __launch_bounds__(128) encode_append_kernel(CacheView cv, const __half* __restrict__ x,
+__global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, const __half* __restrict__ x,
                                                             long long T, int Hkv, int phase, const int* counts) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int r = cv.r;
