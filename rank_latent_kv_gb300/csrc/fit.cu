@@ -399,6 +399,54 @@ __device__ __forceinline__ void df_rotate(float ch, float cl, float sh, float sl
   yl = nyl;
 }
 
+// Double-float (fp32 pair) arithmetic for the rotation angles (Dekker's
+// error-free product and sum; the pair division and square root refine an
+// fp32 quotient or root by the residual): about 44 significant bits, on the
+// fp32 pipes, where this part's fp64 rate made the angles the slow step of a
+// round.  Explicit rounding intrinsics keep the compiler from contracting
+// the error terms.
+struct Dfl {
+  float h, l;
+};
+__device__ __forceinline__ Dfl dfl_norm(float s, float e) {  // |s| >= |e|
+  const float h = __fadd_rn(s, e);
+  return Dfl{h, __fsub_rn(e, __fsub_rn(h, s))};
+}
+__device__ __forceinline__ Dfl dfl_neg(Dfl a) { return Dfl{-a.h, -a.l}; }
+__device__ __forceinline__ Dfl dfl_add(Dfl a, Dfl b) {  // operands that do not cancel
+  float s, e;
+  two_sum(a.h, b.h, s, e);
+  return dfl_norm(s, __fadd_rn(__fadd_rn(e, a.l), b.l));
+}
+__device__ __forceinline__ Dfl dfl_add_exact(Dfl a, Dfl b) {  // also under cancellation
+  float s1, e1, s2, e2;
+  two_sum(a.h, b.h, s1, e1);
+  two_sum(a.l, b.l, s2, e2);
+  const Dfl t = dfl_norm(s1, __fadd_rn(e1, s2));
+  return dfl_norm(t.h, __fadd_rn(t.l, e2));
+}
+__device__ __forceinline__ Dfl dfl_mul(Dfl a, Dfl b) {
+  const float p = __fmul_rn(a.h, b.h);
+  float e = __fmaf_rn(a.h, b.h, -p);
+  e = __fmaf_rn(a.h, b.l, e);
+  e = __fmaf_rn(a.l, b.h, e);
+  return dfl_norm(p, e);
+}
+__device__ __forceinline__ Dfl dfl_div(Dfl a, Dfl b) {
+  const float q1 = __fdiv_rn(a.h, b.h);
+  const Dfl r1 = dfl_add_exact(a, dfl_neg(dfl_mul(Dfl{q1, 0.f}, b)));
+  const float q2 = __fdiv_rn(r1.h, b.h);
+  const Dfl r2 = dfl_add_exact(r1, dfl_neg(dfl_mul(Dfl{q2, 0.f}, b)));
+  const float q3 = __fdiv_rn(r2.h, b.h);
+  return dfl_add(dfl_norm(q1, q2), Dfl{q3, 0.f});
+}
+__device__ __forceinline__ Dfl dfl_sqrt(Dfl a) {  // a > 0
+  const float s1 = __fsqrt_rn(a.h);
+  const float p = __fmul_rn(s1, s1), pe = __fmaf_rn(s1, s1, -p);  // s1^2 = p + pe exactly
+  const Dfl r = dfl_add_exact(a, Dfl{-p, -pe});
+  return dfl_norm(s1, __fdiv_rn(r.h, __fmul_rn(2.f, s1)));
+}
+
 constexpr int kJacBlocks = 64 * 65 / 2;  // 2x2 blocks (pair a, pair b), a <= b, of a round
 
 // A is kept symmetric: entry {i, j} lives once, at row min(i, j), column
@@ -460,30 +508,41 @@ __global__ void __launch_bounds__(kJacThreads) jacobi_kernel(const __grid_consta
   // off-diagonal entries below these bounds are at the pairs' rounding level
   const double floor_abs = kJacFloor * sqrt(fro_all);
 
-  // The rotations of round k (buffer k & 1) from the current A, by warps 0-1
-  // (an fp64 instruction costs a whole warp's issue on this part, active
-  // lanes or not, so the 64 angles go to two full warps).
+  // The rotations of round k (buffer k & 1) from the current A, by warps 0-1,
+  // in double-float arithmetic: theta = (a_qq - a_pp) / (2 a_pq),
+  // t = sign(theta) / (|theta| + sqrt(theta^2 + 1)) (1 / (2 theta) past
+  // |theta| = 2^40), c = 1 / sqrt(t^2 + 1), s = t c.  The difference a_qq -
+  // a_pp is formed exactly, so theta keeps its relative accuracy when the
+  // diagonal entries nearly cancel.
+  const float floor_f = (float)floor_abs;
   auto angles = [&](int rnd, int buf) {
     int p, q;
     rr_pair(rnd, tid, p, q);
-    const double apq = a64(p, q), app = a64(p, p), aqq = a64(q, q);
-    double c = 1.0, s = 0.0;
-    if (fabs(apq) > fmax(kJacRel * sqrt(fabs(app * aqq)), floor_abs)) {
-      const double theta = (aqq - app) / (2.0 * apq);
-      const double t = (theta >= 0.0 ? 1.0 : -1.0) / (fabs(theta) + sqrt(theta * theta + 1.0));
-      c = 1.0 / sqrt(t * t + 1.0);
-      s = t * c;
+    const Dfl apq{Ah[sym(p, q)], Al[sym(p, q)]}, app{Ah[p * kLdA + p], Al[p * kLdA + p]},
+        aqq{Ah[q * kLdA + q], Al[q * kLdA + q]};
+    Dfl c{1.f, 0.f}, s{0.f, 0.f};
+    if (fabsf(apq.h) > fmaxf((float)kJacRel * sqrtf(fabsf(app.h)) * sqrtf(fabsf(aqq.h)), floor_f)) {
+      const Dfl th = dfl_div(dfl_add_exact(aqq, dfl_neg(app)), Dfl{2.f * apq.h, 2.f * apq.l});
+      Dfl t;
+      if (fabsf(th.h) > 0x1p40f) {
+        t = dfl_div(Dfl{0.5f, 0.f}, th);
+      } else {
+        const Dfl root = dfl_sqrt(dfl_add(dfl_mul(th, th), Dfl{1.f, 0.f}));
+        t = dfl_div(Dfl{1.f, 0.f}, dfl_add(th.h >= 0.f ? th : dfl_neg(th), root));
+        if (th.h < 0.f) t = dfl_neg(t);
+      }
+      c = dfl_div(Dfl{1.f, 0.f}, dfl_sqrt(dfl_add(dfl_mul(t, t), Dfl{1.f, 0.f})));
+      s = dfl_mul(t, c);
       atomicAdd(cnt, 1);
     }
     float* r = rot + buf * 256;
     int* ix = pq + buf * 128;
     ix[tid] = p;
     ix[64 + tid] = q;
-    const float ch = (float)c, sh = (float)s;
-    r[tid] = ch;
-    r[64 + tid] = (float)(c - (double)ch);
-    r[128 + tid] = sh;
-    r[192 + tid] = (float)(s - (double)sh);
+    r[tid] = c.h;
+    r[64 + tid] = c.l;
+    r[128 + tid] = s.h;
+    r[192 + tid] = s.l;
   };
   // V <- V J for the rotations in buffer buf, by threads from t0 on
   auto rotate_v = [&](int buf, int t0) {
