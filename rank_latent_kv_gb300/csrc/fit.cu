@@ -82,6 +82,10 @@ __global__ void __launch_bounds__(kGramThreads) gram_kernel(const GramParams p) 
   const int ch = tid & 15;
   const bool want = z == 1 || (ch >> 3) == rb;  // a diagonal block reads its own 64 features
   int cb_[kRowsPer], ch_[kRowsPer], ct_[kRowsPer];  // batch, head in group, token of the slot's row
+  const __half* src_[kRowsPer];                      // that row's 16-byte chunk in x
+  auto row_ptr = [&](int i) {
+    return p.x + (((long long)cb_[i] * p.Hkv + (long long)grp * p.hg + ch_[i]) * p.seq + ct_[i]) * kHeadDim + ch * 8;
+  };
 #pragma unroll
   for (int i = 0; i < kRowsPer; ++i) {
     const long long R = R0 + (tid >> 4) + 16 * i;
@@ -89,6 +93,7 @@ __global__ void __launch_bounds__(kGramThreads) gram_kernel(const GramParams p) 
     ct_[i] = (int)(R - bh * p.seq);
     cb_[i] = (int)(bh / p.hg);
     ch_[i] = (int)(bh - (long long)cb_[i] * p.hg);
+    src_[i] = row_ptr(i);
   }
   auto load_tile = [&](int tile, int stage) {
 #pragma unroll
@@ -97,20 +102,23 @@ __global__ void __launch_bounds__(kGramThreads) gram_kernel(const GramParams p) 
       const long long R = R0 + (long long)tile * kGramTile + row;
       const bool valid = R < R1;
       if (want) {
-        const __half* src = valid ? p.x + (((long long)cb_[i] * p.Hkv + (long long)grp * p.hg + ch_[i]) * p.seq + ct_[i]) *
-                                            kHeadDim + ch * 8
-                                  : p.x;
         uint8_t* dst = smem + stage * (kGramTile * 256) + row * 256 + ((ch ^ (row & 7)) << 4);
-        cp_async16_zfill(dst, src, valid);
+        cp_async16_zfill(dst, valid ? src_[i] : p.x, valid);
       }
-      // advance the slot's row by one tile
+      // advance the slot's row by one tile: 64 rows further in the same
+      // (batch, head) unless the token index passes the sequence's end
       ct_[i] += kGramTile;
-      while (ct_[i] >= p.seq) {
-        ct_[i] -= (int)p.seq;
-        if (++ch_[i] == p.hg) {
-          ch_[i] = 0;
-          ++cb_[i];
-        }
+      if (ct_[i] < p.seq) {
+        src_[i] += kGramTile * kHeadDim;
+      } else {
+        do {
+          ct_[i] -= (int)p.seq;
+          if (++ch_[i] == p.hg) {
+            ch_[i] = 0;
+            ++cb_[i];
+          }
+        } while (ct_[i] >= p.seq);
+        src_[i] = row_ptr(i);
       }
     }
   };
