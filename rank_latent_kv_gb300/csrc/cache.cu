@@ -118,6 +118,19 @@ __device__ __noinline__ float exact_latent(const __half* xrow, const float* __re
   return fp_finish(s, lo, m);
 }
 
+// Warp-wide minimum and maximum of a float by one integer reduction each:
+// the float's bits mapped to an unsigned key of the same order (sign bit set
+// for non-negative values, all bits inverted for negative ones).
+__device__ __forceinline__ unsigned int f2key(float f) {
+  const unsigned int b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key2f(unsigned int k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+__device__ __forceinline__ float warp_min(float f) { return key2f(__reduce_min_sync(0xffffffffu, f2key(f))); }
+__device__ __forceinline__ float warp_max(float f) { return key2f(__reduce_max_sync(0xffffffffu, f2key(f))); }
+
 // The quantizer's code of a latent v (fp32 arithmetic, as the oracle):
 // round((v - z) / s) clamped to [0, qmax]; 0 when s is 0.  Non-decreasing in v.
 __device__ __forceinline__ float quant_code(float v, float z32, float s32, float qmax) {
@@ -371,12 +384,10 @@ __global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, con
               ml[q] = v[q] - e[q];
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                mh[q] = fminf(mh[q], __shfl_xor_sync(0xffffffffu, mh[q], o));
-                ml[q] = fmaxf(ml[q], __shfl_xor_sync(0xffffffffu, ml[q], o));
-              }
+            for (int q = 0; q < 4; ++q) {
+              mh[q] = warp_min(mh[q]);
+              ml[q] = warp_max(ml[q]);
+            }
             bool need[4];
             uint32_t bneed[4];
             int tot = 0;
@@ -424,12 +435,10 @@ __global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, con
               ex[q] = bmin | bmax;
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                mn[q] = fminf(mn[q], __shfl_xor_sync(0xffffffffu, mn[q], o));
-                mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], o));
-              }
+            for (int q = 0; q < 4; ++q) {
+              mn[q] = warp_min(mn[q]);
+              mx[q] = warp_max(mx[q]);
+            }
             bool need[4];
             uint32_t bneed[4];
             int tot = 0;
