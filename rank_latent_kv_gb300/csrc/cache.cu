@@ -7,6 +7,12 @@
 // quantizer (blog post "VeloxQuant-MLX 0.8.0 adds KIVI", "What KIVI is") and
 // pack the codes LSB-first (blog post "How I built VeloxQuant-MLX", "The
 // Bit-Packing Problem").
+//
+// The stored latents, scales, zeros and codes are those of the fp32 latents
+// rounded once from an error-free (float-pair) dot product.  Complete blocks
+// of quantized caches are projected on the tensor cores under a rigorous
+// error bound, and the exact latent is formed only where a stored value
+// depends on it; every other latent takes the float-pair path directly.
 #include <math.h>
 
 #include <algorithm>

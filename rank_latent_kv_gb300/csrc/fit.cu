@@ -9,22 +9,24 @@
 //
 // The right singular vectors of X_c are the eigenvectors of the centred Gram
 // matrix X_c^T X_c = X^T X - n mu mu^T.  GB300 plan:
-//   1. gram_kernel: X^T X and the column sums of row chunks (one CTA per SM)
-//      on tensor cores (prefills above 64K rows per group; smaller ones use
+//   1. gram_kernel: X^T X and the column sums of row chunks on tensor cores,
+//      three CTAs per chunk for the symmetric 64 x 64 blocks (0,0), (0,1),
+//      (1,1) (prefills above 64K rows per group; smaller ones use
 //      gram_exact_kernel, exact accumulation on CUDA cores, because at small
-//      row counts the rounding of each 16-row product sum is not yet averaged
-//      down).  fp16 operands are exact; each 16-row product is
-//      promoted from its fresh fp32 accumulator into an error-free fp32 pair,
-//      so the chunk sums carry ~48-bit accuracy.  Rows are staged through
-//      swizzled shared memory by cp.async.
-//   2. reduce_kernel: chunk partials summed in fp64, centred in fp64.
-//   3. jacobi_kernel: one CTA per group diagonalises the 128x128 matrix with
+//      row counts the rounding of each product sum is not yet averaged down).
+//      fp16 operands are exact; each 64-row stage's product sum is promoted
+//      from its fresh fp32 accumulator into an error-free fp32 pair, so the
+//      chunk sums carry ~48-bit accuracy.  Rows are staged through swizzled
+//      shared memory by cp.async.
+//   2. gram_reduce_kernel: chunk partials summed in fp64, centred in fp64.
+//   3. jacobi_kernel: one CTA per group (one launch for all the groups of
+//      all tensors in a batch) diagonalises the 128x128 matrix with
 //      parallel-ordered cyclic Jacobi rotations (64 disjoint pairs per round),
-//      A as fp32 float pairs (about 48 significant bits; error-free updates
-//      on the fp32 pipes), rotation angles in fp64 and the rotations
-//      accumulated in fp32, all in shared memory;
-//      then eigenvalues sorted descending and each direction's sign fixed so
-//      its largest-magnitude entry is positive.
+//      A as symmetric fp32 float pairs (about 48 significant bits; error-free
+//      updates on the fp32 pipes), rotation angles in double-float and the
+//      rotations accumulated in fp32, all in shared memory; then eigenvalues
+//      sorted descending and each direction's sign fixed so its
+//      largest-magnitude entry is positive.
 //   4. host: energy-threshold rank per group, r = minimum.
 #include <math.h>
 
