@@ -151,7 +151,8 @@ palu_status palu_fit(const palu_config* cfg, const void* x, int64_t batch, int32
  *   cfgs       host [n_tensors] configurations (each its own grouping,
  *              rank rule and threshold).
  *   x, basis, mu, eigvals  host [n_tensors] arrays of device pointers, each
- *              as in palu_fit.
+ *              as in palu_fit; every x[t] must hold batch x kv_heads x seq x D
+ *              fp16 values (the call has only the pointers and cannot check).
  *   rank_out   host int32 [n_tensors].
  *   group_ranks host int32 [sum of n_head_groups], tensor after tensor (may
  *              be NULL).

@@ -203,6 +203,8 @@ def palu_fit_batch(cfgs, xs, workspace, bases, mus, eigvals, stream=None):
     palu_fit, per tensor.  Returns (ranks, group_ranks per tensor)."""
     n = len(cfgs)
     B, H, S, _ = xs[0].shape
+    if len(xs) != n or any(tuple(x.shape) != tuple(xs[0].shape) or not x.is_contiguous() for x in xs):
+        raise ValueError("palu_fit_batch needs one contiguous tensor per configuration, all of one shape")
     arr = (palu_config * n)(*cfgs)
     vp = lambda ts: (c_void_p * n)(*[t.data_ptr() for t in ts])
     r = (c_int32 * n)()
@@ -553,6 +555,8 @@ def fit_batch(cfgs, xs, stream=None):
     """Run palu_fit_batch on tensors xs (fp16 [B, Hkv, S, D], one shape) with configurations cfgs;
     returns [(basis, mu, eigvals, rank, group_ranks)] per tensor."""
     B, H, S, D = xs[0].shape
+    if any(tuple(x.shape) != tuple(xs[0].shape) for x in xs):
+        raise ValueError("fit_batch needs tensors of one shape")
     dev = xs[0].device
     ws = _dev_bytes(palu_fit_batch_workspace_size(cfgs, B, H, S), dev)
     bases = [torch.empty(c.n_head_groups, D, D, dtype=torch.float32, device=dev) for c in cfgs]

@@ -79,3 +79,18 @@ def test_fit_batch_argument_errors(P):
     cfg = P.palu_config_default(n_head_groups=3)  # 4 heads are not a multiple of 3 groups
     with pytest.raises(P.PaluError):
         P.fit_batch([cfg], [x])
+
+
+def test_fit_batch_mixes_gram_paths(P):
+    """At one shape, one grouping above 64K rows per group (tensor-core Gram,
+    its own chunk layout) and one below (exact Gram) in one batch, sharing the
+    partial-sum area: each equals its own palu_fit.  Tensors of different
+    shapes are refused by the binding before any launch."""
+    rng = np.random.default_rng(14)
+    xs = [_keys(rng, 2, 8, 8200).to(DEV) for _ in range(2)]
+    cfgs = [P.palu_config_default(n_head_groups=1, rank=0, energy_threshold=0.9),   # 131,200 rows a group
+            P.palu_config_default(n_head_groups=8, rank=24)]                        # 16,400 rows a group
+    _same(P, cfgs, xs)
+    _same(P, cfgs[::-1], xs[::-1])
+    with pytest.raises(ValueError):
+        P.fit_batch(cfgs, [xs[0], xs[1][:, :, :100].contiguous()])
