@@ -156,6 +156,40 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+_F16 = (torch.float16,)
+_OUT = (torch.float32, torch.float16)
+D = 128
+
+
+def _need(t, name, shape, dtypes=_F16, cuda=True):
+    """Refuse, before any launch, a tensor whose pointer does not describe the
+    buffer the C call will read or write: the library sees the pointer only,
+    so a wrong shape, type or stride would go out of bounds or read the wrong
+    elements.  Entries of `shape` that are None match any extent."""
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a tensor")
+    if t.is_cuda != cuda:
+        raise ValueError(f"{name} must be a {'CUDA' if cuda else 'host'} tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}; expected {' or '.join(map(str, dtypes))}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dim() != len(shape) or any(e is not None and e != s for e, s in zip(shape, t.shape)):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}; expected {tuple('*' if e is None else e for e in shape)}")
+
+
+def _dims(c):
+    """(batch, kv_heads) of an initialised cache struct, else (None, None): the
+    library itself reports an uninitialised cache."""
+    return (c.batch, c.kv_heads) if c.magic else (None, None)
+
+
+def _need_q_out(c, q, out, name="q"):
+    B, _ = _dims(c)
+    _need(q, name, (B, None, D))
+    _need(out, "out", tuple(q.shape), _OUT)
+
+
 # ------------------------------------------------------------------ entry points
 
 def palu_last_error() -> str:
@@ -183,7 +217,12 @@ def palu_fit_workspace_size(cfg, batch, kv_heads, seq) -> int:
 def palu_fit(cfg, x, workspace, basis, mu, eigvals, stream=None):
     """x fp16 [B, Hkv, S, D] (cuda); outputs basis fp32 [n_g, D, D], mu fp32 [n_g, D],
     eigvals fp64 [n_g, D] (cuda).  Returns (rank, group_ranks)."""
+    _need(x, "x", (None, None, None, D))
     B, H, S, _ = x.shape
+    ng = cfg.n_head_groups
+    _need(basis, "basis", (ng, D, D), (torch.float32,))
+    _need(mu, "mu", (ng, D), (torch.float32,))
+    _need(eigvals, "eigvals", (ng, D), (torch.float64,))
     r = c_int32()
     gr = (c_int32 * cfg.n_head_groups)()
     _check(lib().palu_fit(ctypes.byref(cfg), _ptr(x), B, H, S, _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -202,9 +241,16 @@ def palu_fit_batch(cfgs, xs, workspace, bases, mus, eigvals, stream=None):
     """Fit len(cfgs) tensors of one shape (xs fp16 [B, Hkv, S, D] each) in one call; outputs as
     palu_fit, per tensor.  Returns (ranks, group_ranks per tensor)."""
     n = len(cfgs)
+    if n == 0 or len(xs) != n or len(bases) != n or len(mus) != n or len(eigvals) != n:
+        raise ValueError("palu_fit_batch needs one tensor and one set of outputs per configuration")
+    _need(xs[0], "xs[0]", (None, None, None, D))
     B, H, S, _ = xs[0].shape
-    if len(xs) != n or any(tuple(x.shape) != tuple(xs[0].shape) or not x.is_contiguous() for x in xs):
-        raise ValueError("palu_fit_batch needs one contiguous tensor per configuration, all of one shape")
+    for i, c in enumerate(cfgs):
+        ng = c.n_head_groups
+        _need(xs[i], f"xs[{i}]", (B, H, S, D))          # one shape for every tensor
+        _need(bases[i], f"bases[{i}]", (ng, D, D), (torch.float32,))
+        _need(mus[i], f"mus[{i}]", (ng, D), (torch.float32,))
+        _need(eigvals[i], f"eigvals[{i}]", (ng, D), (torch.float64,))
     arr = (palu_config * n)(*cfgs)
     vp = lambda ts: (c_void_p * n)(*[t.data_ptr() for t in ts])
     r = (c_int32 * n)()
@@ -228,6 +274,11 @@ def palu_cache_size(cfg, role, rank, batch, kv_heads, capacity):
 
 def palu_cache_init(cfg, role, rank, batch, kv_heads, capacity, basis, basis_ld, mu, blocks, tail, state,
                     stream=None) -> palu_cache:
+    ng = cfg.n_head_groups
+    _need(basis, "basis", (ng, D, None), (torch.float32,))
+    if basis_ld > basis.shape[2]:
+        raise ValueError(f"basis_ld {basis_ld} exceeds the basis tensor's row length {basis.shape[2]}")
+    _need(mu, "mu", (ng, D), (torch.float32,))
     c = palu_cache()
     _check(lib().palu_cache_init(ctypes.byref(c), ctypes.byref(cfg), role, rank, batch, kv_heads, capacity,
                                  _ptr(basis), basis_ld, _ptr(mu), _ptr(blocks), _ptr(tail), _ptr(state),
@@ -236,7 +287,12 @@ def palu_cache_init(cfg, role, rank, batch, kv_heads, capacity, basis, basis_ld,
 
 
 def palu_encode_append(cache: palu_cache, x, tokens=None, stream=None):
+    """x fp16 [B, Hkv, T, D] (device); appends its T tokens (tokens, if given, must equal T)."""
+    B, H = _dims(cache)
+    _need(x, "x", (B, H, None, D))
     T = x.shape[2] if tokens is None else tokens
+    if T != x.shape[2]:
+        raise ValueError(f"tokens {T} differs from x.shape[2] = {x.shape[2]}")
     _check(lib().palu_encode_append(ctypes.byref(cache), _ptr(x), T, _stream(stream)))
 
 
@@ -247,6 +303,8 @@ def palu_decode_workspace_size(k: palu_cache, v: palu_cache, q_heads: int) -> in
 
 
 def palu_decode_attn(k, v, q, out, workspace, softmax_scale=0.0, stream=None):
+    _need_q_out(k, q, out)
+    _need(workspace, "workspace", (None,), (torch.uint8,))
     _check(lib().palu_decode_attn(ctypes.byref(k), ctypes.byref(v), _ptr(q), q.shape[1], softmax_scale, _ptr(out),
                                   1 if out.dtype == torch.float32 else 0, _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
@@ -254,6 +312,11 @@ def palu_decode_attn(k, v, q, out, workspace, softmax_scale=0.0, stream=None):
 
 def palu_decode_step(k, v, k_new, v_new, q, out, workspace, softmax_scale=0.0, stream=None):
     """Append one token of k and v per stream, then decode attention (k_new, v_new: [B, Hkv, D] or [B, Hkv, 1, D])."""
+    B, H = _dims(k)
+    for t, name in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, name, (B, H, D) if t.dim() == 3 else (B, H, 1, D))
+    _need_q_out(k, q, out)
+    _need(workspace, "workspace", (None,), (torch.uint8,))
     _check(lib().palu_decode_step(ctypes.byref(k), ctypes.byref(v), _ptr(k_new), _ptr(v_new), _ptr(q), q.shape[1],
                                   softmax_scale, _ptr(out), 1 if out.dtype == torch.float32 else 0, _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
@@ -261,6 +324,7 @@ def palu_decode_step(k, v, k_new, v_new, q, out, workspace, softmax_scale=0.0, s
 
 def palu_decode_attn_noalloc(k, v, q, out, softmax_scale=0.0, stream=None):
     """palu_decode_attn using the library's fixed device scratch (no workspace)."""
+    _need_q_out(k, q, out)
     _check(lib().palu_decode_attn_noalloc(ctypes.byref(k), ctypes.byref(v), _ptr(q), q.shape[1], softmax_scale,
                                           _ptr(out), 1 if out.dtype == torch.float32 else 0, _stream(stream)))
 
@@ -283,11 +347,13 @@ def palu_cache_save_size(cache) -> int:
 
 def palu_cache_save(cache, host, stream=None):
     """Copy the cache image into `host` (a CPU uint8 tensor of >= palu_cache_save_size bytes)."""
+    _need(host, "host", (None,), (torch.uint8,), cuda=False)
     _check(lib().palu_cache_save(ctypes.byref(cache), c_void_p(host.data_ptr()), host.numel(), _stream(stream)))
 
 
 def palu_cache_restore(cache, host, stream=None):
     """Copy a cache image (a CPU uint8 tensor) into `cache`."""
+    _need(host, "host", (None,), (torch.uint8,), cuda=False)
     _check(lib().palu_cache_restore(ctypes.byref(cache), c_void_p(host.data_ptr()), host.numel(), _stream(stream)))
 
 
@@ -300,13 +366,15 @@ def palu_cache_sync(cache, stream=None) -> int:
 
 def palu_encode_append_ragged(cache: palu_cache, x, counts, stream=None):
     """x [B, Hkv, T, D] fp16 (device); counts int32 [B] (device): sequence b appends its first counts[b] rows."""
-    assert x.is_cuda and x.dtype == torch.float16 and counts.is_cuda and counts.dtype == torch.int32
+    B, H = _dims(cache)
+    _need(x, "x", (B, H, None, D))
+    _need(counts, "counts", (B,), (torch.int32,))
     _check(lib().palu_encode_append_ragged(ctypes.byref(cache), _ptr(x), x.shape[2], _ptr(counts), _stream(stream)))
 
 
 def palu_cache_truncate_ragged(cache: palu_cache, lengths, stream=None):
     """lengths int64 [B] (device): per-sequence rollback."""
-    assert lengths.is_cuda and lengths.dtype == torch.int64
+    _need(lengths, "lengths", (_dims(cache)[0],), (torch.int64,))
     _check(lib().palu_cache_truncate_ragged(ctypes.byref(cache), _ptr(lengths), _stream(stream)))
 
 
@@ -329,7 +397,13 @@ def palu_fp16_decode_workspace_size(batch, kv_heads, seq_cap, q_heads) -> int:
 
 
 def palu_fp16_decode_attn(k, v, seq, q, out, workspace, softmax_scale=0.0, stream=None):
+    """k, v fp16 [B, Hkv, cap, D] (tokens 0..seq-1 used), q fp16 [B, Hq, D], out [B, Hq, D] (device)."""
+    _need(k, "k", (None, None, None, D))
     B, H, cap, _ = k.shape
+    _need(v, "v", (B, H, cap, D))
+    _need(q, "q", (B, None, D))
+    _need(out, "out", tuple(q.shape), _OUT)
+    _need(workspace, "workspace", (None,), (torch.uint8,))
     _check(lib().palu_fp16_decode_attn(_ptr(k), _ptr(v), B, H, seq, cap, _ptr(q), q.shape[1], softmax_scale,
                                        _ptr(out), 1 if out.dtype == torch.float32 else 0, _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream)))
@@ -348,7 +422,13 @@ def palu_kivi_cache_init(batch, kv_heads, capacity, records, window) -> palu_kiv
 
 
 def palu_kivi_append(cache: palu_kivi_cache, k, v, tokens=None, stream=None):
+    """k, v fp16 [B, Hkv, T, D] (device); appends their T tokens (tokens, if given, must equal T)."""
+    B, H = _dims(cache)
+    _need(k, "k", (B, H, None, D))
+    _need(v, "v", tuple(k.shape))
     n = k.shape[2] if tokens is None else tokens
+    if n != k.shape[2]:
+        raise ValueError(f"tokens {n} differs from k.shape[2] = {k.shape[2]}")
     _check(lib().palu_kivi_append(ctypes.byref(cache), _ptr(k), _ptr(v), n, _stream(stream)))
 
 
@@ -359,6 +439,8 @@ def palu_kivi_decode_workspace_size(cache: palu_kivi_cache, q_heads: int) -> int
 
 
 def palu_kivi_decode_attn(cache: palu_kivi_cache, q, out, workspace, softmax_scale=0.0, stream=None):
+    _need_q_out(cache, q, out)
+    _need(workspace, "workspace", (None,), (torch.uint8,))
     _check(lib().palu_kivi_decode_attn(ctypes.byref(cache), _ptr(q), q.shape[1], softmax_scale, _ptr(out),
                                        1 if out.dtype == torch.float32 else 0, _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream)))
@@ -486,6 +568,10 @@ class SvdqCache:
 
     def __init__(self, batch, kv_heads, ranks, capacity, basis, mu, stream=None):
         dev = basis.device
+        if len(ranks) != kv_heads:
+            raise ValueError(f"{len(ranks)} ranks given for {kv_heads} KV heads")
+        _need(basis, "basis", (kv_heads, D, None), (torch.float32,))
+        _need(mu, "mu", (kv_heads, D), (torch.float32,))
         rk = (c_int32 * kv_heads)(*[int(r) for r in ranks])
         bb, tb, sb = c_size_t(), c_size_t(), c_size_t()
         _check(lib().palu_svdq_cache_size(batch, kv_heads, rk, capacity, ctypes.byref(bb), ctypes.byref(tb),
@@ -505,17 +591,21 @@ class SvdqCache:
 
     def append(self, k, stream=None):
         """k fp16 [B, Hkv, T, D] on the device."""
-        assert k.is_cuda and k.dtype == torch.float16 and k.is_contiguous()
+        _need(k, "k", (*_dims(self.c), None, D))
         _check(lib().palu_svdq_append(ctypes.byref(self.c), _ptr(k), k.shape[2], _stream(stream)))
 
     def decode(self, v, q, out_dtype=torch.float32, softmax_scale=0.0, stream=None, workspace=None, out=None):
         """v fp16 [B, Hkv, v_cap, D] (tokens 0..length-1 used), q fp16 [B, Hq, D]; returns out [B, Hq, D]."""
+        _need(v, "v", (*_dims(self.c), None, D))
+        _need(q, "q", (_dims(self.c)[0], None, D))
         if workspace is None:
             n = c_size_t()
             _check(lib().palu_svdq_decode_workspace_size(ctypes.byref(self.c), q.shape[1], ctypes.byref(n)))
             workspace = _dev_bytes(n.value, q.device)
         if out is None:
             out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+        _need(out, "out", tuple(q.shape), _OUT)
+        _need(workspace, "workspace", (None,), (torch.uint8,))
         _check(lib().palu_svdq_decode_attn(ctypes.byref(self.c), _ptr(v), v.shape[2], _ptr(q), q.shape[1],
                                            c_float(softmax_scale), _ptr(out), 1 if out.dtype == torch.float32 else 0,
                                            _ptr(workspace), workspace.numel(), _stream(stream)))

@@ -7,6 +7,7 @@ import subprocess
 import tempfile
 
 import pytest
+import torch
 
 from tests.conftest import ROOT
 
@@ -275,3 +276,31 @@ def test_fit_batch_workspace_and_validation(palu):
     r = (ctypes.c_int32 * 1)()
     assert palu.lib().palu_fit_batch(arr, 1, None, 2, 4, 4096, ctypes.c_void_p(1 << 20), 1 << 30, None, None, None,
                                      r, None, None) == 1
+
+
+def test_binding_refuses_tensors_before_any_call(palu):
+    """The binding checks every tensor whose pointer crosses the C ABI (the
+    library sees the pointer only): device, dtype, contiguity and shape."""
+    x = torch.zeros(2, 3, 5, 128, dtype=torch.float16)
+    palu._need(x, "x", (2, 3, None, 128), cuda=False)
+    for bad in (x.float(), x.transpose(1, 2), x[:, :2], x[..., :64]):
+        with pytest.raises(ValueError):
+            palu._need(bad, "x", (2, 3, None, 128), cuda=False)
+    with pytest.raises(ValueError):
+        palu._need(x, "x", (2, 3, None, 128))                     # a host tensor where the device is needed
+    with pytest.raises(ValueError):
+        palu._need(x.reshape(6, 5, 128), "x", (2, 3, None, 128), cuda=False)
+    with pytest.raises(ValueError):
+        palu._need(torch_like(256), "x", (None,), cuda=False)
+    # the wrappers run the checks before they call the library (host tensors here)
+    c = palu.palu_cache()
+    q = torch.zeros(1, 4, 128, dtype=torch.float16)
+    ws = torch.zeros(256, dtype=torch.uint8)
+    for call in (lambda: palu.palu_decode_attn(c, c, q, q, ws),
+                 lambda: palu.palu_decode_attn_noalloc(c, c, q, q),
+                 lambda: palu.palu_encode_append(c, x),
+                 lambda: palu.palu_fp16_decode_attn(x, x, 5, q, q, ws),
+                 lambda: palu.palu_kivi_decode_attn(palu.palu_kivi_cache(), q, q, ws),
+                 lambda: palu.palu_cache_save(c, torch_like(256))):
+        with pytest.raises(ValueError):
+            call()

@@ -45,7 +45,7 @@ def _raw_sync(P, cache):
 
 
 def _caches(P, rng, B=1, H=2, S=40, cap=64, r=16):
-    basis = torch.linalg.qr(torch.from_numpy(rng.standard_normal((128, 128))))[0].float().to(DEV).unsqueeze(0)
+    basis = torch.linalg.qr(torch.from_numpy(rng.standard_normal((128, 128))))[0].float().contiguous().to(DEV).unsqueeze(0)
     mu = torch.from_numpy(rng.standard_normal((1, 128)).astype(np.float32)).to(DEV)
     cfg = P.palu_config_default(n_head_groups=1, rank=r)
     kc = P.LatentCache(cfg, P.PALU_ROLE_KEY, r, B, H, cap, basis, mu)

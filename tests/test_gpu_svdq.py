@@ -173,5 +173,5 @@ def test_svdq_errors(P):
     with pytest.raises(P.PaluError):
         c.decode(v, torch.zeros(B, 9 * H, 128, dtype=torch.float16, device=DEV))
     with pytest.raises(P.PaluError):
-        c.decode(v[:, :, :32], q)
+        c.decode(v[:, :, :32].contiguous(), q)
     _check_storage(c, oracle)                                  # the refused calls changed nothing

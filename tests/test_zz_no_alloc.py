@@ -89,7 +89,7 @@ def test_noalloc_refuses_partials_larger_than_its_scratch(P):
     B, H, r, cap = 256, 8, 128, 64
     cfg = P.palu_config_default(n_head_groups=1, rank=r)
     q_heads = 8 * H
-    basis = torch.linalg.qr(torch.randn(128, 128, dtype=torch.float64))[0].float().to(DEV).unsqueeze(0)
+    basis = torch.linalg.qr(torch.randn(128, 128, dtype=torch.float64))[0].float().contiguous().to(DEV).unsqueeze(0)
     mu = torch.zeros(1, 128, dtype=torch.float32, device=DEV)
     kc = P.LatentCache(cfg, P.PALU_ROLE_KEY, r, B, H, cap, basis, mu)
     vc = P.LatentCache(cfg, P.PALU_ROLE_VALUE, r, B, H, cap, basis, mu)
