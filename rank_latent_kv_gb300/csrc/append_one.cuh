@@ -12,45 +12,43 @@
 
 namespace palu {
 
-// Position of code (t, j) inside a quantized record: byte offset and shift.
-// Mirrors the layout definition: channel j -> (octet, slot); (token, slot)
-// -> (lane, field k, half); 4-bit octets are u32 words per lane, 2-bit octets
-// u16 halfwords per lane (paired), LSB-first fields.
-__device__ __forceinline__ void code_pos(int role, int n_hi, int n_hi_oct, int n_lo_oct, int t, int j, int& byte,
-                                         int& shift) {
-  int octet, slot;
-  if (j < n_hi) {
-    octet = j >> 3;
-    slot = j & 7;
-  } else {
-    const int jj = j - n_hi;
-    octet = n_hi_oct + (jj >> 3);
-    slot = jj & 7;
+// Pack a block's codes (codes[t * r + j], token t, channel j) into the code
+// area of its quantized record, one storage unit per thread and step: a u32
+// per lane of a 4-bit octet, a u16 per lane of a 2-bit octet (two 2-bit
+// octets share a lane's u32; a lone last one has u16s), LSB-first fields.
+// The layout: channel j -> (octet, slot), hi channels first; within an
+// octet, lane = 4g + c and field k = 0..3 (bits 4k, or 2k, of a half), half
+// 0/1 (bits 0-15 / 16-31, or 0-7 / 8-15).  Keys: token t = g + 8k, slot
+// 2c + half.  Values: slot g, token t = 8k + 2c + half.  Padding channels of
+// an octet hold code 0.  Every byte of the code area is written.
+__device__ __forceinline__ void pack_codes(const uint8_t* codes, int r, int role, int n_hi, int n_hi_oct,
+                                           int n_lo_oct, uint8_t* rec, int tid, int nthreads) {
+  const int npair = n_lo_oct >> 1;
+  const bool key = role == PALU_ROLE_KEY;
+  for (int u = tid; u < 32 * (n_hi_oct + n_lo_oct); u += nthreads) {
+    const int octet = u >> 5, lane = u & 31, g = lane >> 2, c = lane & 3;
+    const bool hi = octet < n_hi_oct;
+    const int j0 = hi ? 8 * octet : n_hi + 8 * (octet - n_hi_oct);
+    const int jlim = hi ? n_hi : r;
+    uint32_t w = 0u;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int j = j0 + (key ? 2 * c + half : g);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int t = key ? g + 8 * k : 8 * k + 2 * c + half;
+        const uint32_t code = j < jlim ? codes[t * r + j] : 0u;
+        w |= code << (hi ? 4 * k + 16 * half : 2 * k + 8 * half);
+      }
+    }
+    if (hi) {
+      *reinterpret_cast<uint32_t*>(rec + 128 * octet + 4 * lane) = w;
+    } else {
+      const int lo = octet - n_hi_oct;
+      const int unit = 128 * n_hi_oct + (lo < 2 * npair ? 128 * (lo >> 1) + 4 * lane + 2 * (lo & 1) : 128 * npair + 2 * lane);
+      *reinterpret_cast<uint16_t*>(rec + unit) = (uint16_t)w;
+    }
   }
-  const int k = 2 * (t >> 4) + ((t & 15) >> 3);
-  int g, c, half;
-  if (role == PALU_ROLE_KEY) {
-    g = t & 7;
-    c = slot >> 1;
-    half = slot & 1;
-  } else {
-    g = slot;
-    c = (t & 7) >> 1;
-    half = t & 1;
-  }
-  const int lane = 4 * g + c;
-  int unit, bit;
-  if (octet < n_hi_oct) {
-    unit = 128 * octet + 4 * lane;
-    bit = 4 * k + 16 * half;
-  } else {
-    const int lo = octet - n_hi_oct;
-    const int npair = n_lo_oct >> 1;
-    unit = 128 * n_hi_oct + (lo < 2 * npair ? 128 * (lo >> 1) + 4 * lane + 2 * (lo & 1) : 128 * npair + 2 * lane);
-    bit = 2 * k + 8 * half;
-  }
-  byte = unit + (bit >> 3);
-  shift = bit & 7;
 }
 
 __device__ __forceinline__ int latent_off(int t, int j) {
@@ -225,7 +223,6 @@ __device__ __forceinline__ float append_one_token(const CacheView& cv, const __h
   // the token completes the block: quantize and pack it like a prefill block
   uint8_t* rec = sm.rec;
   for (int i = tid; i < (kBlock - 1) * r; i += blockDim.x) lat[(i / r) * ld + (i % r)] = tail[i];
-  for (int i = tid; i < cv.rec_bytes / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(rec)[i] = 0u;
   __syncthreads();
   for (int j = tid; j < r; j += blockDim.x) {
     float mn = lat[j], mx = lat[j];
@@ -248,12 +245,7 @@ __device__ __forceinline__ float append_one_token(const CacheView& cv, const __h
     }
   }
   __syncthreads();
-  for (int i = tid; i < kBlock * r; i += blockDim.x) {
-    const int t = i / r, j = i % r;
-    int byte, shift;
-    code_pos(cv.role, cv.n_hi, cv.n_hi_oct, cv.n_lo_oct, t, j, byte, shift);
-    atomicOr(reinterpret_cast<unsigned int*>(rec + (byte & ~3)), (unsigned int)sm.codes[i] << (8 * (byte & 3) + shift));
-  }
+  pack_codes(sm.codes, r, cv.role, cv.n_hi, cv.n_hi_oct, cv.n_lo_oct, rec, tid, blockDim.x);
   const int n_pad = 8 * cv.n_oct;
   const int szb = 128 * cv.n_hi_oct + 64 * cv.n_lo_oct;
   __half* r16 = reinterpret_cast<__half*>(rec + szb);

@@ -364,7 +364,6 @@ __global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, con
           lat[t * (r + 1) + j] = tail[t * r + j];
           err[t * (r + 1) + j] = 0.f;
         }
-        for (int i = tid; i < cv.rec_bytes / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(rec)[i] = 0u;
         __syncthreads();
         {  // complete block of a quantized cache: tc holds
           // Each new latent is known to within e = 2^-15 (|x_t|_2 |V_j|_2 +
@@ -512,13 +511,9 @@ __global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, con
           }
         }
         __syncthreads();
-        // pack codes (each byte assembled by the thread owning it: fields are disjoint)
-        for (int i = tid; i < kBlock * r; i += blockDim.x) {
-          const int t = i / r, j = i % r;
-          int byte, shift;
-          code_pos(cv.role, cv.n_hi, cv.n_hi_oct, cv.n_lo_oct, t, j, byte, shift);
-          atomicOr(reinterpret_cast<unsigned int*>(rec + (byte & ~3)), (unsigned int)codes[i] << (8 * (byte & 3) + shift));
-        }
+        // every byte of the record is written: the code area by the packer, the
+        // scale / zero area below
+        pack_codes(codes, r, cv.role, cv.n_hi, cv.n_hi_oct, cv.n_lo_oct, rec, tid, blockDim.x);
         // scale / zero per padded channel
         const int n_pad = 8 * cv.n_oct;
         const int szb = 128 * cv.n_hi_oct + 64 * cv.n_lo_oct;
