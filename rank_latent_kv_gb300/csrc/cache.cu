@@ -59,7 +59,7 @@ __global__ void cache_init_kernel(const float* __restrict__ basis, int ld, const
 // quantized cache) reads the basis from global memory and is launched
 // without it.
 struct EncodeSmem {
-  int xs_off, cand_off, lat_off, err_off, codes_off, sz_off, rec_off, work_off, basis_off, total;
+  int xs_off, lat_off, err_off, codes_off, sz_off, rec_off, work_off, basis_off, total;
 };
 
 __host__ __device__ inline int align16(int x) { return (x + 15) / 16 * 16; }
@@ -69,8 +69,7 @@ constexpr int kXsStride = kHeadDim + 8;  // halves per staged row: 272 B, so ldm
 __host__ __device__ inline EncodeSmem encode_smem(int r, int rec_bytes) {
   EncodeSmem s;
   s.xs_off = 0;                                                        // half [32][136]
-  s.cand_off = s.xs_off + kBlock * kXsStride * 2;                      // u32 [2][128]: min / max candidates
-  s.lat_off = s.cand_off + 8 * kHeadDim;                               // float [32][r+1]
+  s.lat_off = s.xs_off + kBlock * kXsStride * 2;                       // float [32][r+1]
   s.err_off = s.lat_off + align16(4 * kBlock * (r + 1));               // float [32][r+1]: bound of |L' - L|
   s.codes_off = s.err_off + align16(4 * kBlock * (r + 1));             // u8 [32][r]
   s.sz_off = s.codes_off + align16(kBlock * r);                        // half2 [r] (scale, zero)
@@ -124,9 +123,9 @@ __device__ __noinline__ float exact_latent(const __half* xrow, const float* __re
   return fp_finish(s, lo, m);
 }
 
-// Warp-wide minimum and maximum of a float by one integer reduction each:
-// the float's bits mapped to an unsigned key of the same order (sign bit set
-// for non-negative values, all bits inverted for negative ones).
+// A float's bits mapped to an unsigned key of the same order (sign bit set
+// for non-negative values, all bits inverted for negative ones; -0 below +0),
+// and back: exact minima and maxima by integer comparisons.
 __device__ __forceinline__ unsigned int f2key(float f) {
   const unsigned int b = __float_as_uint(f);
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
@@ -134,8 +133,22 @@ __device__ __forceinline__ unsigned int f2key(float f) {
 __device__ __forceinline__ float key2f(unsigned int k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
-__device__ __forceinline__ float warp_min(float f) { return key2f(__reduce_min_sync(0xffffffffu, f2key(f))); }
-__device__ __forceinline__ float warp_max(float f) { return key2f(__reduce_max_sync(0xffffffffu, f2key(f))); }
+
+// Append (t, j) for every set bit t of `bits` to a shared work list: one
+// counter reservation per warp (every lane calls), a lane's entries together.
+__device__ __forceinline__ void push_work(uint16_t* work, int* count, uint32_t bits, int j, int lane) {
+  const int n = __popc(bits);
+  int incl = n;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  int base = 0;
+  if (lane == 31 && incl) base = atomicAdd(count, incl);
+  base = __shfl_sync(0xffffffffu, base, 31) + incl - n;
+  for (uint32_t m = bits; m; m &= m - 1u) work[base++] = (uint16_t)((__ffs(m) - 1) * 128 + j);
+}
 
 // The quantizer's code of a latent v (fp32 arithmetic, as the oracle):
 // round((v - z) / s) clamped to [0, qmax]; 0 when s is 0.  Non-decreasing in v.
@@ -244,7 +257,6 @@ __global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, con
   const EncodeSmem L = encode_smem(r, cv.rec_bytes);
   __half* xs = reinterpret_cast<__half*>(smem + L.xs_off);
   float* err = reinterpret_cast<float*>(smem + L.err_off);
-  uint32_t* cand = reinterpret_cast<uint32_t*>(smem + L.cand_off);
   int* n_work = reinterpret_cast<int*>(smem + L.work_off);
   uint32_t* wmax_s = reinterpret_cast<uint32_t*>(smem + L.work_off + 8);  // each warp's largest scale
   uint16_t* work = reinterpret_cast<uint16_t*>(smem + L.work_off + 24);
@@ -366,131 +378,90 @@ __global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, con
         }
         __syncthreads();
         {  // complete block of a quantized cache: tc holds
-          // Each new latent is known to within e = 2^-15 (|x_t|_2 |V_j|_2 +
-          // |mu.V_j|) (tail rows exactly).  Only tokens that can hold the
-          // block's minimum or maximum need their exact latent, so scale and
-          // zero are those of the exact latents; a code is taken from the
-          // bound interval when both ends give the same code (the quantizer
-          // is monotone), else from the exact latent.  Channels go warp by
-          // warp (lane = token); the exact latents are computed by all
-          // threads from shared work lists of (token, channel) pairs.
-          const int warp = tid >> 5, lane = tid & 31, t = lane;
-          const uint32_t lt = (1u << lane) - 1u;
-          // four channels a pass (j0, j0 + 4, j0 + 8, j0 + 12) so their shuffle
-          // chains overlap; one list reservation per pass
-          for (int j0 = warp; j0 < r; j0 += 16) {
-            float v[4], e[4], mh[4], ml[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const bool ok = j0 + 4 * q < r;  // uniform
-              v[q] = ok ? lat[t * (r + 1) + j0 + 4 * q] : 0.f;
-              e[q] = ok ? err[t * (r + 1) + j0 + 4 * q] : 0.f;
-              mh[q] = v[q] + e[q];
-              ml[q] = v[q] - e[q];
+          // Each new latent is known to within its bound err (tail rows
+          // exactly).  Only tokens that can hold the block's minimum or
+          // maximum need their exact latent, so scale and zero are those of
+          // the exact latents; a code is taken from the bound interval when
+          // the whole interval rounds to one code (the quantizer is
+          // monotone), else from the exact latent.  One thread per channel
+          // walks the block's 32 tokens (r <= 128 = blockDim.x); the exact
+          // latents are computed by all threads from shared work lists of
+          // (token, channel) pairs.
+          const int warp = tid >> 5, lane = tid & 31, j = tid;
+          const bool own = j < r;
+          const uint32_t fresh = ~((1u << off_new) - 1u);  // tokens of this append (off_new <= 31)
+          const int ld = r + 1;
+          // the candidates: tokens whose interval reaches below the smallest
+          // upper end (minimum) or above the largest lower end (maximum)
+          uint32_t bmin = 0u, bmax = 0u;
+          if (own) {
+            float mh = INFINITY, ml = -INFINITY;
+#pragma unroll 8
+            for (int t = 0; t < kBlock; ++t) {
+              const float v = lat[t * ld + j], e = err[t * ld + j];
+              mh = fminf(mh, v + e);
+              ml = fmaxf(ml, v - e);
             }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              mh[q] = warp_min(mh[q]);
-              ml[q] = warp_max(ml[q]);
-            }
-            bool need[4];
-            uint32_t bneed[4];
-            int tot = 0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int j = j0 + 4 * q;
-              const bool ok = j < r;
-              const bool cmin = ok && v[q] - e[q] <= mh[q], cmax = ok && v[q] + e[q] >= ml[q];
-              const uint32_t bmin = __ballot_sync(0xffffffffu, cmin), bmax = __ballot_sync(0xffffffffu, cmax);
-              need[q] = (cmin || cmax) && t >= off_new;
-              bneed[q] = __ballot_sync(0xffffffffu, need[q]);
-              tot += __popc(bneed[q]);
-              if (lane == 0 && ok) {
-                cand[j] = bmin;
-                cand[kHeadDim + j] = bmax;
-              }
-            }
-            int base = 0;
-            if (lane == 0 && tot) base = atomicAdd(&n_work[0], tot);
-            base = __shfl_sync(0xffffffffu, base, 0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (need[q]) work[base + __popc(bneed[q] & lt)] = (uint16_t)(t * 128 + j0 + 4 * q);
-              base += __popc(bneed[q]);
+#pragma unroll 8
+            for (int t = 0; t < kBlock; ++t) {
+              const float v = lat[t * ld + j], e = err[t * ld + j];
+              if (v - e <= mh) bmin |= 1u << t;
+              if (v + e >= ml) bmax |= 1u << t;
             }
           }
+          push_work(work, &n_work[0], (bmin | bmax) & fresh, j, lane);
           __syncthreads();
           for (int i = tid; i < n_work[0]; i += blockDim.x) {
             const int tt = work[i] >> 7, jj = work[i] & 127;
-            lat[tt * (r + 1) + jj] =
+            lat[tt * ld + jj] =
                 exact_latent(xs + tt * kXsStride, bT + (size_t)jj * kHeadDim, cv.mv[(size_t)grp * r + jj]);
           }
           __syncthreads();
-          uint32_t wmax = 0u;  // the largest scale of this warp's channels (fp32 bits of a non-negative value)
-          for (int j0 = warp; j0 < r; j0 += 16) {
-            float v[4], mn[4], mx[4];
-            uint32_t ex[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const bool ok = j0 + 4 * q < r;  // uniform
-              const uint32_t bmin = ok ? cand[j0 + 4 * q] : 0u, bmax = ok ? cand[kHeadDim + j0 + 4 * q] : 0u;
-              v[q] = ok ? lat[t * (r + 1) + j0 + 4 * q] : 0.f;
-              mn[q] = (bmin >> t) & 1u ? v[q] : INFINITY;
-              mx[q] = (bmax >> t) & 1u ? v[q] : -INFINITY;
-              ex[q] = bmin | bmax;
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              mn[q] = warp_min(mn[q]);
-              mx[q] = warp_max(mx[q]);
-            }
-            bool need[4];
-            uint32_t bneed[4];
-            int tot = 0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int j = j0 + 4 * q;
-              need[q] = false;
-              if (j < r) {  // uniform
-                const float qmax = (float)((1 << (j < cv.n_hi ? 4 : 2)) - 1);
-                const float scale = __fdiv_rn(__fsub_rn(mx[q], mn[q]), qmax);
-                const __half sh = __float2half_rn(scale);
-                const __half zh = __float2half_rn(mn[q]);
-                const float s32 = __half2float(sh), z32 = __half2float(zh);
-                if (lane == 0) sz[j] = __halves2half2(sh, zh);
-                wmax = max(wmax, __float_as_uint(s32));
-                float qc;
-                if (t < off_new || ((ex[q] >> t) & 1u)) {
-                  qc = quant_code(v[q], z32, s32, qmax);  // exact latent
-                } else if (s32 == 0.f) {
-                  qc = 0.f;
-                } else {
-                  // the exact code is round(fl((L - z) / s)) for some L in [v - e, v + e]:
-                  // it is known when that interval, scaled by an approximate 1/s and
-                  // widened by the approximation's error, lies inside one rounding
-                  // cell; else it is decided from the exact latent below
-                  float inv;
-                  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(s32));
-                  const float e = err[t * (r + 1) + j];
-                  const float u = (v[q] - z32) * inv, du = fmaf(e, inv, fmaf(fabsf(u), 0x1p-18f, 0x1p-20f));
-                  const float k = rintf(u);
-                  need[q] = fabsf(u - k) + du >= 0.5f;
-                  qc = fminf(fmaxf(k, 0.f), qmax);
-                }
-                codes[t * r + j] = (uint8_t)qc;
+          uint32_t need = 0u, wmax = 0u;  // wmax: the fp32 bits of this channel's (non-negative) scale
+          if (own) {
+            // minimum and maximum over the candidates' exact latents (an
+            // unsigned key of the same order, so that the stored zero keeps
+            // the sign of the minimum's zero as the oracle's)
+            unsigned int kmn = 0xffffffffu, kmx = 0u;
+            for (uint32_t m = bmin; m; m &= m - 1u) kmn = min(kmn, f2key(lat[(__ffs(m) - 1) * ld + j]));
+            for (uint32_t m = bmax; m; m &= m - 1u) kmx = max(kmx, f2key(lat[(__ffs(m) - 1) * ld + j]));
+            const float mn = key2f(kmn), mx = key2f(kmx);
+            const float qmax = (float)((1 << (j < cv.n_hi ? 4 : 2)) - 1);
+            const float scale = __fdiv_rn(__fsub_rn(mx, mn), qmax);
+            const __half sh = __float2half_rn(scale);
+            const __half zh = __float2half_rn(mn);
+            const float s32 = __half2float(sh), z32 = __half2float(zh);
+            sz[j] = __halves2half2(sh, zh);
+            wmax = __float_as_uint(s32);
+            if (s32 == 0.f) {
+              for (int t = 0; t < kBlock; ++t) codes[t * r + j] = 0;
+            } else {
+              // the exact code is round(fl((L - z) / s)) for some L in [v - e, v + e]:
+              // it is known when that interval, scaled by an approximate 1/s and
+              // widened by the approximation's error, lies inside one rounding
+              // cell; else it is decided from the exact latent below
+              float inv;
+              asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(s32));
+#pragma unroll 8
+              for (int t = 0; t < kBlock; ++t) {
+                const float v = lat[t * ld + j], e = err[t * ld + j];
+                const float u = (v - z32) * inv, du = fmaf(e, inv, fmaf(fabsf(u), 0x1p-18f, 0x1p-20f));
+                const float k = rintf(u);
+                if (fabsf(u - k) + du >= 0.5f) need |= 1u << t;
+                codes[t * r + j] = (uint8_t)fminf(fmaxf(k, 0.f), qmax);
               }
-              bneed[q] = __ballot_sync(0xffffffffu, need[q]);
-              tot += __popc(bneed[q]);
-            }
-            int base = 0;
-            if (lane == 0 && tot) base = atomicAdd(&n_work[1], tot);
-            base = __shfl_sync(0xffffffffu, base, 0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (need[q]) work[base + __popc(bneed[q] & lt)] = (uint16_t)(t * 128 + j0 + 4 * q);
-              base += __popc(bneed[q]);
+              // tokens whose exact latent is at hand: the candidates and the
+              // earlier tokens of the block (from the tail)
+              const uint32_t exact = bmin | bmax | ~fresh;
+              need &= ~exact;
+              for (uint32_t m = exact; m; m &= m - 1u) {
+                const int t = __ffs(m) - 1;
+                codes[t * r + j] = (uint8_t)quant_code(lat[t * ld + j], z32, s32, qmax);
+              }
             }
           }
+          push_work(work, &n_work[1], need, j, lane);
+          wmax = __reduce_max_sync(0xffffffffu, wmax);
           if (lane == 0) wmax_s[warp] = wmax;
           __syncthreads();
           // the block's largest scale into the stream's and the cache's maxima:
