@@ -379,34 +379,53 @@ __global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, con
         __syncthreads();
         {  // complete block of a quantized cache: tc holds
           // Each new latent is known to within its bound err (tail rows
-          // exactly).  Only tokens that can hold the block's minimum or
-          // maximum need their exact latent, so scale and zero are those of
-          // the exact latents; a code is taken from the bound interval when
-          // the whole interval rounds to one code (the quantizer is
-          // monotone), else from the exact latent.  One thread per channel
-          // walks the block's 32 tokens (r <= 128 = blockDim.x); the exact
-          // latents are computed by all threads from shared work lists of
-          // (token, channel) pairs.
+          // exactly).  The block's minimum over a channel then lies in
+          // [min (v - e), min (v + e)] and its maximum in [max (v - e),
+          // max (v + e)]; zero = fp16(min) and scale = fp16(fl(fl(max - min)
+          // / qmax)) are monotone in them, so when both ends of those
+          // intervals give the same fp16 values they are the exact path's.
+          // Only the other channels need exact latents, of the tokens that can
+          // hold the minimum or maximum.  A code is taken from the bound
+          // interval when the whole interval rounds to one code (the
+          // quantizer is monotone), else from the exact latent.  One thread
+          // per channel walks the block's 32 tokens (r <= 128 = blockDim.x);
+          // the exact latents are computed by all threads from shared work
+          // lists of (token, channel) pairs.
           const int warp = tid >> 5, lane = tid & 31, j = tid;
           const bool own = j < r;
           const uint32_t fresh = ~((1u << off_new) - 1u);  // tokens of this append (off_new <= 31)
           const int ld = r + 1;
-          // the candidates: tokens whose interval reaches below the smallest
-          // upper end (minimum) or above the largest lower end (maximum)
-          uint32_t bmin = 0u, bmax = 0u;
+          const float qmax = (float)((1 << (j < cv.n_hi ? 4 : 2)) - 1);
+          uint32_t bmin = 0u, bmax = 0u;  // candidates of an uncertain channel
+          bool certain = false;
           if (own) {
-            float mh = INFINITY, ml = -INFINITY;
+            float mh = INFINITY, ml = -INFINITY, lmin = INFINITY, hmax = -INFINITY;
 #pragma unroll 8
             for (int t = 0; t < kBlock; ++t) {
               const float v = lat[t * ld + j], e = err[t * ld + j];
-              mh = fminf(mh, v + e);
-              ml = fmaxf(ml, v - e);
+              const float vh = v + e, vl = v - e;
+              mh = fminf(mh, vh);
+              lmin = fminf(lmin, vl);
+              ml = fmaxf(ml, vl);
+              hmax = fmaxf(hmax, vh);
             }
+            const __half za = __float2half_rn(lmin), zb = __float2half_rn(mh);
+            const __half sa = __float2half_rn(__fdiv_rn(__fsub_rn(ml, mh), qmax));
+            const __half sb = __float2half_rn(__fdiv_rn(__fsub_rn(hmax, lmin), qmax));
+            // (a zero that rounds to +-0 goes the exact way, which orders -0 below +0)
+            certain = __half_as_ushort(za) == __half_as_ushort(zb) && (__half_as_ushort(za) & 0x7fffu) != 0u &&
+                      __half_as_ushort(sa) == __half_as_ushort(sb);
+            if (certain) {
+              sz[j] = __halves2half2(sa, za);
+            } else {
+              // the candidates: tokens whose interval reaches below the smallest
+              // upper end (minimum) or above the largest lower end (maximum)
 #pragma unroll 8
-            for (int t = 0; t < kBlock; ++t) {
-              const float v = lat[t * ld + j], e = err[t * ld + j];
-              if (v - e <= mh) bmin |= 1u << t;
-              if (v + e >= ml) bmax |= 1u << t;
+              for (int t = 0; t < kBlock; ++t) {
+                const float v = lat[t * ld + j], e = err[t * ld + j];
+                if (v - e <= mh) bmin |= 1u << t;
+                if (v + e >= ml) bmax |= 1u << t;
+              }
             }
           }
           push_work(work, &n_work[0], (bmin | bmax) & fresh, j, lane);
@@ -419,19 +438,18 @@ __global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, con
           __syncthreads();
           uint32_t need = 0u, wmax = 0u;  // wmax: the fp32 bits of this channel's (non-negative) scale
           if (own) {
-            // minimum and maximum over the candidates' exact latents (an
-            // unsigned key of the same order, so that the stored zero keeps
-            // the sign of the minimum's zero as the oracle's)
-            unsigned int kmn = 0xffffffffu, kmx = 0u;
-            for (uint32_t m = bmin; m; m &= m - 1u) kmn = min(kmn, f2key(lat[(__ffs(m) - 1) * ld + j]));
-            for (uint32_t m = bmax; m; m &= m - 1u) kmx = max(kmx, f2key(lat[(__ffs(m) - 1) * ld + j]));
-            const float mn = key2f(kmn), mx = key2f(kmx);
-            const float qmax = (float)((1 << (j < cv.n_hi ? 4 : 2)) - 1);
-            const float scale = __fdiv_rn(__fsub_rn(mx, mn), qmax);
-            const __half sh = __float2half_rn(scale);
-            const __half zh = __float2half_rn(mn);
-            const float s32 = __half2float(sh), z32 = __half2float(zh);
-            sz[j] = __halves2half2(sh, zh);
+            if (!certain) {
+              // minimum and maximum over the candidates' exact latents (an
+              // unsigned key of the same order, so that the stored zero keeps
+              // the sign of the minimum's zero as the oracle's)
+              unsigned int kmn = 0xffffffffu, kmx = 0u;
+              for (uint32_t m = bmin; m; m &= m - 1u) kmn = min(kmn, f2key(lat[(__ffs(m) - 1) * ld + j]));
+              for (uint32_t m = bmax; m; m &= m - 1u) kmx = max(kmx, f2key(lat[(__ffs(m) - 1) * ld + j]));
+              const float mn = key2f(kmn), mx = key2f(kmx);
+              sz[j] = __halves2half2(__float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), qmax)), __float2half_rn(mn));
+            }
+            const __half2 szj = sz[j];
+            const float s32 = __low2float(szj), z32 = __high2float(szj);
             wmax = __float_as_uint(s32);
             if (s32 == 0.f) {
               for (int t = 0; t < kBlock; ++t) codes[t * r + j] = 0;
@@ -450,8 +468,8 @@ __global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, con
                 if (fabsf(u - k) + du >= 0.5f) need |= 1u << t;
                 codes[t * r + j] = (uint8_t)fminf(fmaxf(k, 0.f), qmax);
               }
-              // tokens whose exact latent is at hand: the candidates and the
-              // earlier tokens of the block (from the tail)
+              // tokens whose exact latent is at hand: the candidates of an
+              // uncertain channel and the earlier tokens of the block (tail)
               const uint32_t exact = bmin | bmax | ~fresh;
               need &= ~exact;
               for (uint32_t m = exact; m; m &= m - 1u) {
