@@ -323,18 +323,21 @@ def run_palu(args, w, world, rank, local):
             e1.record(s)
             torch.cuda.synchronize()
             fit_ms = (fit_ms or 0) + e0.elapsed_time(e1)
+        init_ms = None
         for l in range(L):
             pair = []
             for tensor, role, _rr in roles:
                 i = 2 * l + tensor
-                e1, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e1.record(s)
+                e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                e0.record(s)
                 c = P.LatentCache(cfgs[i], role, branks[i], w.batch, w.hkv, cap, fb[i], fm[i], stream=s)
+                e1.record(s)
                 c.append(xs[i], stream=s)
                 e2.record(s)
                 torch.cuda.synchronize()
-                if l == 0:
+                if l == 0:  # the prefill append (the encode) and, apart, the cache's allocation and init
                     enc_ms = (enc_ms or 0) + e1.elapsed_time(e2)
+                    init_ms = (init_ms or 0) + e0.elapsed_time(e1)
                 pair.append(c)
                 xs[i] = None
             caches.append(pair)
@@ -504,7 +507,7 @@ def run_palu(args, w, world, rank, local):
                      "algorithmic_bytes_per_launch": bytes_launch, "avg_launch_us": avg_launch * 1e3,
                      "launches_timed": n_launch},
         "clocks": clk.summary(),
-        "prefill": {"fit_ms_layer0_kv": fit_ms, "encode_ms_layer0_kv": enc_ms,
+        "prefill": {"fit_ms_layer0_kv": fit_ms, "encode_ms_layer0_kv": enc_ms, "cache_init_ms_layer0_kv": init_ms,
                     "fit_ms_all_layers_batched": fit_batch_ms, "fit_batched_tensors": 2 * L,
                     "prefill_tokens_per_layer": w.batch * S},
         "bits": {"effective_bits_k": stats_k["effective_bits"], "effective_bits_v": stats_v["effective_bits"],

@@ -123,6 +123,52 @@ __device__ __noinline__ float exact_latent(const __half* xrow, const float* __re
   return fp_finish(s, lo, m);
 }
 
+// The same latent computed by a whole warp (every lane calls): lane l takes
+// terms 4l..4l+3 as a float pair, then the pairs merge over a butterfly of
+// error-free sums (symmetric, so every lane ends with the same value).
+__device__ __noinline__ float exact_latent_warp(const __half* xrow, const float* __restrict__ brow, float2 m,
+                                                int lane) {
+  const float4 v = __ldg(reinterpret_cast<const float4*>(brow) + lane);
+  const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(xrow + 4 * lane));
+  const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(xrow + 4 * lane + 2));
+  float S = 0.f, E = 0.f;
+  fp_acc(S, E, x01.x, v.x);
+  fp_acc(S, E, x01.y, v.y);
+  fp_acc(S, E, x23.x, v.z);
+  fp_acc(S, E, x23.y, v.w);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float S2 = __shfl_xor_sync(0xffffffffu, S, o), E2 = __shfl_xor_sync(0xffffffffu, E, o);
+    float s, e;
+    two_sum(S, S2, s, e);
+    S = s;
+    E = __fadd_rn(__fadd_rn(E, E2), e);
+  }
+  return fp_finish(S, E, m);
+}
+
+// f(t, j, L) for every (token, channel) entry of a work list of n, with L
+// the entry's exact latent.  Whole warps of entries go one per lane; a short
+// remainder (below 13 entries a warp per entry takes fewer instructions than
+// one more pass of lanes) goes one entry per warp, starting with the warps
+// that have no lane work.
+template <class F>
+__device__ __forceinline__ void run_exact(const uint16_t* work, int n, const __half* xs, const float* __restrict__ bT,
+                                          const float2* __restrict__ mv, F&& f) {
+  const int tid = threadIdx.x, nw = blockDim.x >> 5, warp = tid >> 5, lane = tid & 31;
+  const int rem = (n & 31) < 13 ? (n & 31) : 0, full = n - rem;
+  for (int i = tid; i < full; i += blockDim.x) {
+    const int t = work[i] >> 7, j = work[i] & 127;
+    f(t, j, exact_latent(xs + t * kXsStride, bT + (size_t)j * kHeadDim, mv[j]));
+  }
+  const int w0 = ((full + 31) >> 5) % nw;
+  for (int k = (warp - w0 + nw) % nw; k < rem; k += nw) {
+    const int t = work[full + k] >> 7, j = work[full + k] & 127;
+    const float L = exact_latent_warp(xs + t * kXsStride, bT + (size_t)j * kHeadDim, mv[j], lane);
+    if (lane == 0) f(t, j, L);
+  }
+}
+
 // A float's bits mapped to an unsigned key of the same order (sign bit set
 // for non-negative values, all bits inverted for negative ones; -0 below +0),
 // and back: exact minima and maxima by integer comparisons.
@@ -412,9 +458,10 @@ __global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, con
             const __half za = __float2half_rn(lmin), zb = __float2half_rn(mh);
             const __half sa = __float2half_rn(__fdiv_rn(__fsub_rn(ml, mh), qmax));
             const __half sb = __float2half_rn(__fdiv_rn(__fsub_rn(hmax, lmin), qmax));
-            // (a zero that rounds to +-0 goes the exact way, which orders -0 below +0)
+            // (zeros that round to +-0, and a scale of -0, go the exact way,
+            // which orders -0 below +0)
             certain = __half_as_ushort(za) == __half_as_ushort(zb) && (__half_as_ushort(za) & 0x7fffu) != 0u &&
-                      __half_as_ushort(sa) == __half_as_ushort(sb);
+                      __half_as_ushort(sa) == __half_as_ushort(sb) && __half_as_ushort(sa) != 0x8000u;
             if (certain) {
               sz[j] = __halves2half2(sa, za);
             } else {
@@ -430,11 +477,8 @@ __global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, con
           }
           push_work(work, &n_work[0], (bmin | bmax) & fresh, j, lane);
           __syncthreads();
-          for (int i = tid; i < n_work[0]; i += blockDim.x) {
-            const int tt = work[i] >> 7, jj = work[i] & 127;
-            lat[tt * ld + jj] =
-                exact_latent(xs + tt * kXsStride, bT + (size_t)jj * kHeadDim, cv.mv[(size_t)grp * r + jj]);
-          }
+          run_exact(work, n_work[0], xs, bT, cv.mv + (size_t)grp * r,
+                    [&](int tt, int jj, float L) { lat[tt * ld + jj] = L; });
           __syncthreads();
           uint32_t need = 0u, wmax = 0u;  // wmax: the fp32 bits of this channel's (non-negative) scale
           if (own) {
@@ -490,14 +534,11 @@ __global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, con
             if (m > __ldcg(sm)) atomicMax(sm, m);
             if (m > __ldcg(&cv.hdr->max_scale)) atomicMax(&cv.hdr->max_scale, m);
           }
-          for (int i = tid; i < n_work[1]; i += blockDim.x) {
-            const int tt = work[i] >> 7, jj = work[i] & 127;
-            const float x =
-                exact_latent(xs + tt * kXsStride, bT + (size_t)jj * kHeadDim, cv.mv[(size_t)grp * r + jj]);
+          run_exact(work, n_work[1], xs, bT, cv.mv + (size_t)grp * r, [&](int tt, int jj, float L) {
             const __half2 szj = sz[jj];
-            codes[tt * r + jj] = (uint8_t)quant_code(x, __high2float(szj), __low2float(szj),
-                                                      (float)((1 << (jj < cv.n_hi ? 4 : 2)) - 1));
-          }
+            codes[tt * r + jj] =
+                (uint8_t)quant_code(L, __high2float(szj), __low2float(szj), (float)((1 << (jj < cv.n_hi ? 4 : 2)) - 1));
+          });
         }
         __syncthreads();
         // every byte of the record is written: the code area by the packer, the
