@@ -99,22 +99,66 @@ __device__ __forceinline__ float fp_finish(float S, float E, float2 m) {
   const float low = __fadd_rn(__fsub_rn(E, m.y), ae);
   return __fadd_rn(a, low);
 }
+// Two fp32 lanes in one 64-bit register: the packed f32x2 arithmetic of
+// this architecture (each element rounded to nearest, as the scalar forms).
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk2(float a, float b) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2(f32x2 r, float& a, float& b) { asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r)); }
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// fp_acc on two float pairs at once, with the product carried negated
+// (np = -x v): the same roundings as fp_acc element by element.
+__device__ __forceinline__ void fp_acc2(f32x2& S, f32x2& E, f32x2 x, f32x2 v) {
+  const f32x2 np = mul2(sub2(0ull, x), v);          // -p
+  const f32x2 pe = fma2(x, v, np);                  // x v - p
+  const f32x2 s2 = sub2(S, np);                     // S + p
+  const f32x2 bb = sub2(s2, S);
+  const f32x2 se = sub2(sub2(S, sub2(s2, bb)), add2(np, bb));  // (S - (s2 - bb)) + (p - bb)
+  E = add2(E, add2(se, pe));
+  S = s2;
+}
 // The same sum with four interleaved float pairs (d mod 4) merged by
 // error-free sums at the end: about 48 significant bits like the sequential
 // pair, so its fp32 rounding is the same except when the sum lies within
-// about 2^-48 of a rounding boundary; a quarter of the dependent chain.
+// about 2^-48 of a rounding boundary; a quarter of the dependent chain.  The
+// four pairs advance two at a time in packed registers.
 __device__ __noinline__ float exact_latent(const __half* xrow, const float* __restrict__ brow, float2 m) {
-  float S[4] = {0.f, 0.f, 0.f, 0.f}, E[4] = {0.f, 0.f, 0.f, 0.f};
+  f32x2 S01 = 0ull, E01 = 0ull, S23 = 0ull, E23 = 0ull;
 #pragma unroll 2
   for (int d = 0; d < kHeadDim; d += 4) {
     const float4 v = __ldg(reinterpret_cast<const float4*>(brow + d));
     const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(xrow + d));
     const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(xrow + d + 2));
-    fp_acc(S[0], E[0], x01.x, v.x);
-    fp_acc(S[1], E[1], x01.y, v.y);
-    fp_acc(S[2], E[2], x23.x, v.z);
-    fp_acc(S[3], E[3], x23.y, v.w);
+    fp_acc2(S01, E01, pk2(x01.x, x01.y), pk2(v.x, v.y));
+    fp_acc2(S23, E23, pk2(x23.x, x23.y), pk2(v.z, v.w));
   }
+  float S[4], E[4];
+  upk2(S01, S[0], S[1]);
+  upk2(S23, S[2], S[3]);
+  upk2(E01, E[0], E[1]);
+  upk2(E23, E[2], E[3]);
   float s01, e01, s23, e23, s, e;
   two_sum(S[0], S[1], s01, e01);
   two_sum(S[2], S[3], s23, e23);
