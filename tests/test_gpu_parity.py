@@ -160,6 +160,39 @@ def test_encode_appends_crossing_open_blocks(P):
     check_encode(P, vc, O.ROLE_VALUE, chunks_v)
 
 
+@pytest.mark.parametrize("rank", [9, 33, 74, 128])
+def test_encode_blocks_that_stress_the_bound_decisions(P, rank):
+    """Blocks built so that the encoder's decisions from its error bound go
+    every way: tokens within 1e-4 of the group mean (latents so small that the
+    bound decides neither zero, scale nor most codes: long exact work
+    lists), outlier tokens (decided from the bounds alone), exact duplicate
+    tokens (tied minima and maxima), one token repeated over a block (scale
+    0), the fp16 rounding of the mean repeated, and an ordinary block.  The
+    records must equal the oracle's on the GPU's basis."""
+    rng = np.random.default_rng(700 + rank)
+    B, H, S = 2, 4, 6 * 32
+    base = rand_lowrank(rng, B, H, 256, n_groups=2)
+    cfg = P.palu_config_default(n_head_groups=2, rank=rank)
+    basis, mu, _, _, _ = P.fit(cfg, torch.from_numpy(base).to(DEV))
+    mu_h = mu.cpu().numpy()
+    x = np.empty((B, H, S, 128), np.float32)
+    for h in range(H):
+        m = mu_h[h // 2]
+        blk = [slice(32 * i, 32 * i + 32) for i in range(6)]
+        x[:, h, blk[0]] = m + 1e-4 * rng.standard_normal((B, 32, 128))
+        x[:, h, blk[1]] = m + rng.standard_normal((B, 32, 128)) * np.where(rng.random((B, 32, 1)) < 0.1, 100.0, 1.0)
+        rows = m + rng.standard_normal((B, 8, 128))
+        x[:, h, blk[2]] = rows[:, rng.integers(0, 8, 32)]
+        x[:, h, blk[3]] = (m + rng.standard_normal(128))[None, None, :]
+        x[:, h, blk[4]] = m
+        x[:, h, blk[5]] = base[:, h, :32]
+    x16 = x.astype(np.float16)
+    for role, orole in ((P.PALU_ROLE_KEY, O.ROLE_KEY), (P.PALU_ROLE_VALUE, O.ROLE_VALUE)):
+        c = P.LatentCache(cfg, role, rank, B, H, S + 32, basis, mu)
+        c.append(torch.from_numpy(x16).to(DEV))
+        check_encode(P, c, orole, [x16])
+
+
 @pytest.mark.parametrize("rank", [5, 32, 100])
 def test_encode_fp16_value_latents(P, rank):
     rng = np.random.default_rng(100 + rank)
