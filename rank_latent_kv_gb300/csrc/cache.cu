@@ -256,16 +256,16 @@ __device__ __forceinline__ float quant_code(float v, float z32, float s32, float
 // |L'_tj - L_tj| with margin: each of the eight accumulation steps of a
 // chain adds a few units of 2^-24 of S_tj, the hi/lo split leaves 2^-22 S_tj,
 // and the final roundings a few units of 2^-24 of S_tj + |mu.V_j|.
-// Warp w takes the 8-channel tiles w, w + 4, ... (two at a time); both
-// 16-row tiles.
+// Warp w of nw takes the 8-channel tiles w, w + nw, ... (two at a time);
+// both 16-row tiles.
 __device__ __forceinline__ void project_tc(const __half* xs, const float* __restrict__ bT, float* lat, float* err,
                                            int r, const float2* mv, int off_new) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+  const int tid = threadIdx.x, nw = blockDim.x >> 5, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
   const int n_nt = (r + 7) / 8;
   const uint32_t xbase = smem_addr(xs);
 #pragma unroll 1
-  for (int pass = 0; pass < 2; ++pass) {
-    if (warp + 8 * pass >= n_nt) break;  // uniform
+  for (int pass = 0;; ++pass) {
+    if (warp + 2 * nw * pass >= n_nt) break;  // uniform
     float ah[2][2][4], al[2][2][4], aa[2][2][4];
 #pragma unroll
     for (int i = 0; i < 2; ++i)
@@ -285,7 +285,7 @@ __device__ __forceinline__ void project_tc(const __half* xs, const float* __rest
       }
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
-        const int nt = warp + 8 * pass + 4 * i;
+        const int nt = warp + 2 * nw * pass + nw * i;
         if (nt < n_nt) {  // uniform
           const int j = 8 * nt + g;
           float2 v01 = make_float2(0.f, 0.f), v89 = make_float2(0.f, 0.f);
@@ -311,7 +311,7 @@ __device__ __forceinline__ void project_tc(const __half* xs, const float* __rest
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      const int nt = warp + 8 * pass + 4 * i;
+      const int nt = warp + 2 * nw * pass + nw * i;
       if (nt >= n_nt) continue;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -332,7 +332,9 @@ __device__ __forceinline__ void project_tc(const __half* xs, const float* __rest
   }
 }
 
-// grid (blocks touched, kv_heads, batch), 128 threads.
+// grid (blocks touched, kv_heads, batch), NT threads: 64 for phase 1 of a
+// quantized cache of rank <= 40 (every block takes the tensor-core path and
+// one thread per channel needs no more), else 128.
 // Two launches per append (phase 1, then phase 2 on the same stream): phase 1
 // fills every block the tokens reach except a last, partial one; phase 2
 // writes that partial block (the tail) and publishes the new length.  A
@@ -340,8 +342,10 @@ __device__ __forceinline__ void project_tc(const __half* xs, const float* __rest
 // the tail rows the CTA of the new partial block overwrites.
 // counts (device [batch], or NULL): sequence b appends the first counts[b]
 // of its T rows; NULL appends all T rows of every sequence.
-__global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, const __half* __restrict__ x,
-                                                            long long T, int Hkv, int phase, const int* counts) {
+template <int NT>
+__global__ void __launch_bounds__(NT, NT == 64 ? 12 : 6) encode_append_kernel(CacheView cv, const __half* __restrict__ x,
+                                                                           long long T, int Hkv, int phase,
+                                                                           const int* counts) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int r = cv.r;
   const EncodeSmem L = encode_smem(r, cv.rec_bytes);
@@ -414,7 +418,7 @@ __global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, con
 
     if (tc) {
       project_tc(xs, bT, lat, err, r, cv.mv + (size_t)grp * r, off_new);
-    } else {
+    } else if constexpr (NT == 128) {  // (the host launches 64 threads only where tc holds)
       // projection: warp w takes tokens off_new + w + 4i, lane takes channels lane + 32k.
       // Each (token, channel) latent is sum_d x_d V_dj accumulated as an
       // unevaluated float pair (error-free products and sums), minus mu_g.V_g[:, j],
@@ -478,7 +482,7 @@ __global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, con
           // hold the minimum or maximum.  A code is taken from the bound
           // interval when the whole interval rounds to one code (the
           // quantizer is monotone), else from the exact latent.  One thread
-          // per channel walks the block's 32 tokens (r <= 128 = blockDim.x);
+          // per channel walks the block's 32 tokens (r <= blockDim.x);
           // the exact latents are computed by all threads from shared work
           // lists of (token, channel) pairs.
           const int warp = tid >> 5, lane = tid & 31, j = tid;
@@ -573,7 +577,8 @@ __global__ void __launch_bounds__(128, 6) encode_append_kernel(CacheView cv, con
           // the block's largest scale into the stream's and the cache's maxima:
           // one atomic each per block, and none when the stored value is as large
           if (tid == 0) {
-            const uint32_t m = max(max(wmax_s[0], wmax_s[1]), max(wmax_s[2], wmax_s[3]));
+            uint32_t m = wmax_s[0];
+            for (int w = 1; w < NT / 32; ++w) m = max(m, wmax_s[w]);
             unsigned int* sm = &cv.smax[(long long)b * Hkv + h];
             if (m > __ldcg(sm)) atomicMax(sm, m);
             if (m > __ldcg(&cv.hdr->max_scale)) atomicMax(&cv.hdr->max_scale, m);
@@ -876,6 +881,31 @@ static palu_status check_cache(const palu_cache* c, const char* name) {
   return PALU_OK;
 }
 
+// One phase of an append.  Phase 1 of a quantized cache covers complete
+// blocks only, on the tensor-core path, and launches without the staged-basis
+// area; at rank <= 40 it runs 64-thread CTAs (one thread per channel is
+// enough, at most five channel tiles of the projection fall on each warp, and
+// more CTAs fit an SM).  Measured on rank 33 and 53 keys and values of one
+// layer: 1.32 -> 1.22 ms at rank 33, 1.53 -> 1.99 ms at rank 53.
+static palu_status launch_encode(const palu_cache* cache, const CacheView& cv, const __half* x, int64_t tokens,
+                                 int phase, const int32_t* counts, unsigned nblk, cudaStream_t strm) {
+  const EncodeSmem es = encode_smem(cache->rank, cache->record_bytes);
+  const bool tc = phase == 1 && cache->quantize;
+  const int smem = tc ? es.basis_off : es.total;
+  const bool narrow = tc && cache->rank <= 40;
+  const void* kfn = narrow ? reinterpret_cast<const void*>(encode_append_kernel<64>)
+                           : reinterpret_cast<const void*>(encode_append_kernel<128>);
+  int per_sm = 0;
+  palu_status st = kernel_occupancy(kfn, narrow ? 64 : 128, es.total, &per_sm);
+  if (st != PALU_OK) return st;
+  const dim3 grid(phase == 1 ? nblk : 1u, cache->kv_heads, cache->batch);
+  if (narrow)
+    encode_append_kernel<64><<<grid, 64, smem, strm>>>(cv, x, tokens, cache->kv_heads, phase, counts);
+  else
+    encode_append_kernel<128><<<grid, 128, smem, strm>>>(cv, x, tokens, cache->kv_heads, phase, counts);
+  return cuda_check(cudaGetLastError(), "encode_append_kernel launch");
+}
+
 extern "C" palu_status palu_encode_append(palu_cache* cache, const void* x, int64_t tokens, void* stream) {
   palu_status st = check_cache(cache, "cache");
   if (st != PALU_OK) return st;
@@ -900,18 +930,10 @@ extern "C" palu_status palu_encode_append(palu_cache* cache, const void* x, int6
     cache->length += 1;
     return PALU_OK;
   }
-  const EncodeSmem es = encode_smem(cache->rank, cache->record_bytes);
-  int per_sm = 0;
-  st = kernel_occupancy(reinterpret_cast<const void*>(encode_append_kernel), 128, es.total, &per_sm);
-  if (st != PALU_OK) return st;
   const CacheView cv = make_view(cache);
   for (int phase = 1; phase <= 2; ++phase) {
-    // phase 1 of a quantized cache: complete blocks only, the tensor-core path
-    const int smem = (phase == 1 && cache->quantize) ? es.basis_off : es.total;
-    encode_append_kernel<<<dim3(phase == 1 ? (unsigned)nblk : 1u, cache->kv_heads, cache->batch), 128, smem,
-                           static_cast<cudaStream_t>(stream)>>>(cv, static_cast<const __half*>(x), tokens,
-                                                                cache->kv_heads, phase, nullptr);
-    st = cuda_check(cudaGetLastError(), "encode_append_kernel launch");
+    st = launch_encode(cache, cv, static_cast<const __half*>(x), tokens, phase, nullptr, (unsigned)nblk,
+                       static_cast<cudaStream_t>(stream));
     if (st != PALU_OK) return st;
   }
   cache->length += tokens;
@@ -935,15 +957,8 @@ extern "C" palu_status palu_encode_append_ragged(palu_cache* cache, const void* 
   cache_make_ragged_kernel<<<1, 1, 0, strm>>>(cv.hdr, cv.seq_len, cache->batch);
   st = cuda_check(cudaGetLastError(), "cache_make_ragged_kernel launch");
   if (st != PALU_OK) return st;
-  const EncodeSmem es = encode_smem(cache->rank, cache->record_bytes);
-  int per_sm = 0;
-  st = kernel_occupancy(reinterpret_cast<const void*>(encode_append_kernel), 128, es.total, &per_sm);
-  if (st != PALU_OK) return st;
   for (int phase = 1; phase <= 2; ++phase) {
-    const int smem = (phase == 1 && cache->quantize) ? es.basis_off : es.total;  // as palu_encode_append
-    encode_append_kernel<<<dim3(phase == 1 ? (unsigned)nblk : 1u, cache->kv_heads, cache->batch), 128, smem, strm>>>(
-        cv, static_cast<const __half*>(x), tokens, cache->kv_heads, phase, counts);
-    st = cuda_check(cudaGetLastError(), "encode_append_kernel launch");
+    st = launch_encode(cache, cv, static_cast<const __half*>(x), tokens, phase, counts, (unsigned)nblk, strm);
     if (st != PALU_OK) return st;
   }
   // the host count stays an upper bound of the longest sequence (the counts
