@@ -258,13 +258,15 @@ __device__ __forceinline__ float quant_code(float v, float z32, float s32, float
 // and the final roundings a few units of 2^-24 of S_tj + |mu.V_j|.
 // Warp w of nw takes the 8-channel tiles w, w + nw, ... (two at a time);
 // both 16-row tiles.
+template <int NT>
 __device__ __forceinline__ void project_tc(const __half* xs, const float* __restrict__ bT, float* lat, float* err,
                                            int r, const float2* mv, int off_new) {
-  const int tid = threadIdx.x, nw = blockDim.x >> 5, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+  constexpr int nw = NT / 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
   const int n_nt = (r + 7) / 8;
   const uint32_t xbase = smem_addr(xs);
 #pragma unroll 1
-  for (int pass = 0;; ++pass) {
+  for (int pass = 0; nw < 4 || pass < 2; ++pass) {  // (at most 16 tiles)
     if (warp + 2 * nw * pass >= n_nt) break;  // uniform
     float ah[2][2][4], al[2][2][4], aa[2][2][4];
 #pragma unroll
@@ -417,7 +419,7 @@ __global__ void __launch_bounds__(NT, NT == 64 ? 12 : 6) encode_append_kernel(Ca
     __syncthreads();
 
     if (tc) {
-      project_tc(xs, bT, lat, err, r, cv.mv + (size_t)grp * r, off_new);
+      project_tc<NT>(xs, bT, lat, err, r, cv.mv + (size_t)grp * r, off_new);
     } else if constexpr (NT == 128) {  // (the host launches 64 threads only where tc holds)
       // projection: warp w takes tokens off_new + w + 4i, lane takes channels lane + 32k.
       // Each (token, channel) latent is sum_d x_d V_dj accumulated as an
