@@ -12,14 +12,14 @@
 // port that reconstructs fp16 first; this is the fused form instead).
 //
 // GB300 design:
-//  * Persistent grid (resident CTAs only).  The flat range of full 32-token
-//    blocks over all (batch, KV head) streams is split evenly over the CTAs, so
-//    every SM gets the same number of blocks whatever the batch and head count.
-//    A CTA walks its range stream by stream ("segments"); each of its 8 warps
-//    takes a contiguous share of the segment and streams it through its own
-//    ring of shared-memory stages (2 blocks of key and value records per stage,
-//    two 1-D bulk copies on the TMA engine, mbarrier completion).  The first
-//    stages are in flight before the per-segment prologue (q~ = q V^K) runs.
+//  * Persistent grid (resident CTAs only, one per SM).  The flat range of full
+//    32-token blocks over all (batch, KV head) streams is split evenly over
+//    the warps of the grid (16, 12 or 8 a CTA), so every SM gets the same
+//    number of blocks whatever the batch and head count.  A warp's range
+//    covers at most two streams ("segments"); it streams them through its own
+//    ring of shared-memory stages (2 blocks of key and value records per
+//    stage, two 1-D bulk copies on the TMA engine, mbarrier completion).  The
+//    first stages are in flight before the stream's query factors are read.
 //  * Scores on tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate):
 //    tokens x channels of exact small-integer codes as A, and as B the
 //    query-side factor q~_j * s_bj for the GQA heads (N = 8) in fp16 as a
@@ -48,8 +48,8 @@
 
 namespace palu {
 
-constexpr int kMaxDecWarps = 16;  // warps per decode CTA: 16 (one CTA per SM) or 8; the class
-                                  // kernels (large ranks, many registers) always run 8
+constexpr int kMaxDecWarps = 16;  // warps per decode CTA: 16 (one CTA per SM) for the exact-octet
+                                  // kernels, or 8 when their rings do not fit
 constexpr int kMaxDecThreads = 32 * kMaxDecWarps;
 // the per-class kernels: up to 12 warps (at most 168 registers a thread), or
 // 8 when their rings do not fit
