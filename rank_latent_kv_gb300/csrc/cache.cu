@@ -146,7 +146,7 @@ __device__ __forceinline__ void fp_acc2(f32x2& S, f32x2& E, f32x2 x, f32x2 v) {
 // four pairs advance two at a time in packed registers.
 __device__ __noinline__ float exact_latent(const __half* xrow, const float* __restrict__ brow, float2 m) {
   f32x2 S01 = 0ull, E01 = 0ull, S23 = 0ull, E23 = 0ull;
-#pragma unroll 2
+#pragma unroll 8  // (eight rows' loads in flight: measured 2.75 -> 2.68 ms per layer against unroll 2)
   for (int d = 0; d < kHeadDim; d += 4) {
     const float4 v = __ldg(reinterpret_cast<const float4*>(brow + d));
     const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(xrow + d));
