@@ -509,7 +509,9 @@ def run_palu(args, w, world, rank, local):
         "clocks": clk.summary(),
         "prefill": {"fit_ms_layer0_kv": fit_ms, "encode_ms_layer0_kv": enc_ms, "cache_init_ms_layer0_kv": init_ms,
                     "fit_ms_all_layers_batched": fit_batch_ms, "fit_batched_tensors": 2 * L,
-                    "prefill_tokens_per_layer": w.batch * S},
+                    "prefill_tokens_per_layer": w.batch * S,
+                    # fp16 K and V rows read by the layer's two prefill appends, per second
+                    "encode_gbs_layer0_kv": 2 * w.batch * w.hkv * S * 128 * 2 / (enc_ms * 1e-3) / 1e9 if enc_ms else None},
         "bits": {"effective_bits_k": stats_k["effective_bits"], "effective_bits_v": stats_v["effective_bits"],
                  "assigned_avg_bits": max(stats_k["effective_bits"], stats_v["effective_bits"]),
                  "bits_with_meta_k": stats_k["bits_with_meta"], "bits_with_meta_v": stats_v["bits_with_meta"]},
