@@ -60,7 +60,9 @@ enum {
   PALU_DEVERR_TIMEOUT = 2u,         /* a bounded wait on a copy ran out */
   PALU_DEVERR_LENGTH_MISMATCH = 4u, /* key and value caches differ in length */
   PALU_DEVERR_NOT_CONVERGED = 8u,   /* eigen-solver hit its sweep limit */
-  PALU_DEVERR_ROLLBACK = 16u        /* a per-sequence rollback was refused (that sequence kept its length) */
+  PALU_DEVERR_ROLLBACK = 16u,       /* a per-sequence rollback was refused (that sequence kept its length) */
+  PALU_DEVERR_BOUNDS = 32u          /* bounds-checking build only (PALU_DEBUG_BOUNDS): a kernel found a
+                                       computed block index out of range and skipped that access */
 };
 
 /* Configuration, mirroring the page's KVCacheConfig fields (section "Usage"):

@@ -196,6 +196,7 @@ __device__ __forceinline__ float append_one_token(const CacheView& cv, const __h
   const int pos = (int)(p0 % kBlock);
   const long long blk = p0 / kBlock;
   const long long sidx = (long long)b * Hkv + h;
+  if (!bounds_ok(blk < cv.n_blk_cap, cv.hdr)) return 0.f;  // (bounds-checking build; uniform over the CTA)
   float* lat = sm.lat;
   __shared__ float smax;
   if (tid == 0) smax = 0.f;

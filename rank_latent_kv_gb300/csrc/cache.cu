@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(NT, NT == 64 ? 12 : 6) encode_append_kernel(Ca
   const long long blk = phase == 2 ? p1 / kBlock : p0 / kBlock + blockIdx.x;
   const long long lo = blk * kBlock;
   const bool last_partial = blk == p1 / kBlock && p1 % kBlock != 0;
-  if (!refused && lo < p1 && last_partial == (phase == 2)) {
+  if (!refused && lo < p1 && last_partial == (phase == 2) && bounds_ok(blk < cv.n_blk_cap, cv.hdr)) {
     const long long new_lo = lo > p0 ? lo : p0;
     const long long hi = (lo + kBlock < p1) ? lo + kBlock : p1;
     const int off_new = (int)(new_lo - lo);

@@ -297,4 +297,27 @@ __device__ __forceinline__ void set_dev_error(StateHeader* hdr, unsigned int bit
   if (hdr) atomicOr(&hdr->err, bit);
 }
 
+// The bounds-checking build (compiled with -DPALU_DEBUG_BOUNDS=1, the library
+// libpalu_debug.so): the kernels check the block indices of their streaming
+// global accesses (the decode's record copies, the encode's record writes and
+// its rows of x) against the cache's extents.  A failed check sets
+// PALU_DEVERR_BOUNDS in the cache's error word and the access is skipped or
+// redirected to the cache's first block, so that nothing out of range is
+// touched and every wait still completes.  The default build compiles the
+// checks out: bounds_ok is then constant true.
+#ifndef PALU_DEBUG_BOUNDS
+#define PALU_DEBUG_BOUNDS 0
+#endif
+template <class Header>  // a cache state header with an `unsigned int err` word
+__device__ __forceinline__ bool bounds_ok(bool ok, Header* hdr) {
+#if PALU_DEBUG_BOUNDS
+  if (!ok && hdr) atomicOr(&hdr->err, (unsigned int)PALU_DEVERR_BOUNDS);
+  return ok;
+#else
+  (void)ok;
+  (void)hdr;
+  return true;
+#endif
+}
+
 }  // namespace palu

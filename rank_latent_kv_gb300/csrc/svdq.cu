@@ -289,8 +289,9 @@ __global__ void __launch_bounds__(128) svdq_encode_kernel(SvdqView cv, const __h
       for (int j = tid; j < kept; j += blockDim.x) reinterpret_cast<__half2*>(rec + szo)[j] = sz[j];
       __syncthreads();
       uint8_t* gdst = cv.blocks + (((long long)b * H + h) * cv.n_blk_cap + blk) * cv.rec_bytes;
-      for (int i = tid; i < cv.rec_bytes / 16; i += blockDim.x)
-        reinterpret_cast<uint4*>(gdst)[i] = reinterpret_cast<const uint4*>(rec)[i];
+      if (bounds_ok(blk < cv.n_blk_cap, cv.hdr))  // (bounds-checking build)
+        for (int i = tid; i < cv.rec_bytes / 16; i += blockDim.x)
+          reinterpret_cast<uint4*>(gdst)[i] = reinterpret_cast<const uint4*>(rec)[i];
     } else {
       __syncthreads();
       for (int i = tid; i < n_new * r; i += blockDim.x) {

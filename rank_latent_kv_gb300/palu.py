@@ -26,6 +26,7 @@ PALU_DEVERR_TIMEOUT = 2
 PALU_DEVERR_LENGTH_MISMATCH = 4
 PALU_DEVERR_NOT_CONVERGED = 8
 PALU_DEVERR_ROLLBACK = 16
+PALU_DEVERR_BOUNDS = 32
 STATUS_NAMES = {0: "PALU_OK", 1: "PALU_ERR_INVALID_ARG", 2: "PALU_ERR_UNSUPPORTED", 3: "PALU_ERR_CAPACITY",
                 4: "PALU_ERR_NOT_INITIALIZED", 5: "PALU_ERR_CUDA", 6: "PALU_ERR_DEVICE"}
 
